@@ -1,0 +1,178 @@
+"""CPU oracle for nested 4-bit dequantization: TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product (the CUDA library and its
+Python binding) never imports, links or runs it, and it shares no code with
+the product: the scalar C file ``dq4_oracle.c`` is built here with gcc, and
+``checker.py`` is a second, independent numpy/torch-CPU implementation.
+
+Method: "Fuse nested scale reconstruction into SM103 4-bit dequantization"
+(bitsandbytes issue #21), sections "Proposed experiment" (the two formulas)
+and "Correctness requirements" (separately rounded FP32 multiply and add,
+bitwise identity with the unfused sequence of section "Problem").
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "dq4_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle_dq4.so")
+
+# -ffp-contract=off: the scale's multiply and add must round separately.
+CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
+          "-Wall", "-Wextra"]
+
+OUT_CODES = {"f16": 0, "bf16": 1, "f32": 2}
+OUT_NP = {"f16": np.uint16, "bf16": np.uint16, "f32": np.float32}
+
+_lock = threading.Lock()
+_lib: Optional[ctypes.CDLL] = None
+
+
+def build(force: bool = False, src: str = _SRC, dst: str = _LIB_PATH,
+          extra_flags: Optional[list] = None) -> str:
+    """Compile the C oracle into a shared library (gcc); return its path."""
+    if not force and os.path.exists(dst) and os.path.getmtime(dst) >= os.path.getmtime(src):
+        return dst
+    os.makedirs(os.path.dirname(dst), exist_ok=True)
+    tmp = f"{dst}.{os.getpid()}.tmp"
+    cmd = ["gcc", *CFLAGS, *(extra_flags or []), src, "-o", tmp]
+    subprocess.run(cmd, check=True, capture_output=True, text=True)
+    os.replace(tmp, dst)
+    return dst
+
+
+def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
+    p, i64, f32, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_int
+    lib.oracle_f32_to_f16.argtypes = [f32]
+    lib.oracle_f32_to_f16.restype = ctypes.c_uint16
+    lib.oracle_f32_to_bf16.argtypes = [f32]
+    lib.oracle_f32_to_bf16.restype = ctypes.c_uint16
+    lib.oracle_f32_to_f16_array.argtypes = [p, p, i64]
+    lib.oracle_f32_to_bf16_array.argtypes = [p, p, i64]
+    lib.oracle_convert_bit_range.argtypes = [ctypes.c_uint32, i64, i32, p]
+    lib.oracle_nested_scale.argtypes = [ctypes.c_uint8, f32, p, f32]
+    lib.oracle_nested_scale.restype = f32
+    lib.oracle_dq4_nested.argtypes = [p, p, p, p, p, f32, i64, i64, i64, i32, p]
+    lib.oracle_dq4.argtypes = [p, p, p, i64, i64, i32, p]
+    lib.oracle_nested_scales.argtypes = [p, p, p, f32, i64, i64, p]
+    for name in ("oracle_f32_to_f16_array", "oracle_f32_to_bf16_array",
+                 "oracle_convert_bit_range", "oracle_dq4_nested", "oracle_dq4",
+                 "oracle_nested_scales"):
+        getattr(lib, name).restype = None
+    return lib
+
+
+def load(path: Optional[str] = None) -> ctypes.CDLL:
+    """The oracle library (built on first use)."""
+    global _lib
+    if path is not None:
+        return _bind(ctypes.CDLL(path))
+    with _lock:
+        if _lib is None:
+            _lib = _bind(ctypes.CDLL(build()))
+        return _lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data
+
+
+# ----------------------------------------------------------------- method
+def dq4_nested(problem, out: str = "f16", threads: int = 1, lib=None) -> np.ndarray:
+    """Dequantize ``problem`` (a dq4_inputs.Problem); uint16 bits or float32 values.
+
+    With ``threads > 1`` the flat range is cut at nested-group boundaries
+    (multiples of blocksize * nested_blocksize values) and the same scalar
+    routine runs on each piece in its own thread; the arithmetic is unchanged.
+    """
+    lib = lib or load()
+    p = problem
+    res = np.empty(p.n, dtype=OUT_NP[out])
+    itemsize = res.itemsize
+    unit = p.blocksize * p.nested_blocksize
+    units = -(-p.n // unit)
+    threads = max(1, min(threads, units))
+    bounds = [min(p.n, (units * t // threads) * unit) for t in range(threads + 1)]
+
+    def run(lo, hi):
+        if hi <= lo:
+            return
+        lib.oracle_dq4_nested(
+            _ptr(p.packed) + lo // 2, _ptr(p.scale_codes) + lo // p.blocksize,
+            _ptr(p.nested_absmax) + 4 * (lo // unit), _ptr(p.scale_codebook),
+            _ptr(p.value_codebook), float(p.offset), hi - lo, p.blocksize,
+            p.nested_blocksize, OUT_CODES[out], _ptr(res) + itemsize * lo)
+
+    if threads == 1:
+        run(0, p.n)
+    else:
+        ts = [threading.Thread(target=run, args=(bounds[t], bounds[t + 1]))
+              for t in range(threads)]
+        for t in ts:
+            t.start()
+        for t in ts:
+            t.join()
+    return res
+
+
+def dq4(packed: np.ndarray, absmax: np.ndarray, value_codebook: np.ndarray, n: int,
+        blocksize: int, out: str = "f16", lib=None) -> np.ndarray:
+    """Non-nested dequantization with a given FP32 absmax per block."""
+    lib = lib or load()
+    res = np.empty(n, dtype=OUT_NP[out])
+    lib.oracle_dq4(_ptr(packed), _ptr(absmax), _ptr(value_codebook), n, blocksize,
+                   OUT_CODES[out], _ptr(res))
+    return res
+
+
+def nested_scales(problem, lib=None) -> np.ndarray:
+    """FP32 per-block scales of the unfused sequence (steps 1 and 2)."""
+    lib = lib or load()
+    p = problem
+    res = np.empty(p.nblocks, dtype=np.float32)
+    lib.oracle_nested_scales(_ptr(p.scale_codes), _ptr(p.nested_absmax),
+                             _ptr(p.scale_codebook), float(p.offset), p.nblocks,
+                             p.nested_blocksize, _ptr(res))
+    return res
+
+
+def nested_scale(code: int, absmax: float, scale_codebook: np.ndarray, offset: float,
+                 lib=None) -> np.float32:
+    lib = lib or load()
+    return np.float32(lib.oracle_nested_scale(code, float(np.float32(absmax)),
+                                              _ptr(scale_codebook), float(np.float32(offset))))
+
+
+def f32_to_f16_bits(x: np.ndarray, lib=None) -> np.ndarray:
+    lib = lib or load()
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    y = np.empty(x.shape, dtype=np.uint16)
+    lib.oracle_f32_to_f16_array(_ptr(x), _ptr(y), x.size)
+    return y
+
+
+def f32_to_bf16_bits(x: np.ndarray, lib=None) -> np.ndarray:
+    lib = lib or load()
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    y = np.empty(x.shape, dtype=np.uint16)
+    lib.oracle_f32_to_bf16_array(_ptr(x), _ptr(y), x.size)
+    return y
+
+
+def convert_bit_range(first: int, count: int, to_bf16: bool, lib=None) -> np.ndarray:
+    """Convert every binary32 bit pattern in [first, first+count)."""
+    lib = lib or load()
+    y = np.empty(count, dtype=np.uint16)
+    lib.oracle_convert_bit_range(first, count, int(to_bf16), _ptr(y))
+    return y
