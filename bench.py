@@ -1,0 +1,489 @@
+#!/usr/bin/env python
+"""Benchmark of fused nested 4-bit dequantization on GB300; prints one JSON line.
+
+A step is one fused dequantization (`dq4_nested`, one kernel launch) of the
+28672x8192 NF4-style weight (234,881,024 values; blocksize 64, nested
+blocksize 256, FP16 out) with its inputs resident in HBM.  Metric:
+dequantized elements/s, with effective HBM GB/s (algorithmic bytes / time)
+against the measured GB300 copy bandwidth as the roofline.
+
+Timing (CUDA events on the launching stream; protocol of "Fuse nested scale
+reconstruction into SM103 4-bit dequantization", section "B300 evidence
+plan": warm-ups, >= 7 timed batches, every batch sample with median / p10 /
+p90, unfused sequence timed interleaved as the comparison):
+  * W untimed warm-up steps, then exactly K steps between barrier +
+    synchronize on both sides; the time is the max over ranks.
+  * every step uses the next of 3 rotating buffer sets (1.77 GB in all, each
+    larger than L2), so no step finds the previous step's lines in L2.
+  * nvidia-smi samples SM clocks and throttle reasons during the timed region.
+
+Other legs: `e2e` (the same metric with host buffers: pinned H2D copy of the
+step's inputs, the call, D2H copy of the output, all timed), `cpu_baseline`
+(the CPU oracle on the host cores), and `--impl reference` (the CPU oracle
+as the reference arm).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import dq4_inputs as gen  # noqa: E402
+
+METRIC = "dequantized elements/s and effective HBM GB/s vs GB300 peak (1 GPU)"
+UNIT = "elements/s"
+DEFAULT_CELL = "C4a"
+N_SETS = 3
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SRC = os.path.join(ROOT, "quantized_weight_dequantization_gb300", "csrc", "dq4.cu")
+PROFILES = os.path.join(ROOT, "profiles")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cell", default=DEFAULT_CELL, choices=sorted(gen.CELLS))
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--compare-batches", type=int, default=7)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------ utilities
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_sha256() -> str:
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def traffic_record(cell: str):
+    """ncu DRAM bytes per launch from a committed summary, if it matches this source."""
+    sha = source_sha256()
+    if not os.path.isdir(PROFILES):
+        return None
+    for fn in sorted(os.listdir(PROFILES)):
+        if not fn.endswith((".md", ".txt")):
+            continue
+        with open(os.path.join(PROFILES, fn)) as f:
+            for line in f:
+                m = re.match(r"\s*traffic_record:\s*(\{.*\})\s*$", line)
+                if not m:
+                    continue
+                rec = json.loads(m.group(1))
+                if rec.get("cell") == cell and rec.get("src_sha256") == sha:
+                    return rec
+    return None
+
+
+def pct(xs, q):
+    return float(np.percentile(np.asarray(xs, dtype=np.float64), q))
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.tmp = None
+        self.error = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except OSError as e:
+            self.error = str(e)
+        time.sleep(0.5)
+
+    def stop(self):
+        if self.proc is None:
+            return {"error": self.error or "nvidia-smi not started"}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.tmp.flush()
+        with open(self.tmp.name) as f:
+            rows = [r.split(",") for r in f.read().strip().splitlines() if r.count(",") >= 8]
+        os.unlink(self.tmp.name)
+        if not rows:
+            return {"error": "no nvidia-smi samples"}
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        power = [float(r[3]) for r in rows if re.match(r"^\s*[\d.]+\s*$", r[3])]
+        reasons = sorted({name for r in rows for name, v in zip(self.REASONS, r[5:9])
+                          if v.strip().lower() == "active"})
+        # samples under load: power above the midpoint of the observed range
+        if power and len(power) == len(sm):
+            thr = (min(power) + max(power)) / 2
+            loaded = [s for s, p in zip(sm, power) if p >= thr] or sm
+        else:
+            loaded = sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows), "samples_under_load": len(loaded),
+                "power_w_max": max(power) if power else None}
+
+
+# -------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import quantized_weight_dequantization_gb300 as dq
+
+    rank, world, local = dist_env()
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def max_over_ranks(x: float) -> float:
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    cell = gen.CELLS[args.cell]
+    p = cell.problem()
+    out_dtype = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[cell.out]
+    n = p.n
+    alg_bytes = cell.algorithmic_bytes()
+    host = {k: torch.from_numpy(np.ascontiguousarray(getattr(p, k)))
+            for k in ("packed", "scale_codes", "nested_absmax", "scale_codebook",
+                      "value_codebook")}
+    scb = host["scale_codebook"].to(dev)
+    vcb = host["value_codebook"].to(dev)
+    sets = []
+    for _ in range(N_SETS):
+        sets.append(dict(packed=host["packed"].to(dev), codes=host["scale_codes"].to(dev),
+                         absmax=host["nested_absmax"].to(dev),
+                         out=torch.empty(n, dtype=out_dtype, device=dev),
+                         scratch=torch.empty(p.nblocks, dtype=torch.float32, device=dev)))
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    L = dq.lib
+    code = {torch.float16: dq.OUT_F16, torch.bfloat16: dq.OUT_BF16,
+            torch.float32: dq.OUT_F32}[out_dtype]
+    ptrs = [(s["packed"].data_ptr(), s["codes"].data_ptr(), s["absmax"].data_ptr(),
+             s["out"].data_ptr(), s["scratch"].data_ptr()) for s in sets]
+    off = float(p.offset)
+    bs, nbs = p.blocksize, p.nested_blocksize
+    scb_p, vcb_p = scb.data_ptr(), vcb.data_ptr()
+
+    def fused(i):
+        pk, cd, am, o, _ = ptrs[i % N_SETS]
+        return L.dq4_nested(pk, cd, am, scb_p, vcb_p, off, n, bs, nbs, code, o, sh)
+
+    def unfused(i):
+        pk, cd, am, o, sc = ptrs[i % N_SETS]
+        return L.dq4_nested_unfused(pk, cd, am, scb_p, vcb_p, off, n, bs, nbs, code, o, sc, sh)
+
+    # correctness gate before timing: first and last 64 Ki values of set 0 vs the
+    # unfused sequence (bit-identical by construction)
+    assert fused(0) == 0 and unfused(1) == 0
+    torch.cuda.synchronize(dev)
+    a, b = sets[0]["out"], sets[1]["out"]
+    if not (torch.equal(a[:65536].view(torch.int16 if a.element_size() == 2 else torch.int32),
+                        b[:65536].view(torch.int16 if b.element_size() == 2 else torch.int32))
+            and torch.equal(a[-65536:].view(torch.int16 if a.element_size() == 2 else torch.int32),
+                            b[-65536:].view(torch.int16 if b.element_size() == 2
+                                            else torch.int32))):
+        raise SystemExit("fused and unfused outputs differ; refusing to time")
+
+    # ---- warm-up, then exactly K timed steps
+    K, W = args.steps, args.warmup
+    for i in range(W):
+        if fused(i):
+            raise SystemExit("dq4_nested failed in warm-up")
+    ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    gpu_uuid = None
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        gpu_uuid = u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        pass
+    clocks = ClockSampler(gpu_uuid)
+    clocks.start()
+    torch.cuda.synchronize(dev)
+    barrier()
+    torch.cuda.synchronize(dev)
+    wall0 = time.perf_counter()
+    t_start.record(stream)
+    bad = 0
+    for i in range(K):
+        ev_s[i].record(stream)
+        bad |= fused(W + i)
+        ev_e[i].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    if bad:
+        raise SystemExit(f"dq4_nested returned status {bad} in the timed region")
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end))
+    launch_ms = [ev_s[i].elapsed_time(ev_e[i]) for i in range(K)]
+    avg_launch_ms = float(np.mean(launch_ms))
+    nb = max(7, min(20, K // 50)) if K >= 7 else K
+    edges = np.linspace(0, K, nb + 1).astype(int)
+    batch_ms = [ev_s[edges[j]].elapsed_time(ev_e[edges[j + 1] - 1]) / (edges[j + 1] - edges[j])
+                for j in range(nb) if edges[j + 1] > edges[j]]
+
+    # ---- interleaved fused / unfused comparison (not part of the timed region)
+    cmp_f, cmp_u = [], []
+    per = 200
+    for j in range(args.compare_batches):
+        for fn, acc in ((fused, cmp_f), (unfused, cmp_u)):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for i in range(per):
+                fn(i)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            acc.append(e0.elapsed_time(e1) / per * 1e3)
+
+    # ---- end to end with host buffers (pinned H2D of the inputs, call, D2H of the output)
+    pin = {k: v.pin_memory() for k, v in host.items()}
+    host_out = torch.empty(n, dtype=out_dtype).pin_memory()
+    s0 = sets[0]
+    h2d = sum(v.numel() * v.element_size() for v in pin.values())
+    d2h = host_out.numel() * host_out.element_size()
+    E = max(3, args.e2e_steps)
+
+    def e2e_step():
+        s0["packed"].copy_(pin["packed"], non_blocking=True)
+        s0["codes"].copy_(pin["scale_codes"], non_blocking=True)
+        s0["absmax"].copy_(pin["nested_absmax"], non_blocking=True)
+        scb.copy_(pin["scale_codebook"], non_blocking=True)
+        vcb.copy_(pin["value_codebook"], non_blocking=True)
+        dq.dq4_nested(s0["packed"], s0["codes"], s0["absmax"], scb, vcb, off, n, bs, nbs,
+                      out_dtype, out=s0["out"], stream=stream)
+        host_out.copy_(s0["out"], non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(E):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1))
+    # the copied-back output must equal the device result
+    if not torch.equal(host_out.view(torch.uint8), s0["out"].cpu().view(torch.uint8)):
+        raise SystemExit("e2e output mismatch")
+
+    peak, peak_kind = read_peaks()
+    ms_per_step = elapsed_ms / K
+    value = world * K * n / (elapsed_ms / 1e3)
+    achieved_gbs = alg_bytes / (avg_launch_ms / 1e3) / 1e9
+    rec = traffic_record(args.cell)
+    out = {
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded splitmix64 codes, lognormal nested absmax)",
+        "config": {
+            "workload": f"{cell.rows}x{cell.cols} {cell.fmt.upper()}-style nested 4-bit dequant, "
+                        f"blocksize {cell.blocksize}, nested blocksize {cell.nested_blocksize}, "
+                        f"{cell.out.upper()} out ({cell.name})",
+            "n_values": n, "blocksize": cell.blocksize,
+            "nested_blocksize": cell.nested_blocksize, "format": cell.fmt,
+            "out_dtype": cell.out, "offset": cell.offset,
+            "algorithmic_bytes_per_step": alg_bytes,
+            "l2": f"inputs larger than L2: {alg_bytes / 1e6:.1f} MB per step, {N_SETS} rotating "
+                  "buffer sets",
+            "parallelism": f"replicas x{world}",
+        },
+        "effective_gbs": alg_bytes / (ms_per_step / 1e3) / 1e9,
+        "roofline": {
+            "bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
+            "frac": achieved_gbs / peak,
+            "traffic": rec["bytes_per_launch"] if rec else None,
+            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+            else "fallback 6.8 TB/s",
+            "frac_of_nominal_8tbs": achieved_gbs / 8000.0,
+            "kernel": "dq4_vec_kernel<f16,nested>" if cell.out == "f16"
+            else f"dq4_vec_kernel<{cell.out},nested>",
+            "avg_launch_us": avg_launch_ms * 1e3,
+        },
+        "batches_us_per_step": [round(x * 1e3, 3) for x in batch_ms],
+        "batch_stats_us": {"median": pct(batch_ms, 50) * 1e3, "p10": pct(batch_ms, 10) * 1e3,
+                           "p90": pct(batch_ms, 90) * 1e3},
+        "fused_vs_unfused": {
+            "fused_us": {"median": pct(cmp_f, 50), "p10": pct(cmp_f, 10), "p90": pct(cmp_f, 90),
+                         "samples": [round(x, 3) for x in cmp_f]},
+            "unfused_us": {"median": pct(cmp_u, 50), "p10": pct(cmp_u, 10),
+                           "p90": pct(cmp_u, 90), "samples": [round(x, 3) for x in cmp_u]},
+            "speedup": pct(cmp_u, 50) / pct(cmp_f, 50),
+            "launches": {"fused": 1, "unfused": 3},
+        },
+        "e2e": {"value": world * E * n / (e2e_ms / 1e3), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": E,
+                "ms_per_step": e2e_ms / E},
+        "gpu_launches": K,
+        "clocks": clk,
+        "wall_s_timed": wall,
+        "gpu": torch.cuda.get_device_name(dev),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(p, cell)
+    if world > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+# --------------------------------------------------------- CPU baseline
+def cpu_baseline(p, cell, repeats: int = 3):
+    """The CPU oracle, as it stands, over the whole workload on all host cores."""
+    import oracle
+
+    threads = os.cpu_count() or 1
+    oracle.dq4_nested(gen.make_problem(1 << 16, 64, 256), "f16")  # build + load
+    times = []
+    for _ in range(repeats):
+        t0 = time.perf_counter()
+        oracle.dq4_nested(p, cell.out, threads=threads)
+        times.append(time.perf_counter() - t0)
+    t = statistics.median(times)
+    return {"value": p.n / t, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"the whole {cell.name} workload ({p.n} values), median of {repeats} runs, "
+                      f"{threads} threads over nested-group-aligned chunks",
+            "gbs": cell.algorithmic_bytes() / t / 1e9}
+
+
+# ------------------------------------------------------- reference arm
+def run_reference(args):
+    """The CPU oracle as the reference arm: K steps, each a bounded sample of the workload."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+
+    cell = gen.CELLS[args.cell]
+    p = cell.problem()
+    threads = os.cpu_count() or 1
+    unit = p.blocksize * p.nested_blocksize
+    # calibrate: rate on one nested-group-aligned slice
+    probe = min(p.n, 1 << 22)
+
+    def sub(lo, hi):
+        return gen.Problem(p.packed[lo // 2:(hi + 1) // 2],
+                           p.scale_codes[lo // p.blocksize:-(-hi // p.blocksize)],
+                           p.nested_absmax[lo // unit:-(-hi // unit)], p.scale_codebook,
+                           p.value_codebook, p.offset, hi - lo, p.blocksize, p.nested_blocksize)
+
+    oracle.dq4_nested(sub(0, probe), cell.out, threads=threads)
+    t0 = time.perf_counter()
+    oracle.dq4_nested(sub(0, probe), cell.out, threads=threads)
+    rate = probe / max(time.perf_counter() - t0, 1e-6)
+    budget_s = 60.0
+    K, W = args.steps, args.warmup
+    sample = int(min(p.n, max(unit, budget_s * rate / max(K + W, 1))))
+    sample = max(unit, (sample // unit) * unit)
+    nsub = max(1, p.n // sample)
+    for i in range(W):
+        lo = (i % nsub) * sample
+        oracle.dq4_nested(sub(lo, min(p.n, lo + sample)), cell.out, threads=threads)
+    done = 0
+    t0 = time.perf_counter()
+    for i in range(K):
+        lo = (i % nsub) * sample
+        hi = min(p.n, lo + sample)
+        oracle.dq4_nested(sub(lo, hi), cell.out, threads=threads)
+        done += hi - lo
+    el = time.perf_counter() - t0
+    value = done / el
+    desc = (f"{sample} consecutive values of {cell.name} per step (of {p.n}), "
+            f"{threads} threads over nested-group-aligned chunks")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": el / K * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded splitmix64 codes, lognormal nested absmax)",
+        "config": {"workload": f"{cell.rows}x{cell.cols} {cell.fmt.upper()}-style nested 4-bit "
+                               f"dequant, blocksize {cell.blocksize}, nested blocksize "
+                               f"{cell.nested_blocksize}, {cell.out.upper()} out ({cell.name})",
+                   "n_values": p.n},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

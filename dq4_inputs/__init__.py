@@ -38,19 +38,28 @@ def _mix(z: np.ndarray) -> np.ndarray:
     return z ^ (z >> np.uint64(31))
 
 
-def splitmix64(seed: int, stream: int, count: int) -> np.ndarray:
-    """``count`` uint64 words of the splitmix64 sequence for (seed, stream)."""
+def splitmix64(seed: int, stream: int, count: int, start: int = 0) -> np.ndarray:
+    """Words ``start .. start+count-1`` of the splitmix64 sequence for (seed, stream)."""
     with np.errstate(over="ignore"):
         base = _mix(np.array([(seed * 0x100000001B3 + stream) & 0xFFFFFFFFFFFFFFFF],
                              dtype=np.uint64))[0]
-        k = np.arange(1, count + 1, dtype=np.uint64)
+        k = np.arange(start + 1, start + count + 1, dtype=np.uint64)
         return _mix(base + k * GOLDEN)
 
 
-def uniform_bytes(seed: int, stream: int, nbytes: int) -> np.ndarray:
-    """``nbytes`` uniform random bytes (the little-endian bytes of the words)."""
-    words = splitmix64(seed, stream, (nbytes + 7) // 8)
-    return words.view(np.uint8)[:nbytes].copy()
+def uniform_bytes(seed: int, stream: int, nbytes: int, chunk_words: int = 1 << 24) -> np.ndarray:
+    """``nbytes`` uniform random bytes (the little-endian bytes of the words).
+
+    Generated in chunks of ``chunk_words`` words so that huge buffers need
+    little memory beyond the result itself; the bytes do not depend on it.
+    """
+    nwords = (nbytes + 7) // 8
+    res = np.empty(nwords * 8, dtype=np.uint8)
+    words = res.view(np.uint64)
+    for lo in range(0, nwords, chunk_words):
+        hi = min(nwords, lo + chunk_words)
+        words[lo:hi] = splitmix64(seed, stream, hi - lo, start=lo)
+    return res[:nbytes]
 
 
 def uniform_open01(words: np.ndarray) -> np.ndarray:

@@ -1,0 +1,132 @@
+/*
+ * dq4 — blockwise 4-bit weight dequantization with nested (double-quantized)
+ * scales, fused into one pass, for NVIDIA GB300 (compute capability 10.3).
+ *
+ * The operation ("Fuse nested scale reconstruction into SM103 4-bit
+ * dequantization", bitsandbytes issue #21, sections "Problem", "Proposed
+ * experiment" and "Correctness requirements"):
+ *
+ *   for i in [0, n):
+ *     nib   = high nibble of packed[i/2] if i is even, else its low nibble
+ *     b     = i / blocksize                  (outer block: one scale code)
+ *     g     = b / nested_blocksize           (nested group of scale codes)
+ *     scale = RN32( RN32(scale_codebook[scale_codes[b]] * nested_absmax[g]) + offset )
+ *     v     = RN32( value_codebook[nib] * scale )
+ *     out[i] = RN_out(v)          (IEEE round-to-nearest-even; FP32 stores v)
+ *
+ * The FP32 multiply and add of the scale are rounded separately (never a
+ * fused multiply-add) so that the result is bit-identical to the unfused
+ * sequence "dequantize scale codes to FP32, add the offset, dequantize the
+ * values" of section "Problem".  No FP32 scale tensor is materialised by
+ * dq4_nested.  Subnormals are kept (no flush to zero); FP16 overflow gives
+ * +-infinity.  Every output bit is deterministic.
+ *
+ * Conventions shared by every entry point
+ *  - All array pointers are DEVICE pointers (global memory of the current
+ *    device), owned by the caller.  The library never allocates, frees or
+ *    synchronizes; inputs are never modified.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  Work is enqueued on it and the call returns immediately;
+ *    ordering with other work on that stream is the stream's order.
+ *  - The return value is a status code (DQ4_OK = 0 means enqueued).  On any
+ *    error nothing has been enqueued, except DQ4_ERR_LAUNCH, which reports
+ *    the CUDA runtime's error right after a launch (dq4_last_cuda_error()
+ *    gives the cudaError_t).
+ *  - n == 0 is a successful no-op (pointers may then be NULL).
+ *  - blocksize: a power of two in [32, 4096].  nested_blocksize: a power of
+ *    two >= 1 (256 is the standard nested layout).
+ *  - Alignment: float arrays 4-byte aligned; `out` aligned to its element
+ *    size.  Fastest path: `packed` 4-byte aligned and `out` 16-byte aligned
+ *    (any cudaMalloc / PyTorch allocation is); other alignments run a
+ *    per-element path with the same results.
+ *  - Calls from several host threads are safe; the library keeps only a
+ *    per-device cache of device properties.
+ */
+#ifndef DQ4_H
+#define DQ4_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Output element types (out_dtype). */
+#define DQ4_OUT_F16 0  /* IEEE binary16, 2 bytes per value */
+#define DQ4_OUT_BF16 1 /* bfloat16, 2 bytes per value */
+#define DQ4_OUT_F32 2  /* IEEE binary32, 4 bytes per value */
+
+/* Status codes. */
+#define DQ4_OK 0
+#define DQ4_ERR_NULL 1             /* a required pointer is NULL while n > 0 */
+#define DQ4_ERR_N 2                /* n < 0 */
+#define DQ4_ERR_BLOCKSIZE 3        /* blocksize not a power of two in [32, 4096] */
+#define DQ4_ERR_NESTED_BLOCKSIZE 4 /* nested_blocksize not a power of two >= 1 */
+#define DQ4_ERR_DTYPE 5            /* out_dtype not one of DQ4_OUT_* */
+#define DQ4_ERR_ALIGN 6            /* a float array or `out` misaligned for its type */
+#define DQ4_ERR_DEVICE 7           /* no current CUDA device could be queried */
+#define DQ4_ERR_ARCH 8             /* current device is not compute capability 10.3 */
+#define DQ4_ERR_LAUNCH 9           /* the CUDA runtime reported an error at launch */
+
+/* Version of this interface (incremented on any change of a signature). */
+int dq4_abi_version(void);
+
+/*
+ * Fused nested dequantization: one kernel launch.
+ *   packed           uint8[ceil(n/2)]  two 4-bit codes per byte, even index in the
+ *                                      high nibble; for odd n the low nibble of the
+ *                                      last byte is padding and is ignored
+ *   scale_codes      uint8[NB]         NB = ceil(n / blocksize), one code per block
+ *   nested_absmax    float[NG]         NG = ceil(NB / nested_blocksize)
+ *   scale_codebook   float[256]        decodes a scale code
+ *   value_codebook   float[16]         decodes a 4-bit code (decode_4bit)
+ *   offset           scalar FP32 added to every rebuilt scale
+ *   n                number of values
+ *   out_dtype        DQ4_OUT_F16 / DQ4_OUT_BF16 / DQ4_OUT_F32
+ *   out              n elements of out_dtype, flat (the weight's row-major order)
+ * Formula: issue #21, section "Proposed experiment"; rounding: section
+ * "Correctness requirements".
+ */
+int dq4_nested(const uint8_t* packed, const uint8_t* scale_codes, const float* nested_absmax,
+               const float* scale_codebook, const float* value_codebook, float offset,
+               int64_t n, int32_t blocksize, int32_t nested_blocksize, int32_t out_dtype,
+               void* out, void* stream);
+
+/*
+ * Non-nested dequantization (a plain FP32 absmax per block): one launch.
+ *   out[i] = RN_out( RN32( value_codebook[nib_i] * absmax[i / blocksize] ) )
+ * absmax is float[ceil(n / blocksize)].  This is the third step of the
+ * unfused sequence (issue #21, section "Problem", step 3) and the non-nested
+ * state of section "Proposed experiment".
+ */
+int dq4(const uint8_t* packed, const float* absmax, const float* value_codebook, int64_t n,
+        int32_t blocksize, int32_t out_dtype, void* out, void* stream);
+
+/*
+ * The unfused sequence of issue #21, section "Problem", as three launches on
+ * `stream`, kept for comparison with the fused kernel:
+ *   1. scale_scratch[b] = RN32(scale_codebook[scale_codes[b]] * nested_absmax[g])
+ *   2. scale_scratch[b] = RN32(scale_scratch[b] + offset)
+ *   3. dq4(packed, scale_scratch, ...)
+ * scale_scratch is a caller-owned device float[ceil(n / blocksize)], fully
+ * overwritten; it holds the FP32 scales afterwards.  The output is
+ * bit-identical to dq4_nested.
+ */
+int dq4_nested_unfused(const uint8_t* packed, const uint8_t* scale_codes,
+                       const float* nested_absmax, const float* scale_codebook,
+                       const float* value_codebook, float offset, int64_t n,
+                       int32_t blocksize, int32_t nested_blocksize, int32_t out_dtype,
+                       void* out, float* scale_scratch, void* stream);
+
+/* A static, human-readable string for a status code (never NULL). */
+const char* dq4_status_string(int status);
+
+/* The cudaError_t behind the last DQ4_ERR_LAUNCH / DQ4_ERR_DEVICE /
+ * DQ4_ERR_ARCH returned on the calling thread (0 if none). */
+int dq4_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DQ4_H */

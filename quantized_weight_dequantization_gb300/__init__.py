@@ -1,0 +1,21 @@
+"""Fused nested 4-bit weight dequantization for NVIDIA GB300 (sm_103a).
+
+The computation lives in the CUDA library ``libdq4.so`` (C ABI in
+``include/dq4.h``); this package is its thin Python binding.  Importing it
+raises if the library has not been built: there is no CPU fallback.
+"""
+
+from ._binding import (  # noqa: F401
+    OUT_BF16,
+    OUT_F16,
+    OUT_F32,
+    Dq4Error,
+    dq4,
+    dq4_nested,
+    dq4_nested_unfused,
+    lib,
+    sizes,
+)
+
+__all__ = ["dq4_nested", "dq4", "dq4_nested_unfused", "Dq4Error", "lib", "sizes",
+           "OUT_F16", "OUT_BF16", "OUT_F32"]

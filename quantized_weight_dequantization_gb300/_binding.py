@@ -1,0 +1,187 @@
+"""ctypes binding of libdq4 (include/dq4.h): argument marshalling only.
+
+Every step of the computation runs in the CUDA library.  PyTorch is used for
+device memory and streams; there is no CPU path and no fallback: if the
+library is missing, importing this module raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from .build import LIB_PATH
+
+OUT_F16, OUT_BF16, OUT_F32 = 0, 1, 2
+_DTYPE_CODE = {torch.float16: OUT_F16, torch.bfloat16: OUT_BF16, torch.float32: OUT_F32}
+_CODE_DTYPE = {v: k for k, v in _DTYPE_CODE.items()}
+
+STATUS_NAMES = {
+    0: "DQ4_OK", 1: "DQ4_ERR_NULL", 2: "DQ4_ERR_N", 3: "DQ4_ERR_BLOCKSIZE",
+    4: "DQ4_ERR_NESTED_BLOCKSIZE", 5: "DQ4_ERR_DTYPE", 6: "DQ4_ERR_ALIGN",
+    7: "DQ4_ERR_DEVICE", 8: "DQ4_ERR_ARCH", 9: "DQ4_ERR_LAUNCH",
+}
+
+
+class Dq4Error(RuntimeError):
+    """A nonzero status from the library."""
+
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = lib.dq4_status_string(status).decode()
+        extra = ""
+        if status in (7, 8, 9):
+            extra = f" (cudaError_t {lib.dq4_last_cuda_error()})"
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}: {msg}{extra}")
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"libdq4.so is not built ({LIB_PATH}); build it with "
+            "quantized_weight_dequantization_gb300.build.build()")
+    L = ctypes.CDLL(LIB_PATH)
+    p, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float
+    L.dq4_abi_version.argtypes = []
+    L.dq4_abi_version.restype = ctypes.c_int
+    L.dq4_nested.argtypes = [p, p, p, p, p, f32, i64, i32, i32, i32, p, p]
+    L.dq4_nested.restype = ctypes.c_int
+    L.dq4.argtypes = [p, p, p, i64, i32, i32, p, p]
+    L.dq4.restype = ctypes.c_int
+    L.dq4_nested_unfused.argtypes = [p, p, p, p, p, f32, i64, i32, i32, i32, p, p, p]
+    L.dq4_nested_unfused.restype = ctypes.c_int
+    L.dq4_status_string.argtypes = [ctypes.c_int]
+    L.dq4_status_string.restype = ctypes.c_char_p
+    L.dq4_last_cuda_error.argtypes = []
+    L.dq4_last_cuda_error.restype = ctypes.c_int
+    return L
+
+
+lib = _load()
+
+
+# ------------------------------------------------------------- helpers
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _check(t: torch.Tensor, name: str, dtype: torch.dtype, numel: int, device) -> None:
+    if t.device.type != "cuda":
+        raise ValueError(f"{name}: must be a CUDA tensor (the library reads device memory)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if t.device != device:
+        raise ValueError(f"{name}: expected a tensor on {device}, got {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if t.numel() < numel:
+        raise ValueError(f"{name}: needs at least {numel} elements, has {t.numel()}")
+
+
+def _stream_handle(stream, device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _out_tensor(out, out_dtype, n, device):
+    if out is None:
+        return torch.empty(n, dtype=out_dtype, device=device)
+    if out.dtype not in _DTYPE_CODE:
+        raise TypeError(f"out: unsupported dtype {out.dtype}")
+    _check(out, "out", out.dtype, n, device)
+    return out
+
+
+def sizes(n: int, blocksize: int, nested_blocksize: int = 1):
+    """(packed bytes, NB outer blocks, NG nested groups) of a problem of n values."""
+    nb = -(-n // blocksize)
+    return (n + 1) // 2, nb, -(-nb // nested_blocksize)
+
+
+# ------------------------------------------------------------- the API
+def dq4_nested(packed: torch.Tensor, scale_codes: torch.Tensor, nested_absmax: torch.Tensor,
+               scale_codebook: torch.Tensor, value_codebook: torch.Tensor, offset: float,
+               n: int, blocksize: int = 64, nested_blocksize: int = 256,
+               out_dtype: torch.dtype = torch.float16, out: Optional[torch.Tensor] = None,
+               stream=None) -> torch.Tensor:
+    """Fused nested 4-bit dequantization (one launch); returns ``out`` (allocated if None).
+
+    Issue #21 "Fuse nested scale reconstruction into SM103 4-bit
+    dequantization", section "Proposed experiment".  All tensors live on one
+    CUDA device; the call is asynchronous on ``stream`` (default: current).
+    """
+    device = packed.device
+    npk, nb, ng = sizes(n, blocksize, nested_blocksize)
+    _check(packed, "packed", torch.uint8, npk, device)
+    _check(scale_codes, "scale_codes", torch.uint8, nb, device)
+    _check(nested_absmax, "nested_absmax", torch.float32, ng, device)
+    _check(scale_codebook, "scale_codebook", torch.float32, 256, device)
+    _check(value_codebook, "value_codebook", torch.float32, 16, device)
+    if out is not None:
+        out_dtype = out.dtype
+    if out_dtype not in _DTYPE_CODE:
+        raise TypeError(f"out_dtype: unsupported {out_dtype}")
+    res = _out_tensor(out, out_dtype, n, device)
+    st = lib.dq4_nested(_ptr(packed), _ptr(scale_codes), _ptr(nested_absmax),
+                        _ptr(scale_codebook), _ptr(value_codebook), float(offset), n,
+                        blocksize, nested_blocksize, _DTYPE_CODE[out_dtype], _ptr(res),
+                        _stream_handle(stream, device))
+    if st:
+        raise Dq4Error(st, "dq4_nested")
+    return res
+
+
+def dq4(packed: torch.Tensor, absmax: torch.Tensor, value_codebook: torch.Tensor, n: int,
+        blocksize: int = 64, out_dtype: torch.dtype = torch.float16,
+        out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Non-nested 4-bit dequantization with an FP32 absmax per block (one launch)."""
+    device = packed.device
+    npk, nb, _ = sizes(n, blocksize)
+    _check(packed, "packed", torch.uint8, npk, device)
+    _check(absmax, "absmax", torch.float32, nb, device)
+    _check(value_codebook, "value_codebook", torch.float32, 16, device)
+    if out is not None:
+        out_dtype = out.dtype
+    if out_dtype not in _DTYPE_CODE:
+        raise TypeError(f"out_dtype: unsupported {out_dtype}")
+    res = _out_tensor(out, out_dtype, n, device)
+    st = lib.dq4(_ptr(packed), _ptr(absmax), _ptr(value_codebook), n, blocksize,
+                 _DTYPE_CODE[out_dtype], _ptr(res), _stream_handle(stream, device))
+    if st:
+        raise Dq4Error(st, "dq4")
+    return res
+
+
+def dq4_nested_unfused(packed: torch.Tensor, scale_codes: torch.Tensor,
+                       nested_absmax: torch.Tensor, scale_codebook: torch.Tensor,
+                       value_codebook: torch.Tensor, offset: float, n: int, blocksize: int = 64,
+                       nested_blocksize: int = 256, out_dtype: torch.dtype = torch.float16,
+                       out: Optional[torch.Tensor] = None,
+                       scale_scratch: Optional[torch.Tensor] = None, stream=None):
+    """The unfused three-launch sequence; returns (out, scale_scratch)."""
+    device = packed.device
+    npk, nb, ng = sizes(n, blocksize, nested_blocksize)
+    _check(packed, "packed", torch.uint8, npk, device)
+    _check(scale_codes, "scale_codes", torch.uint8, nb, device)
+    _check(nested_absmax, "nested_absmax", torch.float32, ng, device)
+    _check(scale_codebook, "scale_codebook", torch.float32, 256, device)
+    _check(value_codebook, "value_codebook", torch.float32, 16, device)
+    if out is not None:
+        out_dtype = out.dtype
+    if out_dtype not in _DTYPE_CODE:
+        raise TypeError(f"out_dtype: unsupported {out_dtype}")
+    res = _out_tensor(out, out_dtype, n, device)
+    if scale_scratch is None:
+        scale_scratch = torch.empty(max(nb, 1), dtype=torch.float32, device=device)
+    _check(scale_scratch, "scale_scratch", torch.float32, nb, device)
+    st = lib.dq4_nested_unfused(_ptr(packed), _ptr(scale_codes), _ptr(nested_absmax),
+                                _ptr(scale_codebook), _ptr(value_codebook), float(offset), n,
+                                blocksize, nested_blocksize, _DTYPE_CODE[out_dtype], _ptr(res),
+                                _ptr(scale_scratch), _stream_handle(stream, device))
+    if st:
+        raise Dq4Error(st, "dq4_nested_unfused")
+    return res, scale_scratch

@@ -1,0 +1,470 @@
+// Blockwise 4-bit dequantization with nested (double-quantized) scales for
+// GB300 (sm_103a): the kernels and the C-ABI entry points declared in
+// include/dq4.h.
+//
+// Operation: "Fuse nested scale reconstruction into SM103 4-bit
+// dequantization" (bitsandbytes issue #21), section "Proposed experiment":
+//   scale = scale_codebook[scale_code] * nested_absmax[nested_group] + offset
+//   value = decode_4bit(packed_value) * scale
+// with the multiply and the add of the scale rounded separately (section
+// "Correctness requirements").  __fmul_rn / __fadd_rn are never contracted
+// into an FMA, and the library is also compiled with -fmad=false.
+//
+// Design (a streaming, HBM-bound map; no tensor cores):
+//  * A warp owns a tile of 32*U consecutive "words".  A word is the packed
+//    data of 16 output bytes: 8 values (4 packed bytes) for FP16/BF16
+//    output, 4 values (2 packed bytes) for FP32.  Lane l handles words
+//    tile + 32k + l, so each packed load and each 16-byte output store of a
+//    warp covers one contiguous, fully used span.
+//  * blocksize >= 32 is a power of two, so a word never straddles two outer
+//    blocks.  Each lane rebuilds at most one scale per tile (the tile's
+//    blocks are consecutive) and the words fetch theirs with a warp shuffle:
+//    one scale code, one nested absmax and one codebook lookup per block,
+//    never an FP32 scale array.
+//  * The 16-entry value codebook sits in shared memory (banks 0..15, so the
+//    data-dependent lookups of a warp never conflict); the 256-entry scale
+//    codebook too.
+//  * Packed loads and output stores use the streaming (evict-first) cache
+//    hint: every byte is touched once.
+//  * Values after the last whole word (fewer than one word, including an
+//    odd padding nibble) are written one by one by CTA 0.  Unaligned
+//    `packed` / `out` pointers take a per-value kernel with the same math.
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+
+#include "dq4.h"
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarpsPerCta = kThreads / 32;
+constexpr int kMaxDevices = 64;
+constexpr int kAbiVersion = 1;
+
+thread_local int t_last_cuda_error = 0;
+
+// ------------------------------------------------------------------ args
+struct Args {
+  const uint8_t* packed;
+  const uint8_t* codes;   // scale codes (nested form only)
+  const float* absmax;    // nested absmax (nested form) or per-block absmax
+  const float* scb;       // scale codebook (nested form only)
+  const float* vcb;       // value codebook
+  void* out;
+  int64_t n;
+  int64_t nblocks;
+  float offset;
+  int log2_bs;
+  int log2_nbs;
+};
+
+template <int OUT>
+struct Traits;
+template <>
+struct Traits<DQ4_OUT_F16> {
+  using Word = uint32_t;
+  static constexpr int kLog2Vals = 3;
+};
+template <>
+struct Traits<DQ4_OUT_BF16> {
+  using Word = uint32_t;
+  static constexpr int kLog2Vals = 3;
+};
+template <>
+struct Traits<DQ4_OUT_F32> {
+  using Word = uint16_t;
+  static constexpr int kLog2Vals = 2;
+};
+
+// Words per warp tile.  Tiles of at most 32 outer blocks keep "one scale
+// per lane" exact: 32*U words >> log2(words per block) <= 32 for every
+// blocksize >= 32.
+template <int OUT>
+struct Tile {
+  static constexpr int U = (OUT == DQ4_OUT_F32) ? 8 : 4;
+};
+
+// ------------------------------------------------------------- device math
+__device__ __forceinline__ float nested_scale(const Args& a, const float* s_scb, int64_t b) {
+  const float A = __ldg(a.absmax + (b >> a.log2_nbs));
+  const float c = s_scb[__ldg(a.codes + b)];
+  return __fadd_rn(__fmul_rn(c, A), a.offset);  // two roundings, never an FMA
+}
+
+template <bool NESTED>
+__device__ __forceinline__ float block_scale(const Args& a, const float* s_scb, int64_t b) {
+  if constexpr (NESTED) {
+    return nested_scale(a, s_scb, b);
+  } else {
+    return __ldg(a.absmax + b);
+  }
+}
+
+template <int OUT>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  uint32_t u;
+  if constexpr (OUT == DQ4_OUT_F16) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    memcpy(&u, &h, sizeof u);
+  } else {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    memcpy(&u, &h, sizeof u);
+  }
+  return u;
+}
+
+// 16 output bytes from one packed word and its block's scale.
+template <int OUT>
+__device__ __forceinline__ uint4 decode_word(typename Traits<OUT>::Word w, float s,
+                                             const float* vcb) {
+  uint32_t r[4];
+  if constexpr (OUT == DQ4_OUT_F32) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {  // byte j -> values 2j (high nibble), 2j+1 (low)
+      const uint32_t byte = (uint32_t(w) >> (8 * j)) & 0xFFu;
+      r[2 * j] = __float_as_uint(__fmul_rn(vcb[byte >> 4], s));
+      r[2 * j + 1] = __float_as_uint(__fmul_rn(vcb[byte & 0xFu], s));
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t byte = (w >> (8 * j)) & 0xFFu;
+      r[j] = pack2<OUT>(__fmul_rn(vcb[byte >> 4], s), __fmul_rn(vcb[byte & 0xFu], s));
+    }
+  }
+  return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
+template <bool NESTED>
+__device__ __forceinline__ float value_at(const Args& a, const float* s_scb, const float* s_vcb,
+                                          int64_t i) {
+  const uint32_t byte = a.packed[i >> 1];
+  const uint32_t nib = (i & 1) ? (byte & 0xFu) : (byte >> 4);
+  return __fmul_rn(s_vcb[nib], block_scale<NESTED>(a, s_scb, i >> a.log2_bs));
+}
+
+template <int OUT>
+__device__ __forceinline__ void store_one(void* out, int64_t i, float v) {
+  if constexpr (OUT == DQ4_OUT_F16) {
+    static_cast<__half*>(out)[i] = __float2half_rn(v);
+  } else if constexpr (OUT == DQ4_OUT_BF16) {
+    static_cast<__nv_bfloat16*>(out)[i] = __float2bfloat16_rn(v);
+  } else {
+    static_cast<float*>(out)[i] = v;
+  }
+}
+
+template <bool NESTED>
+__device__ __forceinline__ void stage_codebooks(const Args& a, float* s_vcb, float* s_scb) {
+  if (threadIdx.x < 16) s_vcb[threadIdx.x] = __ldg(a.vcb + threadIdx.x);
+  if constexpr (NESTED) {
+    for (int k = threadIdx.x; k < 256; k += blockDim.x) s_scb[k] = __ldg(a.scb + k);
+  }
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------- kernels
+template <int OUT, bool NESTED>
+__global__ void __launch_bounds__(kThreads) dq4_vec_kernel(const Args a) {
+  using T = Traits<OUT>;
+  using Word = typename T::Word;
+  constexpr int U = Tile<OUT>::U;
+  constexpr int64_t kTile = 32 * U;
+  __shared__ float s_vcb[16];
+  __shared__ float s_scb[NESTED ? 256 : 1];
+  stage_codebooks<NESTED>(a, s_vcb, s_scb);
+
+  const Word* pw = reinterpret_cast<const Word*>(a.packed);
+  uint4* po = reinterpret_cast<uint4*>(a.out);
+  const int64_t n_words = a.n >> T::kLog2Vals;
+  const int wshift = a.log2_bs - T::kLog2Vals;  // log2(words per outer block)
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (int64_t(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+  const int64_t n_warps = (int64_t(gridDim.x) * kThreads) >> 5;
+
+  for (int64_t base = warp * kTile; base < n_words; base += n_warps * kTile) {
+    Word w[U];
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+      const int64_t wi = base + k * 32 + lane;
+      w[k] = wi < n_words ? __ldcs(pw + wi) : Word(0);
+    }
+    // lane j rebuilds the scale of the tile's j-th block
+    const int64_t b0 = base >> wshift;
+    const int64_t b_last = ((base + kTile < n_words ? base + kTile : n_words) - 1) >> wshift;
+    const float my_scale = (b0 + lane <= b_last) ? block_scale<NESTED>(a, s_scb, b0 + lane) : 0.f;
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+      const int64_t wi = base + k * 32 + lane;
+      const float s = __shfl_sync(0xffffffffu, my_scale, int((wi >> wshift) - b0));
+      if (wi < n_words) __stcs(po + wi, decode_word<OUT>(w[k], s, s_vcb));
+    }
+  }
+
+  // fewer than one word of values remains after the last whole word
+  const int64_t tail0 = n_words << T::kLog2Vals;
+  if (blockIdx.x == 0 && tail0 + threadIdx.x < a.n) {
+    const int64_t i = tail0 + threadIdx.x;
+    store_one<OUT>(a.out, i, value_at<NESTED>(a, s_scb, s_vcb, i));
+  }
+}
+
+template <int OUT, bool NESTED>
+__global__ void __launch_bounds__(kThreads) dq4_scalar_kernel(const Args a) {
+  __shared__ float s_vcb[16];
+  __shared__ float s_scb[NESTED ? 256 : 1];
+  stage_codebooks<NESTED>(a, s_vcb, s_scb);
+  const int64_t stride = int64_t(gridDim.x) * kThreads;
+  for (int64_t i = int64_t(blockIdx.x) * kThreads + threadIdx.x; i < a.n; i += stride)
+    store_one<OUT>(a.out, i, value_at<NESTED>(a, s_scb, s_vcb, i));
+}
+
+// Unfused step 1: FP32 scale buffer from the codes (no offset yet).
+__global__ void __launch_bounds__(kThreads)
+    scale_codes_kernel(const uint8_t* codes, const float* nested_absmax, const float* scb,
+                       int64_t nblocks, int log2_nbs, float* scales) {
+  const int64_t stride = int64_t(gridDim.x) * kThreads;
+  for (int64_t b = int64_t(blockIdx.x) * kThreads + threadIdx.x; b < nblocks; b += stride)
+    scales[b] = __fmul_rn(__ldg(scb + __ldg(codes + b)), __ldg(nested_absmax + (b >> log2_nbs)));
+}
+
+// Unfused step 2: the offset as a separate elementwise pass.
+__global__ void __launch_bounds__(kThreads)
+    add_offset_kernel(float* scales, int64_t nblocks, float offset) {
+  const int64_t stride = int64_t(gridDim.x) * kThreads;
+  for (int64_t b = int64_t(blockIdx.x) * kThreads + threadIdx.x; b < nblocks; b += stride)
+    scales[b] = __fadd_rn(scales[b], offset);
+}
+
+// ------------------------------------------------------------- host side
+struct DeviceCache {
+  std::atomic<int> sms{0};
+  std::atomic<int> cc{0};
+};
+DeviceCache g_devices[kMaxDevices];
+
+int fail_cuda(int status, cudaError_t e) {
+  t_last_cuda_error = static_cast<int>(e);
+  return status;
+}
+
+// Current device's SM count, after checking that it is compute capability 10.3.
+int current_device(int* dev_out, int* sms_out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(DQ4_ERR_DEVICE, e);
+  int cc = 0, sms = 0;
+  if (dev >= 0 && dev < kMaxDevices) {
+    cc = g_devices[dev].cc.load(std::memory_order_relaxed);
+    sms = g_devices[dev].sms.load(std::memory_order_relaxed);
+  }
+  if (cc == 0 || sms == 0) {
+    int major = 0, minor = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return fail_cuda(DQ4_ERR_DEVICE, e);
+    cc = major * 10 + minor;
+    if (dev >= 0 && dev < kMaxDevices) {
+      g_devices[dev].cc.store(cc, std::memory_order_relaxed);
+      g_devices[dev].sms.store(sms, std::memory_order_relaxed);
+    }
+  }
+  if (cc != 103) return fail_cuda(DQ4_ERR_ARCH, cudaErrorNoKernelImageForDevice);
+  *dev_out = dev;
+  *sms_out = sms;
+  return DQ4_OK;
+}
+
+// Resident CTAs per SM of `kernel`, cached per device.
+template <typename Kernel>
+int ctas_per_sm(Kernel kernel, int dev, std::atomic<int>* cache) {
+  int occ = (dev >= 0 && dev < kMaxDevices) ? cache[dev].load(std::memory_order_relaxed) : 0;
+  if (occ > 0) return occ;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, 0) != cudaSuccess ||
+      occ < 1) {
+    cudaGetLastError();
+    occ = 1;
+  }
+  if (dev >= 0 && dev < kMaxDevices) cache[dev].store(occ, std::memory_order_relaxed);
+  return occ;
+}
+
+int check_launch() {
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail_cuda(DQ4_ERR_LAUNCH, e);
+  return DQ4_OK;
+}
+
+template <int OUT, bool NESTED>
+int launch_dq4(const Args& a, cudaStream_t stream) {
+  int dev = 0, sms = 0;
+  if (int st = current_device(&dev, &sms)) return st;
+  using Word = typename Traits<OUT>::Word;
+  const bool vec = (reinterpret_cast<uintptr_t>(a.packed) % sizeof(Word) == 0) &&
+                   (reinterpret_cast<uintptr_t>(a.out) % 16 == 0);
+  if (vec) {
+    static std::atomic<int> occ_cache[kMaxDevices];
+    auto kernel = dq4_vec_kernel<OUT, NESTED>;
+    const int64_t n_words = a.n >> Traits<OUT>::kLog2Vals;
+    const int64_t tiles = (n_words + 32 * Tile<OUT>::U - 1) / (32 * Tile<OUT>::U);
+    int64_t grid = (tiles + kWarpsPerCta - 1) / kWarpsPerCta;
+    const int64_t cap = int64_t(sms) * ctas_per_sm(kernel, dev, occ_cache);
+    if (grid > cap) grid = cap;
+    if (grid < 1) grid = 1;
+    kernel<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(a);
+  } else {
+    static std::atomic<int> occ_cache[kMaxDevices];
+    auto kernel = dq4_scalar_kernel<OUT, NESTED>;
+    int64_t grid = (a.n + kThreads - 1) / kThreads;
+    const int64_t cap = int64_t(sms) * ctas_per_sm(kernel, dev, occ_cache);
+    if (grid > cap) grid = cap;
+    kernel<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(a);
+  }
+  return check_launch();
+}
+
+template <bool NESTED>
+int dispatch_dtype(const Args& a, int32_t out_dtype, cudaStream_t stream) {
+  switch (out_dtype) {
+    case DQ4_OUT_F16: return launch_dq4<DQ4_OUT_F16, NESTED>(a, stream);
+    case DQ4_OUT_BF16: return launch_dq4<DQ4_OUT_BF16, NESTED>(a, stream);
+    case DQ4_OUT_F32: return launch_dq4<DQ4_OUT_F32, NESTED>(a, stream);
+    default: return DQ4_ERR_DTYPE;
+  }
+}
+
+bool is_pow2(int64_t v) { return v > 0 && (v & (v - 1)) == 0; }
+
+int log2_exact(int64_t v) {
+  int r = 0;
+  while ((int64_t(1) << r) < v) ++r;
+  return r;
+}
+
+bool misaligned(const void* p, uintptr_t align) {
+  return reinterpret_cast<uintptr_t>(p) % align != 0;
+}
+
+int out_itemsize(int32_t out_dtype) { return out_dtype == DQ4_OUT_F32 ? 4 : 2; }
+
+// Checks shared by every entry point, in a fixed order; n == 0 returns
+// DQ4_OK before any pointer is looked at.
+int validate(int64_t n, int32_t blocksize, int32_t nested_blocksize, bool nested,
+             int32_t out_dtype) {
+  if (n < 0) return DQ4_ERR_N;
+  if (!is_pow2(blocksize) || blocksize < 32 || blocksize > 4096) return DQ4_ERR_BLOCKSIZE;
+  if (nested && !is_pow2(nested_blocksize)) return DQ4_ERR_NESTED_BLOCKSIZE;
+  if (out_dtype != DQ4_OUT_F16 && out_dtype != DQ4_OUT_BF16 && out_dtype != DQ4_OUT_F32)
+    return DQ4_ERR_DTYPE;
+  return DQ4_OK;
+}
+
+Args make_args(const uint8_t* packed, const uint8_t* codes, const float* absmax,
+               const float* scb, const float* vcb, float offset, int64_t n, int32_t blocksize,
+               int32_t nested_blocksize, void* out) {
+  Args a;
+  a.packed = packed;
+  a.codes = codes;
+  a.absmax = absmax;
+  a.scb = scb;
+  a.vcb = vcb;
+  a.out = out;
+  a.n = n;
+  a.nblocks = (n + blocksize - 1) / blocksize;
+  a.offset = offset;
+  a.log2_bs = log2_exact(blocksize);
+  a.log2_nbs = log2_exact(nested_blocksize);
+  return a;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------ C-ABI
+extern "C" {
+
+int dq4_abi_version(void) { return kAbiVersion; }
+
+int dq4_nested(const uint8_t* packed, const uint8_t* scale_codes, const float* nested_absmax,
+               const float* scale_codebook, const float* value_codebook, float offset,
+               int64_t n, int32_t blocksize, int32_t nested_blocksize, int32_t out_dtype,
+               void* out, void* stream) {
+  if (int st = validate(n, blocksize, nested_blocksize, true, out_dtype)) return st;
+  if (n == 0) return DQ4_OK;
+  if (!packed || !scale_codes || !nested_absmax || !scale_codebook || !value_codebook || !out)
+    return DQ4_ERR_NULL;
+  if (misaligned(nested_absmax, 4) || misaligned(scale_codebook, 4) ||
+      misaligned(value_codebook, 4) || misaligned(out, out_itemsize(out_dtype)))
+    return DQ4_ERR_ALIGN;
+  const Args a = make_args(packed, scale_codes, nested_absmax, scale_codebook, value_codebook,
+                           offset, n, blocksize, nested_blocksize, out);
+  return dispatch_dtype<true>(a, out_dtype, static_cast<cudaStream_t>(stream));
+}
+
+int dq4(const uint8_t* packed, const float* absmax, const float* value_codebook, int64_t n,
+        int32_t blocksize, int32_t out_dtype, void* out, void* stream) {
+  if (int st = validate(n, blocksize, 1, false, out_dtype)) return st;
+  if (n == 0) return DQ4_OK;
+  if (!packed || !absmax || !value_codebook || !out) return DQ4_ERR_NULL;
+  if (misaligned(absmax, 4) || misaligned(value_codebook, 4) ||
+      misaligned(out, out_itemsize(out_dtype)))
+    return DQ4_ERR_ALIGN;
+  const Args a = make_args(packed, nullptr, absmax, nullptr, value_codebook, 0.f, n, blocksize,
+                           1, out);
+  return dispatch_dtype<false>(a, out_dtype, static_cast<cudaStream_t>(stream));
+}
+
+int dq4_nested_unfused(const uint8_t* packed, const uint8_t* scale_codes,
+                       const float* nested_absmax, const float* scale_codebook,
+                       const float* value_codebook, float offset, int64_t n,
+                       int32_t blocksize, int32_t nested_blocksize, int32_t out_dtype,
+                       void* out, float* scale_scratch, void* stream) {
+  if (int st = validate(n, blocksize, nested_blocksize, true, out_dtype)) return st;
+  if (n == 0) return DQ4_OK;
+  if (!packed || !scale_codes || !nested_absmax || !scale_codebook || !value_codebook || !out ||
+      !scale_scratch)
+    return DQ4_ERR_NULL;
+  if (misaligned(nested_absmax, 4) || misaligned(scale_codebook, 4) ||
+      misaligned(value_codebook, 4) || misaligned(scale_scratch, 4) ||
+      misaligned(out, out_itemsize(out_dtype)))
+    return DQ4_ERR_ALIGN;
+  int dev = 0, sms = 0;
+  if (int st = current_device(&dev, &sms)) return st;
+  const auto st = static_cast<cudaStream_t>(stream);
+  const int64_t nblocks = (n + blocksize - 1) / blocksize;
+  int64_t grid = (nblocks + kThreads - 1) / kThreads;
+  if (grid > int64_t(sms) * 8) grid = int64_t(sms) * 8;
+  scale_codes_kernel<<<static_cast<unsigned>(grid), kThreads, 0, st>>>(
+      scale_codes, nested_absmax, scale_codebook, nblocks, log2_exact(nested_blocksize),
+      scale_scratch);
+  if (int e = check_launch()) return e;
+  add_offset_kernel<<<static_cast<unsigned>(grid), kThreads, 0, st>>>(scale_scratch, nblocks,
+                                                                       offset);
+  if (int e = check_launch()) return e;
+  return dq4(packed, scale_scratch, value_codebook, n, blocksize, out_dtype, out, stream);
+}
+
+const char* dq4_status_string(int status) {
+  switch (status) {
+    case DQ4_OK: return "ok";
+    case DQ4_ERR_NULL: return "a required pointer is NULL";
+    case DQ4_ERR_N: return "n is negative";
+    case DQ4_ERR_BLOCKSIZE: return "blocksize must be a power of two in [32, 4096]";
+    case DQ4_ERR_NESTED_BLOCKSIZE: return "nested_blocksize must be a power of two >= 1";
+    case DQ4_ERR_DTYPE: return "out_dtype must be DQ4_OUT_F16, DQ4_OUT_BF16 or DQ4_OUT_F32";
+    case DQ4_ERR_ALIGN: return "a float array or the output is misaligned for its type";
+    case DQ4_ERR_DEVICE: return "the current CUDA device could not be queried";
+    case DQ4_ERR_ARCH: return "the current device is not compute capability 10.3 (GB300)";
+    case DQ4_ERR_LAUNCH: return "the CUDA runtime reported an error at kernel launch";
+    default: return "unknown status";
+  }
+}
+
+int dq4_last_cuda_error(void) { return t_last_cuda_error; }
+
+}  // extern "C"
