@@ -55,13 +55,20 @@ PROFILES = os.path.join(ROOT, "profiles")
 def parse_args():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cell", default=DEFAULT_CELL, choices=sorted(gen.CELLS))
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--compare-batches", type=int, default=7)
+    ap.add_argument("--sets", type=int, default=N_SETS,
+                    help="rotating device buffer sets (each larger than L2)")
+    ap.add_argument("--event-every", type=int, default=16,
+                    help="bracket every m-th timed launch with its own event pair")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-compare", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
     return ap.parse_args()
 
 
@@ -202,8 +209,9 @@ def run_ours(args):
                       "value_codebook")}
     scb = host["scale_codebook"].to(dev)
     vcb = host["value_codebook"].to(dev)
+    n_sets = max(1, args.sets)
     sets = []
-    for _ in range(N_SETS):
+    for _ in range(n_sets):
         sets.append(dict(packed=host["packed"].to(dev), codes=host["scale_codes"].to(dev),
                          absmax=host["nested_absmax"].to(dev),
                          out=torch.empty(n, dtype=out_dtype, device=dev),
@@ -220,18 +228,21 @@ def run_ours(args):
     scb_p, vcb_p = scb.data_ptr(), vcb.data_ptr()
 
     def fused(i):
-        pk, cd, am, o, _ = ptrs[i % N_SETS]
+        pk, cd, am, o, _ = ptrs[i % n_sets]
         return L.dq4_nested(pk, cd, am, scb_p, vcb_p, off, n, bs, nbs, code, o, sh)
 
     def unfused(i):
-        pk, cd, am, o, sc = ptrs[i % N_SETS]
+        pk, cd, am, o, sc = ptrs[i % n_sets]
         return L.dq4_nested_unfused(pk, cd, am, scb_p, vcb_p, off, n, bs, nbs, code, o, sc, sh)
 
-    # correctness gate before timing: first and last 64 Ki values of set 0 vs the
-    # unfused sequence (bit-identical by construction)
-    assert fused(0) == 0 and unfused(1) == 0
+    # correctness gate before timing: first and last 64 Ki values of the fused
+    # output vs the unfused sequence (bit-identical by construction)
+    assert fused(0) == 0
     torch.cuda.synchronize(dev)
-    a, b = sets[0]["out"], sets[1]["out"]
+    a = sets[0]["out"].clone()
+    assert unfused(0) == 0
+    torch.cuda.synchronize(dev)
+    b = sets[0]["out"]
     if not (torch.equal(a[:65536].view(torch.int16 if a.element_size() == 2 else torch.int32),
                         b[:65536].view(torch.int16 if b.element_size() == 2 else torch.int32))
             and torch.equal(a[-65536:].view(torch.int16 if a.element_size() == 2 else torch.int32),
@@ -244,47 +255,54 @@ def run_ours(args):
     for i in range(W):
         if fused(i):
             raise SystemExit("dq4_nested failed in warm-up")
-    ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
+    # batch boundaries (>= 7 batches) and a sample of single launches, each with
+    # its own event pair; all other launches run back to back
+    nb = max(1, min(K, max(7, min(20, K // 50))))
+    edges = sorted(set(np.linspace(0, K, nb + 1).astype(int).tolist()))
+    ev_b = {e: torch.cuda.Event(enable_timing=True) for e in edges}
+    every = max(1, args.event_every)
+    sampled = list(range(every // 2, K, every)) or [0]
+    ev_s = {i: torch.cuda.Event(enable_timing=True) for i in sampled}
+    ev_e = {i: torch.cuda.Event(enable_timing=True) for i in sampled}
     gpu_uuid = None
     try:
         u = str(torch.cuda.get_device_properties(dev).uuid)
         gpu_uuid = u if u.startswith("GPU-") else "GPU-" + u
     except Exception:
         pass
-    clocks = ClockSampler(gpu_uuid)
-    clocks.start()
+    clocks = None if args.no_clocks else ClockSampler(gpu_uuid)
+    if clocks:
+        clocks.start()
     torch.cuda.synchronize(dev)
     barrier()
     torch.cuda.synchronize(dev)
     wall0 = time.perf_counter()
-    t_start.record(stream)
     bad = 0
     for i in range(K):
-        ev_s[i].record(stream)
-        bad |= fused(W + i)
-        ev_e[i].record(stream)
-    t_end.record(stream)
+        if i in ev_b:
+            ev_b[i].record(stream)
+        if i in ev_s:
+            ev_s[i].record(stream)
+            bad |= fused(W + i)
+            ev_e[i].record(stream)
+        else:
+            bad |= fused(W + i)
+    ev_b[K].record(stream)
     torch.cuda.synchronize(dev)
     barrier()
     wall = time.perf_counter() - wall0
-    clk = clocks.stop()
+    clk = clocks.stop() if clocks else {"error": "not sampled (--no-clocks)"}
     if bad:
         raise SystemExit(f"dq4_nested returned status {bad} in the timed region")
-    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end))
-    launch_ms = [ev_s[i].elapsed_time(ev_e[i]) for i in range(K)]
+    elapsed_ms = max_over_ranks(ev_b[0].elapsed_time(ev_b[K]))
+    launch_ms = [ev_s[i].elapsed_time(ev_e[i]) for i in sampled]
     avg_launch_ms = float(np.mean(launch_ms))
-    nb = max(7, min(20, K // 50)) if K >= 7 else K
-    edges = np.linspace(0, K, nb + 1).astype(int)
-    batch_ms = [ev_s[edges[j]].elapsed_time(ev_e[edges[j + 1] - 1]) / (edges[j + 1] - edges[j])
-                for j in range(nb) if edges[j + 1] > edges[j]]
+    batch_ms = [ev_b[a].elapsed_time(ev_b[b]) / (b - a) for a, b in zip(edges[:-1], edges[1:])]
 
     # ---- interleaved fused / unfused comparison (not part of the timed region)
     cmp_f, cmp_u = [], []
     per = 200
-    for j in range(args.compare_batches):
+    for j in range(0 if args.no_compare else args.compare_batches):
         for fn, acc in ((fused, cmp_f), (unfused, cmp_u)):
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
@@ -296,8 +314,10 @@ def run_ours(args):
             acc.append(e0.elapsed_time(e1) / per * 1e3)
 
     # ---- end to end with host buffers (pinned H2D of the inputs, call, D2H of the output)
-    pin = {k: v.pin_memory() for k, v in host.items()}
-    host_out = torch.empty(n, dtype=out_dtype).pin_memory()
+    pin = {k: v.pin_memory() for k, v in host.items()} if not args.no_e2e else dict(host)
+    host_out = torch.empty(n if not args.no_e2e else 0, dtype=out_dtype)
+    if not args.no_e2e:
+        host_out = host_out.pin_memory()
     s0 = sets[0]
     h2d = sum(v.numel() * v.element_size() for v in pin.values())
     d2h = host_out.numel() * host_out.element_size()
@@ -313,22 +333,24 @@ def run_ours(args):
                       out_dtype, out=s0["out"], stream=stream)
         host_out.copy_(s0["out"], non_blocking=True)
 
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize(dev)
-    barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(E):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1))
-    # the copied-back output must equal the device result
-    if not torch.equal(host_out.view(torch.uint8), s0["out"].cpu().view(torch.uint8)):
-        raise SystemExit("e2e output mismatch")
+    e2e_ms = None
+    if not args.no_e2e:
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(E):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1))
+        # the copied-back output must equal the device result
+        if not torch.equal(host_out.view(torch.uint8), s0["out"].cpu().view(torch.uint8)):
+            raise SystemExit("e2e output mismatch")
 
     peak, peak_kind = read_peaks()
     ms_per_step = elapsed_ms / K
@@ -356,7 +378,7 @@ def run_ours(args):
             "nested_blocksize": cell.nested_blocksize, "format": cell.fmt,
             "out_dtype": cell.out, "offset": cell.offset,
             "algorithmic_bytes_per_step": alg_bytes,
-            "l2": f"inputs larger than L2: {alg_bytes / 1e6:.1f} MB per step, {N_SETS} rotating "
+            "l2": f"inputs larger than L2: {alg_bytes / 1e6:.1f} MB per step, {n_sets} rotating "
                   "buffer sets",
             "parallelism": f"replicas x{world}",
         },
@@ -371,11 +393,12 @@ def run_ours(args):
             "kernel": "dq4_vec_kernel<f16,nested>" if cell.out == "f16"
             else f"dq4_vec_kernel<{cell.out},nested>",
             "avg_launch_us": avg_launch_ms * 1e3,
+            "launches_sampled": len(launch_ms),
         },
         "batches_us_per_step": [round(x * 1e3, 3) for x in batch_ms],
         "batch_stats_us": {"median": pct(batch_ms, 50) * 1e3, "p10": pct(batch_ms, 10) * 1e3,
                            "p90": pct(batch_ms, 90) * 1e3},
-        "fused_vs_unfused": {
+        "fused_vs_unfused": None if not cmp_f else {
             "fused_us": {"median": pct(cmp_f, 50), "p10": pct(cmp_f, 10), "p90": pct(cmp_f, 90),
                          "samples": [round(x, 3) for x in cmp_f]},
             "unfused_us": {"median": pct(cmp_u, 50), "p10": pct(cmp_u, 10),
@@ -383,9 +406,10 @@ def run_ours(args):
             "speedup": pct(cmp_u, 50) / pct(cmp_f, 50),
             "launches": {"fused": 1, "unfused": 3},
         },
-        "e2e": {"value": world * E * n / (e2e_ms / 1e3), "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": E,
-                "ms_per_step": e2e_ms / E},
+        "e2e": None if e2e_ms is None else {
+            "value": world * E * n / (e2e_ms / 1e3), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": E,
+            "ms_per_step": e2e_ms / E},
         "gpu_launches": K,
         "clocks": clk,
         "wall_s_timed": wall,

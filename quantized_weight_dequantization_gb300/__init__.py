@@ -1,8 +1,9 @@
 """Fused nested 4-bit weight dequantization for NVIDIA GB300 (sm_103a).
 
 The computation lives in the CUDA library ``libdq4.so`` (C ABI in
-``include/dq4.h``); this package is its thin Python binding.  Importing it
-raises if the library has not been built: there is no CPU fallback.
+``include/dq4.h``); this package is its thin Python binding.  The first use
+of the library raises ImportError if it has not been built (see ``build``):
+there is no CPU fallback.
 """
 
 from ._binding import (  # noqa: F401
@@ -13,9 +14,16 @@ from ._binding import (  # noqa: F401
     dq4,
     dq4_nested,
     dq4_nested_unfused,
-    lib,
+    get_lib,
     sizes,
 )
 
-__all__ = ["dq4_nested", "dq4", "dq4_nested_unfused", "Dq4Error", "lib", "sizes",
+
+def __getattr__(name):
+    if name == "lib":
+        return get_lib()
+    raise AttributeError(name)
+
+
+__all__ = ["dq4_nested", "dq4", "dq4_nested_unfused", "Dq4Error", "get_lib", "sizes",
            "OUT_F16", "OUT_BF16", "OUT_F32"]

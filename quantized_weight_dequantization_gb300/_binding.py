@@ -1,8 +1,9 @@
 """ctypes binding of libdq4 (include/dq4.h): argument marshalling only.
 
 Every step of the computation runs in the CUDA library.  PyTorch is used for
-device memory and streams; there is no CPU path and no fallback: if the
-library is missing, importing this module raises.
+device memory and streams; there is no CPU path and no fallback: the first
+use of the library (any call, or the ``lib`` attribute) raises ImportError if
+libdq4.so has not been built.
 """
 
 from __future__ import annotations
@@ -31,10 +32,11 @@ class Dq4Error(RuntimeError):
 
     def __init__(self, status: int, where: str):
         self.status = status
-        msg = lib.dq4_status_string(status).decode()
+        L = get_lib()
+        msg = L.dq4_status_string(status).decode()
         extra = ""
         if status in (7, 8, 9):
-            extra = f" (cudaError_t {lib.dq4_last_cuda_error()})"
+            extra = f" (cudaError_t {L.dq4_last_cuda_error()})"
         super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}: {msg}{extra}")
 
 
@@ -60,7 +62,21 @@ def _load() -> ctypes.CDLL:
     return L
 
 
-lib = _load()
+_LIB = None
+
+
+def get_lib() -> ctypes.CDLL:
+    """The loaded library (loaded on first use; raises ImportError if not built)."""
+    global _LIB
+    if _LIB is None:
+        _LIB = _load()
+    return _LIB
+
+
+def __getattr__(name):
+    if name == "lib":
+        return get_lib()
+    raise AttributeError(name)
 
 
 # ------------------------------------------------------------- helpers
@@ -126,7 +142,7 @@ def dq4_nested(packed: torch.Tensor, scale_codes: torch.Tensor, nested_absmax: t
     if out_dtype not in _DTYPE_CODE:
         raise TypeError(f"out_dtype: unsupported {out_dtype}")
     res = _out_tensor(out, out_dtype, n, device)
-    st = lib.dq4_nested(_ptr(packed), _ptr(scale_codes), _ptr(nested_absmax),
+    st = get_lib().dq4_nested(_ptr(packed), _ptr(scale_codes), _ptr(nested_absmax),
                         _ptr(scale_codebook), _ptr(value_codebook), float(offset), n,
                         blocksize, nested_blocksize, _DTYPE_CODE[out_dtype], _ptr(res),
                         _stream_handle(stream, device))
@@ -149,7 +165,7 @@ def dq4(packed: torch.Tensor, absmax: torch.Tensor, value_codebook: torch.Tensor
     if out_dtype not in _DTYPE_CODE:
         raise TypeError(f"out_dtype: unsupported {out_dtype}")
     res = _out_tensor(out, out_dtype, n, device)
-    st = lib.dq4(_ptr(packed), _ptr(absmax), _ptr(value_codebook), n, blocksize,
+    st = get_lib().dq4(_ptr(packed), _ptr(absmax), _ptr(value_codebook), n, blocksize,
                  _DTYPE_CODE[out_dtype], _ptr(res), _stream_handle(stream, device))
     if st:
         raise Dq4Error(st, "dq4")
@@ -178,7 +194,7 @@ def dq4_nested_unfused(packed: torch.Tensor, scale_codes: torch.Tensor,
     if scale_scratch is None:
         scale_scratch = torch.empty(max(nb, 1), dtype=torch.float32, device=device)
     _check(scale_scratch, "scale_scratch", torch.float32, nb, device)
-    st = lib.dq4_nested_unfused(_ptr(packed), _ptr(scale_codes), _ptr(nested_absmax),
+    st = get_lib().dq4_nested_unfused(_ptr(packed), _ptr(scale_codes), _ptr(nested_absmax),
                                 _ptr(scale_codebook), _ptr(value_codebook), float(offset), n,
                                 blocksize, nested_blocksize, _DTYPE_CODE[out_dtype], _ptr(res),
                                 _ptr(scale_scratch), _stream_handle(stream, device))

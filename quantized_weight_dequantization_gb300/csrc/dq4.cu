@@ -11,16 +11,22 @@
 // into an FMA, and the library is also compiled with -fmad=false.
 //
 // Design (a streaming, HBM-bound map; no tensor cores):
-//  * A warp owns a tile of 32*U consecutive "words".  A word is the packed
-//    data of 16 output bytes: 8 values (4 packed bytes) for FP16/BF16
+//  * A warp owns a tile of 32*U consecutive "words" (U = 8).  A word is the
+//    packed data of 16 output bytes: 8 values (4 packed bytes) for FP16/BF16
 //    output, 4 values (2 packed bytes) for FP32.  Lane l handles words
 //    tile + 32k + l, so each packed load and each 16-byte output store of a
 //    warp covers one contiguous, fully used span.
+//  * The grid covers the whole array, one tile per warp: the hardware hands
+//    out CTAs in index order, so the addresses in flight at any time form one
+//    compact window moving through HBM.  (On GB300 this beats a persistent
+//    grid-stride loop by ~13% for this 1:4 read:write stream.)  Only if the
+//    grid would exceed the launch limit do warps loop over several tiles,
+//    loading the next tile before decoding the current one.
 //  * blocksize >= 32 is a power of two, so a word never straddles two outer
-//    blocks.  Each lane rebuilds at most one scale per tile (the tile's
-//    blocks are consecutive) and the words fetch theirs with a warp shuffle:
-//    one scale code, one nested absmax and one codebook lookup per block,
-//    never an FP32 scale array.
+//    blocks.  The tile's blocks are consecutive; lane j rebuilds the scale of
+//    the tile's blocks j, j+32, ... and each word takes its scale by a warp
+//    shuffle: one scale code, one nested absmax and one codebook lookup per
+//    block, never an FP32 scale array.
 //  * The 16-entry value codebook sits in shared memory (banks 0..15, so the
 //    data-dependent lookups of a warp never conflict); the 256-entry scale
 //    codebook too.
@@ -41,9 +47,13 @@
 
 namespace {
 
-constexpr int kThreads = 256;
+#ifndef DQ4_THREADS
+#define DQ4_THREADS 256
+#endif
+constexpr int kThreads = DQ4_THREADS;
 constexpr int kWarpsPerCta = kThreads / 32;
 constexpr int kMaxDevices = 64;
+constexpr int64_t kMaxGrid = 2147483647;  // gridDim.x limit
 constexpr int kAbiVersion = 1;
 
 thread_local int t_last_cuda_error = 0;
@@ -81,12 +91,40 @@ struct Traits<DQ4_OUT_F32> {
   static constexpr int kLog2Vals = 2;
 };
 
-// Words per warp tile.  Tiles of at most 32 outer blocks keep "one scale
-// per lane" exact: 32*U words >> log2(words per block) <= 32 for every
-// blocksize >= 32.
+// Words per lane per warp tile (tunable at build time).  A tile of 32*U
+// words touches at most 32*U >> log2(words per block) outer blocks; each
+// lane rebuilds J = ceil(that / 32) of their scales.
+#ifndef DQ4_U_HALF
+#define DQ4_U_HALF 8
+#endif
+#ifndef DQ4_U_F32
+#define DQ4_U_F32 8
+#endif
+// 1: a warp loads its next tile before it decodes the current one.
+#ifndef DQ4_PREFETCH
+#define DQ4_PREFETCH 1
+#endif
+// packed-word loads: 0 streaming (ld.global.cs), 1 read-only non-coherent (ld.global.nc)
+#ifndef DQ4_LD_HINT
+#define DQ4_LD_HINT 0
+#endif
+// output stores: 0 streaming (st.global.cs), 1 default write-back
+#ifndef DQ4_ST_HINT
+#define DQ4_ST_HINT 0
+#endif
+// 0: one tile per warp over the whole array; k > 0: at most k CTAs per SM
+// (a persistent grid-stride loop)
+#ifndef DQ4_CTAS_PER_SM
+#define DQ4_CTAS_PER_SM 0
+#endif
+
 template <int OUT>
 struct Tile {
-  static constexpr int U = (OUT == DQ4_OUT_F32) ? 8 : 4;
+  static constexpr int U = (OUT == DQ4_OUT_F32) ? DQ4_U_F32 : DQ4_U_HALF;
+  static constexpr int kWshiftMin = 5 - Traits<OUT>::kLog2Vals;  // blocksize >= 32
+  static constexpr int kBlocksMax = (32 * U) >> kWshiftMin;
+  static constexpr int J = kBlocksMax > 32 ? kBlocksMax / 32 : 1;
+  static_assert(J <= 4, "at most four scale registers per lane");
 };
 
 // ------------------------------------------------------------- device math
@@ -169,42 +207,130 @@ __device__ __forceinline__ void stage_codebooks(const Args& a, float* s_vcb, flo
 }
 
 // ---------------------------------------------------------------- kernels
+template <typename Word>
+__device__ __forceinline__ Word load_word(const Word* p) {
+#if DQ4_LD_HINT == 0
+  return __ldcs(p);
+#else
+  return __ldg(p);
+#endif
+}
+
+__device__ __forceinline__ void store_16(uint4* p, uint4 v) {
+#if DQ4_ST_HINT == 0
+  __stcs(p, v);
+#else
+  *p = v;
+#endif
+}
+
+// Registers of one warp tile: U packed words per lane, and the raw scale
+// inputs (code, absmax) of up to J blocks per lane.
+template <int OUT>
+struct TileRegs {
+  typename Traits<OUT>::Word w[Tile<OUT>::U];
+  uint32_t code[Tile<OUT>::J];
+  float am[Tile<OUT>::J];
+};
+
+template <int OUT, bool NESTED>
+__device__ __forceinline__ void load_tile(const Args& a, int64_t base, int64_t n_words, int wshift,
+                                          int lane, TileRegs<OUT>& r) {
+  using Word = typename Traits<OUT>::Word;
+  constexpr int U = Tile<OUT>::U;
+  constexpr int64_t kTile = 32 * U;
+  const Word* pw = reinterpret_cast<const Word*>(a.packed);
+#pragma unroll
+  for (int k = 0; k < U; ++k) {
+    const int64_t wi = base + k * 32 + lane;
+    r.w[k] = wi < n_words ? load_word(pw + wi) : Word(0);
+  }
+  const int64_t b0 = base >> wshift;
+  const int64_t b_last = ((base + kTile < n_words ? base + kTile : n_words) - 1) >> wshift;
+#pragma unroll
+  for (int j = 0; j < Tile<OUT>::J; ++j) {
+    const int64_t b = b0 + lane + 32 * j;
+    r.code[j] = 0;
+    r.am[j] = 0.f;
+    if (b <= b_last) {
+      if constexpr (NESTED) {
+        r.code[j] = __ldg(a.codes + b);
+        r.am[j] = __ldg(a.absmax + (b >> a.log2_nbs));
+      } else {
+        r.am[j] = __ldg(a.absmax + b);
+      }
+    }
+  }
+}
+
+template <int OUT, bool NESTED>
+__device__ __forceinline__ void decode_tile(const Args& a, int64_t base, int64_t n_words,
+                                            int wshift, int lane, const TileRegs<OUT>& r,
+                                            const float* s_scb, const float* s_vcb) {
+  constexpr int U = Tile<OUT>::U;
+  constexpr int J = Tile<OUT>::J;
+  float sc[J];
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    if constexpr (NESTED) {
+      sc[j] = __fadd_rn(__fmul_rn(s_scb[r.code[j]], r.am[j]), a.offset);  // never an FMA
+    } else {
+      sc[j] = r.am[j];
+    }
+  }
+  uint4* po = reinterpret_cast<uint4*>(a.out);
+  const int64_t b0 = base >> wshift;
+#pragma unroll
+  for (int k = 0; k < U; ++k) {
+    const int64_t wi = base + k * 32 + lane;
+    const int idx = int((wi >> wshift) - b0);  // the word's block within the tile
+    // idx >> 5 == k >> wshift for every lane, so the register choice is warp-uniform
+    float src = sc[0];
+#pragma unroll
+    for (int j = 1; j < J; ++j)
+      if ((k >> wshift) == j) src = sc[j];
+    const float s = __shfl_sync(0xffffffffu, src, idx & 31);
+    if (wi < n_words) store_16(po + wi, decode_word<OUT>(r.w[k], s, s_vcb));
+  }
+}
+
 template <int OUT, bool NESTED>
 __global__ void __launch_bounds__(kThreads) dq4_vec_kernel(const Args a) {
   using T = Traits<OUT>;
-  using Word = typename T::Word;
-  constexpr int U = Tile<OUT>::U;
-  constexpr int64_t kTile = 32 * U;
+  constexpr int64_t kTile = 32 * Tile<OUT>::U;
   __shared__ float s_vcb[16];
   __shared__ float s_scb[NESTED ? 256 : 1];
   stage_codebooks<NESTED>(a, s_vcb, s_scb);
 
-  const Word* pw = reinterpret_cast<const Word*>(a.packed);
-  uint4* po = reinterpret_cast<uint4*>(a.out);
   const int64_t n_words = a.n >> T::kLog2Vals;
   const int wshift = a.log2_bs - T::kLog2Vals;  // log2(words per outer block)
   const int lane = threadIdx.x & 31;
   const int64_t warp = (int64_t(blockIdx.x) * kThreads + threadIdx.x) >> 5;
-  const int64_t n_warps = (int64_t(gridDim.x) * kThreads) >> 5;
+  const int64_t stride = ((int64_t(gridDim.x) * kThreads) >> 5) * kTile;
 
-  for (int64_t base = warp * kTile; base < n_words; base += n_warps * kTile) {
-    Word w[U];
-#pragma unroll
-    for (int k = 0; k < U; ++k) {
-      const int64_t wi = base + k * 32 + lane;
-      w[k] = wi < n_words ? __ldcs(pw + wi) : Word(0);
-    }
-    // lane j rebuilds the scale of the tile's j-th block
-    const int64_t b0 = base >> wshift;
-    const int64_t b_last = ((base + kTile < n_words ? base + kTile : n_words) - 1) >> wshift;
-    const float my_scale = (b0 + lane <= b_last) ? block_scale<NESTED>(a, s_scb, b0 + lane) : 0.f;
-#pragma unroll
-    for (int k = 0; k < U; ++k) {
-      const int64_t wi = base + k * 32 + lane;
-      const float s = __shfl_sync(0xffffffffu, my_scale, int((wi >> wshift) - b0));
-      if (wi < n_words) __stcs(po + wi, decode_word<OUT>(w[k], s, s_vcb));
+  int64_t base = warp * kTile;
+#if DQ4_PREFETCH
+  if (base < n_words) {
+    TileRegs<OUT> cur;
+    load_tile<OUT, NESTED>(a, base, n_words, wshift, lane, cur);
+    for (;;) {
+      const int64_t next = base + stride;
+      TileRegs<OUT> nxt;
+      const bool more = next < n_words;  // warp-uniform
+      if (more) load_tile<OUT, NESTED>(a, next, n_words, wshift, lane, nxt);
+      decode_tile<OUT, NESTED>(a, base, n_words, wshift, lane, cur, s_scb, s_vcb);
+      if (!more) break;
+      cur = nxt;
+      base = next;
     }
   }
+#else
+  for (; base < n_words; base += stride) {
+    TileRegs<OUT> cur;
+    load_tile<OUT, NESTED>(a, base, n_words, wshift, lane, cur);
+    decode_tile<OUT, NESTED>(a, base, n_words, wshift, lane, cur, s_scb, s_vcb);
+  }
+#endif
 
   // fewer than one word of values remains after the last whole word
   const int64_t tail0 = n_words << T::kLog2Vals;
@@ -309,15 +435,13 @@ int launch_dq4(const Args& a, cudaStream_t stream) {
   const bool vec = (reinterpret_cast<uintptr_t>(a.packed) % sizeof(Word) == 0) &&
                    (reinterpret_cast<uintptr_t>(a.out) % 16 == 0);
   if (vec) {
-    static std::atomic<int> occ_cache[kMaxDevices];
-    auto kernel = dq4_vec_kernel<OUT, NESTED>;
     const int64_t n_words = a.n >> Traits<OUT>::kLog2Vals;
     const int64_t tiles = (n_words + 32 * Tile<OUT>::U - 1) / (32 * Tile<OUT>::U);
     int64_t grid = (tiles + kWarpsPerCta - 1) / kWarpsPerCta;
-    const int64_t cap = int64_t(sms) * ctas_per_sm(kernel, dev, occ_cache);
+    const int64_t cap = DQ4_CTAS_PER_SM > 0 ? int64_t(sms) * DQ4_CTAS_PER_SM : kMaxGrid;
     if (grid > cap) grid = cap;
     if (grid < 1) grid = 1;
-    kernel<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(a);
+    dq4_vec_kernel<OUT, NESTED><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(a);
   } else {
     static std::atomic<int> occ_cache[kMaxDevices];
     auto kernel = dq4_scalar_kernel<OUT, NESTED>;

@@ -6,6 +6,8 @@ scale reconstruction into SM103 4-bit dequantization", bitsandbytes issue
 #21, section "Correctness requirements": bitwise identity; no FMA).
 """
 
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -57,16 +59,17 @@ def assert_same(got: torch.Tensor, want: np.ndarray, what: str):
                              f"want {[hex(int(x)) for x in w[bad[:5]]]}")
 
 
-def fused(dq, p, t, out, **kw):
+def fused(dq, p, t, kind, **kw):
+    """The fused entry point for problem p (device tensors t), output dtype name ``kind``."""
     return dq.dq4_nested(t["packed"], t["scale_codes"], t["nested_absmax"], t["scale_codebook"],
                          t["value_codebook"], float(p.offset), p.n, p.blocksize,
-                         p.nested_blocksize, DT[out], **kw)
+                         p.nested_blocksize, DT[kind], **kw)
 
 
-def unfused(dq, p, t, out):
+def unfused(dq, p, t, kind):
     return dq.dq4_nested_unfused(t["packed"], t["scale_codes"], t["nested_absmax"],
                                  t["scale_codebook"], t["value_codebook"], float(p.offset), p.n,
-                                 p.blocksize, p.nested_blocksize, DT[out])
+                                 p.blocksize, p.nested_blocksize, DT[kind])
 
 
 # --------------------------------------------------------------- suites
@@ -261,10 +264,12 @@ def test_n_zero_and_errors(dq):
     with pytest.raises(dq.Dq4Error, match="BLOCKSIZE"):
         dq.dq4_nested(t["packed"], t["scale_codes"], t["nested_absmax"], t["scale_codebook"],
                       t["value_codebook"], 0.1, 1000, 8192, 256, torch.float16)
-    with pytest.raises(dq.Dq4Error, match="NESTED_BLOCKSIZE"):
-        dq.dq4_nested(t["packed"], t["scale_codes"], t["nested_absmax"], t["scale_codebook"],
-                      t["value_codebook"], 0.1, 1000, 64, 3, torch.float16)
     L = dq.lib
+    o = torch.empty(1000, dtype=torch.float16, device=DEV)
+    st = L.dq4_nested(t["packed"].data_ptr(), t["scale_codes"].data_ptr(),
+                      t["nested_absmax"].data_ptr(), t["scale_codebook"].data_ptr(),
+                      t["value_codebook"].data_ptr(), 0.1, 1000, 64, 3, 0, o.data_ptr(), None)
+    assert st == 4  # DQ4_ERR_NESTED_BLOCKSIZE
     st = L.dq4_nested(t["packed"].data_ptr(), t["scale_codes"].data_ptr(),
                       t["nested_absmax"].data_ptr() + 2, t["scale_codebook"].data_ptr(),
                       t["value_codebook"].data_ptr(), 0.1, 1000, 64, 256, 0,
@@ -295,3 +300,30 @@ def test_gpu_conversions_through_the_kernel(dq):
         got = bits(dq.dq4(packed, absmax, vcb_d, n, bs, DT[out])).reshape(-1, bs)
         assert np.all(got == got[:, :1])
         assert np.array_equal(got[:, 0], conv(x)), out
+
+
+def test_grid_stride_fallback_path(dq, tmp_path):
+    """A build capped at one CTA per SM makes every warp loop over many tiles,
+    loading the next tile before decoding the current one: same bits."""
+    from quantized_weight_dequantization_gb300 import build as B
+    path = B.build(force=True, out=str(tmp_path / "libdq4_capped.so"),
+                   extra_flags=["-DDQ4_CTAS_PER_SM=1"])
+    L = ctypes.CDLL(path)
+    p_, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float
+    L.dq4_nested.argtypes = [p_, p_, p_, p_, p_, f32, i64, i32, i32, i32, p_, p_]
+    L.dq4_nested.restype = ctypes.c_int
+    cases = [(gen.CELLS["C2a"].problem(), "bf16"), (gen.CELLS["C2b"].problem(), "f32")]
+    cases += [(gen.enumeration_problem(-0.52, blocksize=32), k) for k in DT]
+    cases += [(gen.make_problem(64 * 256 * 37 + 5, 4096, 256, "nf4", 0.5, 0.1, seed=8), k)
+              for k in DT]
+    for p, kind in cases:
+        t = to_dev(p)
+        out = torch.empty(p.n, dtype=DT[kind], device=DEV)
+        st = L.dq4_nested(t["packed"].data_ptr(), t["scale_codes"].data_ptr(),
+                          t["nested_absmax"].data_ptr(), t["scale_codebook"].data_ptr(),
+                          t["value_codebook"].data_ptr(), float(p.offset), p.n, p.blocksize,
+                          p.nested_blocksize, {"f16": 0, "bf16": 1, "f32": 2}[kind],
+                          out.data_ptr(), torch.cuda.current_stream().cuda_stream)
+        assert st == 0
+        assert_same(out, oracle.dq4_nested(p, kind, threads=ORACLE_THREADS),
+                    f"capped n={p.n} bs={p.blocksize} {kind}")
