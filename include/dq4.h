@@ -40,7 +40,8 @@
  *    (any cudaMalloc / PyTorch allocation is); other alignments run a
  *    per-element path with the same results.
  *  - Calls from several host threads are safe; the library keeps only a
- *    per-device cache of device properties.
+ *    per-device cache of device properties (and, for
+ *    dq4_nested_unfused_static, one static scratch array per device).
  */
 #ifndef DQ4_H
 #define DQ4_H
@@ -67,6 +68,7 @@ extern "C" {
 #define DQ4_ERR_DEVICE 7           /* no current CUDA device could be queried */
 #define DQ4_ERR_ARCH 8             /* current device is not compute capability 10.3 */
 #define DQ4_ERR_LAUNCH 9           /* the CUDA runtime reported an error at launch */
+#define DQ4_ERR_TOO_LARGE 10       /* n needs more scratch than the library's static array */
 
 /* Version of this interface (incremented on any change of a signature). */
 int dq4_abi_version(void);
@@ -117,6 +119,41 @@ int dq4_nested_unfused(const uint8_t* packed, const uint8_t* scale_codes,
                        const float* value_codebook, float offset, int64_t n,
                        int32_t blocksize, int32_t nested_blocksize, int32_t out_dtype,
                        void* out, float* scale_scratch, void* stream);
+
+/*
+ * The unfused sequence of dq4_nested_unfused, for callers that cannot
+ * allocate device memory.  Some callers may not call cudaMalloc / cudaFree
+ * at all: a serving loop that reserves all device memory when it starts
+ * and forbids allocation afterwards (cudaMalloc and cudaFree can
+ * synchronize the device and stall every other stream), a runtime whose
+ * memory is handed out only by its own pool, or an allocator's own hook,
+ * which must not re-enter the allocator.  This entry point allocates
+ * nothing: the FP32 scale scratch is a fixed array inside the library.
+ * The paper (issue #21) has no counterpart of this entry point; it only
+ * repackages the unfused sequence above.
+ *
+ * Arguments, layout and results are those of dq4_nested_unfused, without
+ * `scale_scratch`; the output is bit-identical.
+ *   - Limit: ceil(n / blocksize) <= DQ4_STATIC_SCRATCH_BLOCKS outer blocks
+ *     (16 MiB of FP32 scratch); a larger problem returns DQ4_ERR_TOO_LARGE
+ *     before anything is enqueued.
+ *   - The scratch is a file-scope __device__ array, so every GPU on which
+ *     the library's kernels are loaded holds those 16 MiB until the
+ *     process exits.
+ *   - The first call on each device looks up the array's device address
+ *     (once per device, with that device current).  Make that first call
+ *     before any stream capture begins.
+ *   - All calls share the one array, and each call overwrites the part it
+ *     uses before reading it (nothing has to start at zero).  Calls that
+ *     overlap on the GPU (on different streams, or from different host
+ *     threads without ordering) race on it: order them on one stream.
+ */
+#define DQ4_STATIC_SCRATCH_BLOCKS 4194304
+int dq4_nested_unfused_static(const uint8_t* packed, const uint8_t* scale_codes,
+                              const float* nested_absmax, const float* scale_codebook,
+                              const float* value_codebook, float offset, int64_t n,
+                              int32_t blocksize, int32_t nested_blocksize, int32_t out_dtype,
+                              void* out, void* stream);
 
 /* A static, human-readable string for a status code (never NULL). */
 const char* dq4_status_string(int status);

@@ -23,7 +23,7 @@ _CODE_DTYPE = {v: k for k, v in _DTYPE_CODE.items()}
 STATUS_NAMES = {
     0: "DQ4_OK", 1: "DQ4_ERR_NULL", 2: "DQ4_ERR_N", 3: "DQ4_ERR_BLOCKSIZE",
     4: "DQ4_ERR_NESTED_BLOCKSIZE", 5: "DQ4_ERR_DTYPE", 6: "DQ4_ERR_ALIGN",
-    7: "DQ4_ERR_DEVICE", 8: "DQ4_ERR_ARCH", 9: "DQ4_ERR_LAUNCH",
+    7: "DQ4_ERR_DEVICE", 8: "DQ4_ERR_ARCH", 9: "DQ4_ERR_LAUNCH", 10: "DQ4_ERR_TOO_LARGE",
 }
 
 
@@ -55,6 +55,8 @@ def _load() -> ctypes.CDLL:
     L.dq4.restype = ctypes.c_int
     L.dq4_nested_unfused.argtypes = [p, p, p, p, p, f32, i64, i32, i32, i32, p, p, p]
     L.dq4_nested_unfused.restype = ctypes.c_int
+    L.dq4_nested_unfused_static.argtypes = [p, p, p, p, p, f32, i64, i32, i32, i32, p, p]
+    L.dq4_nested_unfused_static.restype = ctypes.c_int
     L.dq4_status_string.argtypes = [ctypes.c_int]
     L.dq4_status_string.restype = ctypes.c_char_p
     L.dq4_last_cuda_error.argtypes = []
@@ -201,3 +203,37 @@ def dq4_nested_unfused(packed: torch.Tensor, scale_codes: torch.Tensor,
     if st:
         raise Dq4Error(st, "dq4_nested_unfused")
     return res, scale_scratch
+
+
+def dq4_nested_unfused_static(packed: torch.Tensor, scale_codes: torch.Tensor,
+                              nested_absmax: torch.Tensor, scale_codebook: torch.Tensor,
+                              value_codebook: torch.Tensor, offset: float, n: int,
+                              blocksize: int = 64, nested_blocksize: int = 256,
+                              out_dtype: torch.dtype = torch.float16,
+                              out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """The unfused sequence with the library's own static FP32 scratch.
+
+    For callers that must not allocate device memory while they run (pass a
+    preallocated ``out``; the call itself allocates nothing).  Limited to
+    ceil(n / blocksize) <= 4,194,304 outer blocks.  Calls that overlap on
+    the GPU share one scratch array and race: keep them on one stream.
+    """
+    device = packed.device
+    npk, nb, ng = sizes(n, blocksize, nested_blocksize)
+    _check(packed, "packed", torch.uint8, npk, device)
+    _check(scale_codes, "scale_codes", torch.uint8, nb, device)
+    _check(nested_absmax, "nested_absmax", torch.float32, ng, device)
+    _check(scale_codebook, "scale_codebook", torch.float32, 256, device)
+    _check(value_codebook, "value_codebook", torch.float32, 16, device)
+    if out is not None:
+        out_dtype = out.dtype
+    if out_dtype not in _DTYPE_CODE:
+        raise TypeError(f"out_dtype: unsupported {out_dtype}")
+    res = _out_tensor(out, out_dtype, n, device)
+    st = get_lib().dq4_nested_unfused_static(
+        _ptr(packed), _ptr(scale_codes), _ptr(nested_absmax), _ptr(scale_codebook),
+        _ptr(value_codebook), float(offset), n, blocksize, nested_blocksize,
+        _DTYPE_CODE[out_dtype], _ptr(res), _stream_handle(stream, device))
+    if st:
+        raise Dq4Error(st, "dq4_nested_unfused_static")
+    return res

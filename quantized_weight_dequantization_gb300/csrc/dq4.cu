@@ -585,6 +585,8 @@ const char* dq4_status_string(int status) {
     case DQ4_ERR_DEVICE: return "the current CUDA device could not be queried";
     case DQ4_ERR_ARCH: return "the current device is not compute capability 10.3 (GB300)";
     case DQ4_ERR_LAUNCH: return "the CUDA runtime reported an error at kernel launch";
+    case DQ4_ERR_TOO_LARGE:
+      return "ceil(n / blocksize) exceeds DQ4_STATIC_SCRATCH_BLOCKS (the static scratch array)";
     default: return "unknown status";
   }
 }
@@ -592,3 +594,52 @@ const char* dq4_status_string(int status) {
 int dq4_last_cuda_error(void) { return t_last_cuda_error; }
 
 }  // extern "C"
+
+// ------------------------------------------------ allocation-free variant
+// The FP32 scale scratch of the unfused sequence, as a fixed array in the
+// library, for callers that may not allocate device memory.  Host code
+// must not use the symbol itself as a pointer (on the host it only names
+// the array); its device address is looked up once per device.
+namespace {
+
+static __device__ __align__(256) float g_static_scale_scratch[DQ4_STATIC_SCRATCH_BLOCKS];
+
+std::atomic<float*> g_static_scratch_addr[kMaxDevices];
+
+// Device address of the scratch array on the current device `dev`.
+int static_scratch_address(int dev, float** out) {
+  if (dev < 0 || dev >= kMaxDevices) return fail_cuda(DQ4_ERR_DEVICE, cudaErrorInvalidDevice);
+  float* ptr = g_static_scratch_addr[dev].load(std::memory_order_acquire);
+  if (ptr == nullptr) {
+    void* addr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&addr, g_static_scale_scratch);
+    if (e != cudaSuccess || addr == nullptr)
+      return fail_cuda(DQ4_ERR_DEVICE, e != cudaSuccess ? e : cudaErrorInvalidSymbol);
+    ptr = static_cast<float*>(addr);
+    g_static_scratch_addr[dev].store(ptr, std::memory_order_release);
+  }
+  *out = ptr;
+  return DQ4_OK;
+}
+
+}  // namespace
+
+extern "C" int dq4_nested_unfused_static(const uint8_t* packed, const uint8_t* scale_codes,
+                                         const float* nested_absmax, const float* scale_codebook,
+                                         const float* value_codebook, float offset, int64_t n,
+                                         int32_t blocksize, int32_t nested_blocksize,
+                                         int32_t out_dtype, void* out, void* stream) {
+  if (int st = validate(n, blocksize, nested_blocksize, true, out_dtype)) return st;
+  if (n == 0) return DQ4_OK;
+  if ((n + blocksize - 1) / blocksize > int64_t(DQ4_STATIC_SCRATCH_BLOCKS))
+    return DQ4_ERR_TOO_LARGE;
+  if (!packed || !scale_codes || !nested_absmax || !scale_codebook || !value_codebook || !out)
+    return DQ4_ERR_NULL;
+  int dev = 0, sms = 0;
+  if (int st = current_device(&dev, &sms)) return st;
+  float* scratch = nullptr;
+  if (int st = static_scratch_address(dev, &scratch)) return st;
+  return dq4_nested_unfused(packed, scale_codes, nested_absmax, scale_codebook, value_codebook,
+                            offset, n, blocksize, nested_blocksize, out_dtype, out, scratch,
+                            stream);
+}

@@ -35,7 +35,8 @@ def _declared_constants():
 def test_header_declares_the_boundary():
     names = _declared_functions()
     assert names == sorted(["dq4_abi_version", "dq4_nested", "dq4", "dq4_nested_unfused",
-                            "dq4_status_string", "dq4_last_cuda_error"]), names
+                            "dq4_nested_unfused_static", "dq4_status_string",
+                            "dq4_last_cuda_error"]), names
 
 
 def test_library_exports_every_declared_symbol(dq):
@@ -61,7 +62,7 @@ def test_header_constants_match_binding(dq):
 
 
 def test_status_strings(dq):
-    for code in range(0, 10):
+    for code in range(0, 11):
         s = dq.lib.dq4_status_string(code)
         assert s and s != b"unknown status", code
     assert dq.lib.dq4_status_string(1234) == b"unknown status"
@@ -98,6 +99,12 @@ def test_host_validation_before_any_cuda_call(dq):
     assert L.dq4(nz, nz, nz, 0, 64, 0, nz, None) == 0
     assert L.dq4_nested_unfused(nz, nz, nz, nz, nz, 0.0, 10, 64, 256, 0, nz, None, None) == 1
     assert L.dq4_nested_unfused(nz, nz, nz, nz, nz, 0.0, 10, 64, 256, 0, nz, nz + 1, None) == 6
+    # allocation-free form: the static scratch limit is checked before anything else runs
+    limit = _declared_constants()["DQ4_STATIC_SCRATCH_BLOCKS"]
+    assert L.dq4_nested_unfused_static(nz, nz, nz, nz, nz, 0.0, 64 * limit + 1, 64, 256, 0, nz,
+                                       None) == 10
+    assert L.dq4_nested_unfused_static(nz, nz, nz, nz, nz, 0.0, 0, 64, 256, 0, nz, None) == 0
+    assert L.dq4_nested_unfused_static(None, nz, nz, nz, nz, 0.0, 100, 64, 256, 0, nz, None) == 1
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device status")
