@@ -63,8 +63,8 @@ def parse_args():
     ap.add_argument("--compare-batches", type=int, default=7)
     ap.add_argument("--sets", type=int, default=N_SETS,
                     help="rotating device buffer sets (each larger than L2)")
-    ap.add_argument("--event-every", type=int, default=16,
-                    help="bracket every m-th timed launch with its own event pair")
+    ap.add_argument("--isolated-launches", type=int, default=100,
+                    help="launches timed one by one (own event pair) after the timed region")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-compare", action="store_true")
@@ -255,15 +255,10 @@ def run_ours(args):
     for i in range(W):
         if fused(i):
             raise SystemExit("dq4_nested failed in warm-up")
-    # batch boundaries (>= 7 batches) and a sample of single launches, each with
-    # its own event pair; all other launches run back to back
+    # batch boundaries (>= 7 batches); the launches run back to back
     nb = max(1, min(K, max(7, min(20, K // 50))))
     edges = sorted(set(np.linspace(0, K, nb + 1).astype(int).tolist()))
     ev_b = {e: torch.cuda.Event(enable_timing=True) for e in edges}
-    every = max(1, args.event_every)
-    sampled = list(range(every // 2, K, every)) or [0]
-    ev_s = {i: torch.cuda.Event(enable_timing=True) for i in sampled}
-    ev_e = {i: torch.cuda.Event(enable_timing=True) for i in sampled}
     gpu_uuid = None
     try:
         u = str(torch.cuda.get_device_properties(dev).uuid)
@@ -281,12 +276,7 @@ def run_ours(args):
     for i in range(K):
         if i in ev_b:
             ev_b[i].record(stream)
-        if i in ev_s:
-            ev_s[i].record(stream)
-            bad |= fused(W + i)
-            ev_e[i].record(stream)
-        else:
-            bad |= fused(W + i)
+        bad |= fused(W + i)
     ev_b[K].record(stream)
     torch.cuda.synchronize(dev)
     barrier()
@@ -295,9 +285,25 @@ def run_ours(args):
     if bad:
         raise SystemExit(f"dq4_nested returned status {bad} in the timed region")
     elapsed_ms = max_over_ranks(ev_b[0].elapsed_time(ev_b[K]))
-    launch_ms = [ev_s[i].elapsed_time(ev_e[i]) for i in sampled]
-    avg_launch_ms = float(np.mean(launch_ms))
+    # The timed region launches this one kernel and nothing else (one launch per
+    # step; the ncu launch list of this command shows a 100 % share), so its
+    # average launch duration is the region's time over K.
+    share = 1.0
+    avg_launch_ms = elapsed_ms * share / K
     batch_ms = [ev_b[a].elapsed_time(ev_b[b]) / (b - a) for a, b in zip(edges[:-1], edges[1:])]
+
+    # launches timed one by one (each between its own events, so no overlap with
+    # a neighbour): not part of the timed region
+    iso_ms = []
+    for i in range(max(0, args.isolated_launches)):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fused(i)
+        e1.record(stream)
+        iso_ms.append((e0, e1))
+    torch.cuda.synchronize(dev)
+    iso_ms = [a.elapsed_time(b) for a, b in iso_ms]
 
     # ---- interleaved fused / unfused comparison (not part of the timed region)
     cmp_f, cmp_u = [], []
@@ -393,7 +399,10 @@ def run_ours(args):
             "kernel": "dq4_vec_kernel<f16,nested>" if cell.out == "f16"
             else f"dq4_vec_kernel<{cell.out},nested>",
             "avg_launch_us": avg_launch_ms * 1e3,
-            "launches_sampled": len(launch_ms),
+            "share_of_timed_region": share,
+            "isolated_launch_us": {"median": pct(iso_ms, 50) * 1e3, "p10": pct(iso_ms, 10) * 1e3,
+                                   "p90": pct(iso_ms, 90) * 1e3, "count": len(iso_ms)}
+            if iso_ms else None,
         },
         "batches_us_per_step": [round(x * 1e3, 3) for x in batch_ms],
         "batch_stats_us": {"median": pct(batch_ms, 50) * 1e3, "p10": pct(batch_ms, 10) * 1e3,
