@@ -59,6 +59,9 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cell", default=DEFAULT_CELL, choices=sorted(gen.CELLS))
+    ap.add_argument("--op", choices=["nested", "transposed"], default="nested",
+                    help="nested: dq4_nested (flat output); transposed: dq4_nested_transposed "
+                         "(W^T output of the rows x cols weight)")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--compare-batches", type=int, default=7)
     ap.add_argument("--sets", type=int, default=N_SETS,
@@ -227,20 +230,40 @@ def run_ours(args):
     bs, nbs = p.blocksize, p.nested_blocksize
     scb_p, vcb_p = scb.data_ptr(), vcb.data_ptr()
 
+    transposed = args.op == "transposed"
+    rows, cols = cell.rows, cell.cols
+
     def fused(i):
         pk, cd, am, o, _ = ptrs[i % n_sets]
-        return L.dq4_nested(pk, cd, am, scb_p, vcb_p, off, n, bs, nbs, code, o, sh)
+        if not transposed:
+            return L.dq4_nested(pk, cd, am, scb_p, vcb_p, off, n, bs, nbs, code, o, sh)
+        return L.dq4_nested_transposed(pk, cd, am, scb_p, vcb_p, off, rows, cols, bs, nbs, code,
+                                       o, sh)
 
     def unfused(i):
         pk, cd, am, o, sc = ptrs[i % n_sets]
         return L.dq4_nested_unfused(pk, cd, am, scb_p, vcb_p, off, n, bs, nbs, code, o, sc, sh)
 
     # correctness gate before timing: first and last 64 Ki values of the fused
-    # output vs the unfused sequence (bit-identical by construction)
+    # output vs the unfused sequence (bit-identical by construction); for the
+    # transposed op, its first 64 rows vs the flat output's first 64 columns
+    if transposed:
+        ref = torch.empty_like(sets[0]["out"])
+        pk, cd, am, _, _ = ptrs[0]
+        assert fused(0) == 0
+        assert L.dq4_nested(pk, cd, am, scb_p, vcb_p, off, n, bs, nbs, code, ref.data_ptr(),
+                            sh) == 0
+        torch.cuda.synchronize(dev)
+        iv = torch.int32 if ref.element_size() == 4 else torch.int16
+        t_rows = sets[0]["out"].view(cols, rows)[:64].view(iv)
+        f_cols = ref.view(rows, cols)[:, :64].t().contiguous().view(iv)
+        if not torch.equal(t_rows, f_cols):
+            raise SystemExit("transposed and flat outputs differ; refusing to time")
+        del ref, t_rows, f_cols
     assert fused(0) == 0
     torch.cuda.synchronize(dev)
     a = sets[0]["out"].clone()
-    assert unfused(0) == 0
+    assert (unfused(0) if not transposed else fused(0)) == 0
     torch.cuda.synchronize(dev)
     b = sets[0]["out"]
     if not (torch.equal(a[:65536].view(torch.int16 if a.element_size() == 2 else torch.int32),
@@ -308,7 +331,7 @@ def run_ours(args):
     # ---- interleaved fused / unfused comparison (not part of the timed region)
     cmp_f, cmp_u = [], []
     per = 200
-    for j in range(0 if args.no_compare else args.compare_batches):
+    for j in range(0 if (args.no_compare or transposed) else args.compare_batches):
         for fn, acc in ((fused, cmp_f), (unfused, cmp_u)):
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
@@ -335,8 +358,13 @@ def run_ours(args):
         s0["absmax"].copy_(pin["nested_absmax"], non_blocking=True)
         scb.copy_(pin["scale_codebook"], non_blocking=True)
         vcb.copy_(pin["value_codebook"], non_blocking=True)
-        dq.dq4_nested(s0["packed"], s0["codes"], s0["absmax"], scb, vcb, off, n, bs, nbs,
-                      out_dtype, out=s0["out"], stream=stream)
+        if transposed:
+            dq.dq4_nested_transposed(s0["packed"], s0["codes"], s0["absmax"], scb, vcb, off,
+                                     rows, cols, bs, nbs, out_dtype, out=s0["out"],
+                                     stream=stream)
+        else:
+            dq.dq4_nested(s0["packed"], s0["codes"], s0["absmax"], scb, vcb, off, n, bs, nbs,
+                          out_dtype, out=s0["out"], stream=stream)
         host_out.copy_(s0["out"], non_blocking=True)
 
     e2e_ms = None
@@ -379,7 +407,9 @@ def run_ours(args):
         "config": {
             "workload": f"{cell.rows}x{cell.cols} {cell.fmt.upper()}-style nested 4-bit dequant, "
                         f"blocksize {cell.blocksize}, nested blocksize {cell.nested_blocksize}, "
-                        f"{cell.out.upper()} out ({cell.name})",
+                        f"{cell.out.upper()} out ({cell.name})"
+                        + (", transposed output" if transposed else ""),
+            "op": args.op,
             "n_values": n, "blocksize": cell.blocksize,
             "nested_blocksize": cell.nested_blocksize, "format": cell.fmt,
             "out_dtype": cell.out, "offset": cell.offset,
@@ -396,8 +426,8 @@ def run_ours(args):
             "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
             else "fallback 6.8 TB/s",
             "frac_of_nominal_8tbs": achieved_gbs / 8000.0,
-            "kernel": "dq4_vec_kernel<f16,nested>" if cell.out == "f16"
-            else f"dq4_vec_kernel<{cell.out},nested>",
+            "kernel": (f"dq4_transposed_kernel<{cell.out}>" if transposed
+                       else f"dq4_vec_kernel<{cell.out},nested>"),
             "avg_launch_us": avg_launch_ms * 1e3,
             "share_of_timed_region": share,
             "isolated_launch_us": {"median": pct(iso_ms, 50) * 1e3, "p10": pct(iso_ms, 10) * 1e3,
@@ -425,7 +455,7 @@ def run_ours(args):
         "gpu": torch.cuda.get_device_name(dev),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(p, cell)
+        out["cpu_baseline"] = cpu_baseline(p, cell, transposed)
     if world > 1:
         dist.destroy_process_group()
     if rank == 0:
@@ -433,7 +463,7 @@ def run_ours(args):
 
 
 # --------------------------------------------------------- CPU baseline
-def cpu_baseline(p, cell, repeats: int = 3):
+def cpu_baseline(p, cell, transposed: bool = False, repeats: int = 3):
     """The CPU oracle, as it stands, over the whole workload on all host cores."""
     import oracle
 
@@ -442,7 +472,10 @@ def cpu_baseline(p, cell, repeats: int = 3):
     times = []
     for _ in range(repeats):
         t0 = time.perf_counter()
-        oracle.dq4_nested(p, cell.out, threads=threads)
+        if transposed:
+            oracle.dq4_nested_transposed(p, cell.rows, cell.cols, cell.out, threads=threads)
+        else:
+            oracle.dq4_nested(p, cell.out, threads=threads)
         times.append(time.perf_counter() - t0)
     t = statistics.median(times)
     return {"value": p.n / t, "unit": UNIT, "cores": threads, "kind": "oracle",

@@ -60,7 +60,7 @@ extern "C" {
 /* Status codes. */
 #define DQ4_OK 0
 #define DQ4_ERR_NULL 1             /* a required pointer is NULL while n > 0 */
-#define DQ4_ERR_N 2                /* n < 0 */
+#define DQ4_ERR_N 2                /* n < 0 (or rows, cols < 0 / rows * cols too large) */
 #define DQ4_ERR_BLOCKSIZE 3        /* blocksize not a power of two in [32, 4096] */
 #define DQ4_ERR_NESTED_BLOCKSIZE 4 /* nested_blocksize not a power of two >= 1 */
 #define DQ4_ERR_DTYPE 5            /* out_dtype not one of DQ4_OUT_* */
@@ -93,6 +93,25 @@ int dq4_nested(const uint8_t* packed, const uint8_t* scale_codes, const float* n
                const float* scale_codebook, const float* value_codebook, float offset,
                int64_t n, int32_t blocksize, int32_t nested_blocksize, int32_t out_dtype,
                void* out, void* stream);
+
+/*
+ * Fused nested dequantization with transposed output: one kernel launch.
+ * The n = rows * cols values are the row-major rows x cols weight W (value
+ * i = W[i / cols][i % cols], exactly as dq4_nested reads them), and `out`
+ * receives W^T row-major (cols x rows): value (r, c) goes to
+ * out[c * rows + r].  Arguments and per-value arithmetic are those of
+ * dq4_nested; rows and cols must be >= 0 and rows * cols must fit in
+ * int64 (DQ4_ERR_N otherwise).  Source: issue #21, section "Correctness
+ * requirements", which lists the op's transposed-output behaviour among
+ * the cases that must stay bitwise identical.  Fastest when cols % 8 == 0
+ * and rows * element size % 16 == 0 (other shapes take per-element loads or
+ * stores inside the same kernel).
+ */
+int dq4_nested_transposed(const uint8_t* packed, const uint8_t* scale_codes,
+                          const float* nested_absmax, const float* scale_codebook,
+                          const float* value_codebook, float offset, int64_t rows,
+                          int64_t cols, int32_t blocksize, int32_t nested_blocksize,
+                          int32_t out_dtype, void* out, void* stream);
 
 /*
  * Non-nested dequantization (a plain FP32 absmax per block): one launch.

@@ -64,10 +64,11 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_nested_scale.restype = f32
     lib.oracle_dq4_nested.argtypes = [p, p, p, p, p, f32, i64, i64, i64, i32, p]
     lib.oracle_dq4.argtypes = [p, p, p, i64, i64, i32, p]
+    lib.oracle_dq4_nested_transposed.argtypes = [p, p, p, p, p, f32, i64, i64, i64, i64, i32, p]
     lib.oracle_nested_scales.argtypes = [p, p, p, f32, i64, i64, p]
     for name in ("oracle_f32_to_f16_array", "oracle_f32_to_bf16_array",
                  "oracle_convert_bit_range", "oracle_dq4_nested", "oracle_dq4",
-                 "oracle_nested_scales"):
+                 "oracle_nested_scales", "oracle_dq4_nested_transposed"):
         getattr(lib, name).restype = None
     return lib
 
@@ -124,6 +125,27 @@ def dq4_nested(problem, out: str = "f16", threads: int = 1, lib=None) -> np.ndar
         for t in ts:
             t.join()
     return res
+
+
+def dq4_nested_transposed(problem, rows: int, cols: int, out: str = "f16",
+                          threads: int = 1, lib=None) -> np.ndarray:
+    """Dequantize ``problem`` as a rows x cols weight and return W^T flat (cols x rows).
+
+    With ``threads > 1`` the threaded flat oracle runs and numpy's transpose
+    (a library primitive) is the last step; the arithmetic is unchanged.
+    """
+    lib = lib or load()
+    p = problem
+    assert rows * cols == p.n
+    if threads <= 1:
+        res = np.empty(p.n, dtype=OUT_NP[out])
+        lib.oracle_dq4_nested_transposed(
+            _ptr(p.packed), _ptr(p.scale_codes), _ptr(p.nested_absmax), _ptr(p.scale_codebook),
+            _ptr(p.value_codebook), float(p.offset), rows, cols, p.blocksize,
+            p.nested_blocksize, OUT_CODES[out], _ptr(res))
+        return res
+    flat = dq4_nested(p, out, threads=threads, lib=lib).reshape(rows, cols)
+    return np.ascontiguousarray(flat.T).reshape(-1)
 
 
 def dq4(packed: np.ndarray, absmax: np.ndarray, value_codebook: np.ndarray, n: int,

@@ -153,6 +153,27 @@ void oracle_dq4_nested(const uint8_t* packed, const uint8_t* scale_codes,
     }
 }
 
+/* Transposed output: the flat values are the row-major rows x cols weight W
+ * (value i = W[i / cols][i % cols]); out holds W^T row-major, so element
+ * (r, c) of W goes to out[c * rows + r].  Same per-value arithmetic. */
+void oracle_dq4_nested_transposed(const uint8_t* packed, const uint8_t* scale_codes,
+                                  const float* nested_absmax, const float* scale_codebook,
+                                  const float* value_codebook, float offset, int64_t rows,
+                                  int64_t cols, int64_t blocksize, int64_t nested_blocksize,
+                                  int out_dtype, void* out) {
+    for (int64_t r = 0; r < rows; r++) {
+        for (int64_t c = 0; c < cols; c++) {
+            const int64_t i = r * cols + c;
+            const int64_t b = i / blocksize;
+            const int64_t g = b / nested_blocksize;
+            const float scale = oracle_nested_scale(scale_codes[b], nested_absmax[g],
+                                                    scale_codebook, offset);
+            const float v = value_codebook[nibble_of(packed, i)] * scale;
+            store_value(out, c * rows + r, v, out_dtype);
+        }
+    }
+}
+
 /* Non-nested dequantization: the per-block FP32 absmax is given directly. */
 void oracle_dq4(const uint8_t* packed, const float* absmax, const float* value_codebook,
                 int64_t n, int64_t blocksize, int out_dtype, void* out) {

@@ -51,6 +51,8 @@ def _load() -> ctypes.CDLL:
     L.dq4_abi_version.restype = ctypes.c_int
     L.dq4_nested.argtypes = [p, p, p, p, p, f32, i64, i32, i32, i32, p, p]
     L.dq4_nested.restype = ctypes.c_int
+    L.dq4_nested_transposed.argtypes = [p, p, p, p, p, f32, i64, i64, i32, i32, i32, p, p]
+    L.dq4_nested_transposed.restype = ctypes.c_int
     L.dq4.argtypes = [p, p, p, i64, i32, i32, p, p]
     L.dq4.restype = ctypes.c_int
     L.dq4_nested_unfused.argtypes = [p, p, p, p, p, f32, i64, i32, i32, i32, p, p, p]
@@ -151,6 +153,40 @@ def dq4_nested(packed: torch.Tensor, scale_codes: torch.Tensor, nested_absmax: t
     if st:
         raise Dq4Error(st, "dq4_nested")
     return res
+
+
+def dq4_nested_transposed(packed: torch.Tensor, scale_codes: torch.Tensor,
+                          nested_absmax: torch.Tensor, scale_codebook: torch.Tensor,
+                          value_codebook: torch.Tensor, offset: float, rows: int, cols: int,
+                          blocksize: int = 64, nested_blocksize: int = 256,
+                          out_dtype: torch.dtype = torch.float16,
+                          out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Fused nested dequantization of a rows x cols weight, written transposed.
+
+    Returns ``out`` shaped (cols, rows): out[c, r] is the dequantized value
+    (r, c).  Same arithmetic as :func:`dq4_nested` (issue #21, section
+    "Correctness requirements": transposed output stays bitwise identical).
+    """
+    device = packed.device
+    n = rows * cols
+    npk, nb, ng = sizes(n, blocksize, nested_blocksize)
+    _check(packed, "packed", torch.uint8, npk, device)
+    _check(scale_codes, "scale_codes", torch.uint8, nb, device)
+    _check(nested_absmax, "nested_absmax", torch.float32, ng, device)
+    _check(scale_codebook, "scale_codebook", torch.float32, 256, device)
+    _check(value_codebook, "value_codebook", torch.float32, 16, device)
+    if out is not None:
+        out_dtype = out.dtype
+    if out_dtype not in _DTYPE_CODE:
+        raise TypeError(f"out_dtype: unsupported {out_dtype}")
+    res = _out_tensor(out, out_dtype, n, device)
+    st = get_lib().dq4_nested_transposed(
+        _ptr(packed), _ptr(scale_codes), _ptr(nested_absmax), _ptr(scale_codebook),
+        _ptr(value_codebook), float(offset), rows, cols, blocksize, nested_blocksize,
+        _DTYPE_CODE[out_dtype], _ptr(res), _stream_handle(stream, device))
+    if st:
+        raise Dq4Error(st, "dq4_nested_transposed")
+    return res.view(cols, rows) if out is None else res
 
 
 def dq4(packed: torch.Tensor, absmax: torch.Tensor, value_codebook: torch.Tensor, n: int,

@@ -34,7 +34,8 @@ def _declared_constants():
 
 def test_header_declares_the_boundary():
     names = _declared_functions()
-    assert names == sorted(["dq4_abi_version", "dq4_nested", "dq4", "dq4_nested_unfused",
+    assert names == sorted(["dq4_abi_version", "dq4_nested", "dq4_nested_transposed", "dq4",
+                            "dq4_nested_unfused",
                             "dq4_nested_unfused_static", "dq4_status_string",
                             "dq4_last_cuda_error"]), names
 
@@ -99,6 +100,15 @@ def test_host_validation_before_any_cuda_call(dq):
     assert L.dq4(nz, nz, nz, 0, 64, 0, nz, None) == 0
     assert L.dq4_nested_unfused(nz, nz, nz, nz, nz, 0.0, 10, 64, 256, 0, nz, None, None) == 1
     assert L.dq4_nested_unfused(nz, nz, nz, nz, nz, 0.0, 10, 64, 256, 0, nz, nz + 1, None) == 6
+    # transposed form: rows / cols validated on the host
+    T = L.dq4_nested_transposed
+    assert T(nz, nz, nz, nz, nz, 0.0, -1, 8, 64, 256, 0, nz, None) == 2
+    assert T(nz, nz, nz, nz, nz, 0.0, 8, -1, 64, 256, 0, nz, None) == 2
+    assert T(nz, nz, nz, nz, nz, 0.0, 1 << 40, 1 << 40, 64, 256, 0, nz, None) == 2
+    assert T(None, None, None, None, None, 0.0, 0, 77, 64, 256, 0, None, None) == 0
+    assert T(nz, nz, nz, nz, nz, 0.0, 8, 8, 48, 256, 0, nz, None) == 3
+    assert T(nz, None, nz, nz, nz, 0.0, 8, 8, 64, 256, 0, nz, None) == 1
+    assert T(nz, nz, nz, nz, nz, 0.0, 8, 8, 64, 256, 0, nz + 1, None) == 6
     # allocation-free form: the static scratch limit is checked before anything else runs
     limit = _declared_constants()["DQ4_STATIC_SCRATCH_BLOCKS"]
     assert L.dq4_nested_unfused_static(nz, nz, nz, nz, nz, 0.0, 64 * limit + 1, 64, 256, 0, nz,

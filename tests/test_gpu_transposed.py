@@ -1,0 +1,125 @@
+"""Transposed-output dequantization on the GPU, bit for bit against the oracle.
+
+dq4_nested_transposed writes W^T for the row-major rows x cols weight W:
+out[c * rows + r] is value (r, c) ("Fuse nested scale reconstruction into
+SM103 4-bit dequantization", bitsandbytes issue #21, section "Correctness
+requirements": transposed output must stay bitwise identical).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import dq4_inputs as gen
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+DT = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module")
+def dq():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import quantized_weight_dequantization_gb300 as m
+    return m
+
+
+def to_dev(p):
+    return {k: torch.from_numpy(np.ascontiguousarray(getattr(p, k))).to(DEV)
+            for k in ("packed", "scale_codes", "nested_absmax", "scale_codebook",
+                      "value_codebook")}
+
+
+def bits(t):
+    t = t.detach().reshape(-1).cpu()
+    return t.view(torch.int32 if t.dtype == torch.float32 else torch.int16).numpy().view(
+        np.uint32 if t.dtype == torch.float32 else np.uint16)
+
+
+def want_bits(a):
+    return a.view(np.uint32) if a.dtype == np.float32 else a
+
+
+def run(dq, p, t, rows, cols, kind, **kw):
+    return dq.dq4_nested_transposed(t["packed"], t["scale_codes"], t["nested_absmax"],
+                                    t["scale_codebook"], t["value_codebook"], float(p.offset),
+                                    rows, cols, p.blocksize, p.nested_blocksize, DT[kind], **kw)
+
+
+def check(dq, p, rows, cols, kind, threads=16, **kw):
+    t = to_dev(p)
+    got = run(dq, p, t, rows, cols, kind, **kw)
+    want = oracle.dq4_nested_transposed(p, rows, cols, kind, threads=threads)
+    g, w = bits(got), want_bits(want)
+    if not np.array_equal(g, w):
+        bad = np.flatnonzero(g != w)
+        raise AssertionError(f"{rows}x{cols} {kind}: {bad.size} values differ, first {bad[:5]}")
+
+
+SHAPES = [
+    (1, 1), (1, 8), (8, 1), (3, 5), (63, 65), (64, 64), (65, 64), (64, 72), (127, 129),
+    (96, 40), (200, 8), (8, 200), (1, 4096), (4096, 1), (130, 1000), (1000, 130),
+    (257, 264), (512, 4095), (4095, 512), (333, 777),
+]
+
+
+@pytest.mark.parametrize("rows,cols", SHAPES)
+def test_small_shapes_all_dtypes(dq, rows, cols):
+    for bs, nbs in ((32, 1), (64, 256), (4096, 2)):
+        p = gen.make_problem(rows * cols, bs, nbs, "nf4" if bs == 64 else "fp4", 0.5, -0.52,
+                             seed=rows * 1000 + cols + bs)
+        for kind in DT:
+            check(dq, p, rows, cols, kind, threads=1)
+
+
+@pytest.mark.parametrize("name,rows,cols", [("C3a", 11008, 4096), ("C3c", 4096, 11008),
+                                            ("C2a", 4097, 4095), ("C2b", 4097, 4095),
+                                            ("C1", 4096, 4096)])
+def test_cells(dq, name, rows, cols):
+    cell = gen.CELLS[name]
+    check(dq, cell.problem(), rows, cols, cell.out)
+
+
+@pytest.mark.parametrize("name", ["C4a", "C4d"])
+def test_large_weight(dq, name):
+    cell = gen.CELLS[name]
+    check(dq, cell.problem(), cell.rows, cell.cols, cell.out)
+
+
+def test_every_code_transposed(dq):
+    p = gen.enumeration_problem(0.52, blocksize=32, groups=4)
+    rows, cols = 256, p.n // 256
+    for kind in DT:
+        check(dq, p, rows, cols, kind, threads=1)
+
+
+def test_unaligned_output_and_canaries(dq):
+    rows, cols = 200, 136
+    p = gen.make_problem(rows * cols, 64, 256, "fp4", 0.5, 0.1, seed=5)
+    t = to_dev(p)
+    for kind in DT:
+        isz = torch.empty(0, dtype=DT[kind]).element_size()
+        guard = 4096
+        buf = torch.full((rows * cols * isz + 2 * guard + isz,), 0x5A, dtype=torch.uint8,
+                         device=DEV)
+        # out shifted by one element: 16-byte stores cannot be used
+        view = buf[guard + isz:guard + isz + rows * cols * isz].view(DT[kind])
+        run(dq, p, t, rows, cols, kind, out=view)
+        host = buf.cpu().numpy()
+        assert np.all(host[:guard + isz] == 0x5A) and np.all(host[guard + isz + rows * cols * isz:]
+                                                             == 0x5A), kind
+        assert np.array_equal(bits(view), want_bits(oracle.dq4_nested_transposed(p, rows, cols,
+                                                                                  kind)))
+
+
+def test_zero_and_errors(dq):
+    p = gen.make_problem(64, 64, 256, "nf4", 0.5, 0.1, seed=1)
+    t = to_dev(p)
+    z = run(dq, p, t, 0, 17, "f16")
+    assert z.numel() == 0
+    with pytest.raises(dq.Dq4Error, match="BLOCKSIZE"):
+        dq.dq4_nested_transposed(t["packed"], t["scale_codes"], t["nested_absmax"],
+                                 t["scale_codebook"], t["value_codebook"], 0.1, 8, 8, 8192, 256)

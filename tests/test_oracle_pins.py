@@ -307,3 +307,24 @@ def test_threaded_oracle_equals_single_thread():
     p = gen.CELLS["C2a"].problem()
     assert np.array_equal(oracle.dq4_nested(p, "bf16", threads=1),
                           oracle.dq4_nested(p, "bf16", threads=5))
+
+
+def test_transposed_oracle_index_map():
+    """W^T output: out[c*rows + r] is the value (r, c) of the flat row-major definition.
+
+    Pinned against numpy's transpose of the flat oracle (itself pinned above)
+    and against exact evaluation of single elements.
+    """
+    for rows, cols, bs, nbs in ((1, 1, 32, 1), (3, 5, 32, 1), (65, 130, 32, 2), (64, 64, 64, 256),
+                                (17, 4096, 4096, 1), (4097, 3, 64, 256)):
+        p = gen.make_problem(rows * cols, bs, nbs, "fp4", 0.5, -0.52, seed=rows * 7 + cols)
+        ex = exact.dequantize(p) if rows * cols <= 5000 else None
+        for out in OUTS:
+            t = oracle.dq4_nested_transposed(p, rows, cols, out)
+            flat = oracle.dq4_nested(p, out)
+            assert np.array_equal(t.reshape(cols, rows).view(np.uint8),
+                                  np.ascontiguousarray(flat.reshape(rows, cols).T).view(np.uint8))
+            if ex is not None:
+                for r, c in ((0, 0), (rows - 1, cols - 1), (rows // 2, cols // 3)):
+                    got = _bits(t[c * rows + r:c * rows + r + 1], out)[0]
+                    assert got == ex[out][r * cols + c], (rows, cols, r, c, out)
