@@ -430,16 +430,26 @@ __device__ __forceinline__ void store_pair(void* out, int64_t o, float v0, float
 // order.
 constexpr int kSR = 128;                 // CTA tile rows
 constexpr int kSC = 256;                 // CTA tile columns (128 packed bytes per row)
-constexpr int kSRowBytes = kSC / 2 + 16; // padded smem row (16-byte aligned)
+constexpr int kSRowBytes = kSC / 2;      // smem row: 8 chunks of 16 B, XOR-swizzled
 constexpr int kSSeg = kSC / 32;          // 32-value scale segments per row
 
+// 16-byte chunk `ch` of staged row `rr` sits at chunk position ch ^ key(rr):
+// lanes reading rows 2p (and 2p + 1) of 8 consecutive p then hit 8 distinct
+// chunk positions, i.e. all 32 banks.
+__device__ __forceinline__ int swz(int rr, int ch) { return ch ^ ((rr >> 1) & 7); }
+
+// minimum resident CTAs per SM the staged transposed kernel is compiled for
+#ifndef DQ4_T_MIN_CTAS
+#define DQ4_T_MIN_CTAS 8
+#endif
+
 template <int OUT, bool kStoreVec>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, DQ4_T_MIN_CTAS)
     dq4_transposed_kernel(const Args a, int64_t rows, int64_t cols, uint32_t tiles_r) {
   __shared__ float s_vcb[16];
   __shared__ float s_scb[256];
   __shared__ __align__(16) uint8_t s_pk[kSR][kSRowBytes];
-  __shared__ float s_sc[kSR][kSSeg];
+  __shared__ __align__(8) float s_sc[kSSeg][kSR];  // [segment][row]: a lane's 2 rows are a float2
 #if DQ4_PDL
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
@@ -458,7 +468,7 @@ __global__ void __launch_bounds__(kThreads)
     uint4 v = make_uint4(0, 0, 0, 0);
     if (r < rows && c < cols)
       v = __ldcs(reinterpret_cast<const uint4*>(a.packed + ((r * cols + c) >> 1)));
-    *reinterpret_cast<uint4*>(&s_pk[rr][16 * ch]) = v;
+    *reinterpret_cast<uint4*>(&s_pk[rr][16 * swz(rr, ch)]) = v;
   }
   __syncthreads();  // codebooks staged
   // scales of the 32-value segments (bs >= 32 and cols % 32 == 0: one block each)
@@ -467,7 +477,7 @@ __global__ void __launch_bounds__(kThreads)
     const int id = threadIdx.x + kThreads * k;
     const int rr = id / kSSeg, q = id % kSSeg;
     const int64_t r = r0 + rr, c = c0 + 32 * q;
-    s_sc[rr][q] = (r < rows && c < cols) ? nested_scale(a, s_scb, (r * cols + c) >> a.log2_bs)
+    s_sc[q][rr] = (r < rows && c < cols) ? nested_scale(a, s_scb, (r * cols + c) >> a.log2_bs)
                                          : 0.f;
   }
   __syncthreads();
@@ -486,10 +496,11 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
   for (int q = 0; q < 2; ++q) {
     if (32 * q >= ncol) break;
-    const uint4 s0 = *reinterpret_cast<const uint4*>(&s_pk[lr][wc / 2 + 16 * q]);
-    const uint4 s1 = *reinterpret_cast<const uint4*>(&s_pk[lr + 1][wc / 2 + 16 * q]);
-    const float sc0 = s_sc[lr][wc / 32 + q];
-    const float sc1 = s_sc[lr + 1][wc / 32 + q];
+    const int ch = wc / 32 + q;  // 16-byte chunk of this 32-column half
+    const uint4 s0 = *reinterpret_cast<const uint4*>(&s_pk[lr][16 * swz(lr, ch)]);
+    const uint4 s1 = *reinterpret_cast<const uint4*>(&s_pk[lr + 1][16 * swz(lr + 1, ch)]);
+    const float2 scp = *reinterpret_cast<const float2*>(&s_sc[ch][lr]);
+    const float sc0 = scp.x, sc1 = scp.y;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {  // packed word k: 8 columns
       const uint32_t w0 = k == 0 ? s0.x : k == 1 ? s0.y : k == 2 ? s0.z : s0.w;
