@@ -296,3 +296,59 @@ def describe(problem: Problem, out: Optional[str] = None) -> str:
     return (f"n={problem.n} bs={problem.blocksize} nbs={problem.nested_blocksize} "
             f"packed={npk}B codes={nb} absmax={ng} offset={float(problem.offset)!r}"
             + (f" out={out}" if out else ""))
+
+
+# ------------------------------------------- LLM.int8 correction operands
+STREAM_A = 11
+STREAM_CB = 12
+STREAM_SCB = 13
+STREAM_COLS = 14
+
+
+@dataclasses.dataclass
+class Int8Problem:
+    """Inputs of the LLM.int8 correction-operand preparation (host arrays)."""
+
+    A_bits: np.ndarray  # uint16[M, K]: raw 16-bit activations (gathered bit for bit)
+    CB: np.ndarray      # int8[N, K]: row-major int8 weights, the full code domain
+    SCB: np.ndarray     # float32[N]: per-row statistics
+    cols: np.ndarray    # int64[L]: outlier column indices in [0, K)
+
+    @property
+    def shape(self):
+        return self.A_bits.shape[0], self.CB.shape[0], self.A_bits.shape[1], self.cols.size
+
+
+def make_int8_problem(M: int, N: int, K: int, L: int, seed: int = 0,
+                      cols_mode: str = "sorted", scb_sigma: float = 1.0) -> Int8Problem:
+    """Random FP16-like activations, uniform int8 codes, lognormal row statistics.
+
+    cols_mode: "sorted" (sorted distinct), "unsorted" (distinct, shuffled),
+    "repeated" (with repeats), "edges" (contains 0 and K - 1).
+    """
+    a = uniform_bytes(seed, STREAM_A, 2 * M * K).view(np.uint16).reshape(M, K).copy()
+    cb = uniform_bytes(seed, STREAM_CB, N * K).view(np.int8).reshape(N, K).copy()
+    scb = lognormal_f32(seed, STREAM_SCB, N, scb_sigma)
+    w = splitmix64(seed, STREAM_COLS, max(1, 4 * L))
+    if L == 0:
+        cols = np.zeros(0, dtype=np.int64)
+    elif cols_mode == "repeated":
+        cols = (w[:L] % np.uint64(K)).astype(np.int64)
+        cols[L // 2:] = cols[:L - L // 2]
+    else:
+        # distinct columns: the L smallest random keys among a K-long key array
+        keys = splitmix64(seed, STREAM_COLS + 100, K)
+        pick = np.argsort(keys, kind="stable")[:L].astype(np.int64)
+        if cols_mode == "sorted":
+            cols = np.sort(pick)
+        elif cols_mode == "edges":
+            cols = np.sort(pick)
+            cols[0], cols[-1] = 0, K - 1
+        else:
+            cols = pick
+    return Int8Problem(A_bits=a, CB=cb, SCB=scb, cols=cols)
+
+
+INT8_GRID_M = (1, 8, 64, 512, 2048)
+INT8_GRID_KN = (3584, 4096, 8192, 14336)
+INT8_GRID_L = (0, 1, 5, 16, 64)

@@ -66,9 +66,11 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_dq4.argtypes = [p, p, p, i64, i64, i32, p]
     lib.oracle_dq4_nested_transposed.argtypes = [p, p, p, p, p, f32, i64, i64, i64, i64, i32, p]
     lib.oracle_nested_scales.argtypes = [p, p, p, f32, i64, i64, p]
+    lib.oracle_int8_correction_prep.argtypes = [p, p, p, p, i64, i64, i64, i64, p, p]
     for name in ("oracle_f32_to_f16_array", "oracle_f32_to_bf16_array",
                  "oracle_convert_bit_range", "oracle_dq4_nested", "oracle_dq4",
-                 "oracle_nested_scales", "oracle_dq4_nested_transposed"):
+                 "oracle_nested_scales", "oracle_dq4_nested_transposed",
+                 "oracle_int8_correction_prep"):
         getattr(lib, name).restype = None
     return lib
 
@@ -198,3 +200,24 @@ def convert_bit_range(first: int, count: int, to_bf16: bool, lib=None) -> np.nda
     y = np.empty(count, dtype=np.uint16)
     lib.oracle_convert_bit_range(first, count, int(to_bf16), _ptr(y))
     return y
+
+
+def int8_correction_prep(A_bits: np.ndarray, CB: np.ndarray, SCB: np.ndarray, cols: np.ndarray,
+                         lib=None):
+    """LLM.int8 correction operands (issue #16): (subA[M, L], subB[L, N]) as uint16 bits."""
+    lib = lib or load()
+    M, K = A_bits.shape
+    N = CB.shape[0]
+    L = cols.size
+    A_bits = np.ascontiguousarray(A_bits, dtype=np.uint16)
+    CB = np.ascontiguousarray(CB, dtype=np.int8)
+    SCB = np.ascontiguousarray(SCB, dtype=np.float32)
+    cols = np.ascontiguousarray(cols, dtype=np.int64)
+    assert CB.shape[1] == K and SCB.size == N
+    assert L == 0 or (cols.min() >= 0 and cols.max() < K)
+    subA = np.empty((M, L), dtype=np.uint16)
+    subB = np.empty((L, N), dtype=np.uint16)
+    if L:
+        lib.oracle_int8_correction_prep(_ptr(A_bits), _ptr(CB), _ptr(SCB), _ptr(cols), M, N, K,
+                                        L, _ptr(subA), _ptr(subB))
+    return subA, subB

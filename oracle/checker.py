@@ -68,3 +68,20 @@ def dq4_nested(problem, out: str = "f16", chunk_values: int = 1 << 24) -> np.nda
     if not parts:
         return to_out_bits(np.empty(0, dtype=np.float32), out)
     return np.concatenate(parts)
+
+
+def int8_correction_prep(A_bits, CB, SCB, cols):
+    """Second implementation of the LLM.int8 correction operands (issue #16).
+
+    subA is a numpy fancy-index gather of the raw bits; subB is two float32
+    ufunc multiplies (CB * SCB, then * float32(1)/float32(127)) and numpy's
+    float16 cast, transposed.
+    """
+    subA = np.ascontiguousarray(A_bits[:, cols])
+    recip = np.float32(1) / np.float32(127)
+    t1 = CB[:, cols].astype(np.float32) * SCB.astype(np.float32)[:, None]
+    t2 = t1 * recip
+    assert t2.dtype == np.float32
+    with np.errstate(over="ignore"):
+        subB = np.ascontiguousarray(t2.T.astype(np.float16).view(np.uint16))
+    return subA, subB

@@ -191,3 +191,29 @@ void oracle_nested_scales(const uint8_t* scale_codes, const float* nested_absmax
         scales[b] = oracle_nested_scale(scale_codes[b], nested_absmax[b / nested_blocksize],
                                         scale_codebook, offset);
 }
+
+/* ------------------------------------------------------------------------
+ * LLM.int8 correction-operand preparation: "Fuse LLM.int8 correction
+ * operand preparation into one CUDA kernel" (bitsandbytes issue #16),
+ * sections "Summary", "Bounded method" and "Exact correctness oracle":
+ *   subA[m][l] = A[m][cols[l]]                               (raw 16-bit copy)
+ *   subB[l][n] = RN16( RN32( RN32(CB[n][cols[l]] * SCB[n]) * RN32(1/127) ) )
+ * A is M x K (16-bit elements), CB is N x K int8, SCB has N FP32 entries,
+ * cols has L column indices in [0, K) (repeats allowed).  The reciprocal-127
+ * constant is the FP32 quotient 1/127 rounded once.
+ * ---------------------------------------------------------------------- */
+void oracle_int8_correction_prep(const uint16_t* A, const int8_t* CB, const float* SCB,
+                                 const int64_t* cols, int64_t M, int64_t N, int64_t K,
+                                 int64_t L, uint16_t* subA, uint16_t* subB) {
+    const float recip127 = 1.0f / 127.0f;
+    for (int64_t m = 0; m < M; m++)
+        for (int64_t l = 0; l < L; l++)
+            subA[m * L + l] = A[m * K + cols[l]];
+    for (int64_t l = 0; l < L; l++) {
+        for (int64_t n = 0; n < N; n++) {
+            const float t1 = (float)CB[n * K + cols[l]] * SCB[n];   /* RN32(CB * SCB) */
+            const float t2 = t1 * recip127;                         /* RN32(t1 * 1/127) */
+            subB[l * N + n] = oracle_f32_to_f16(t2);
+        }
+    }
+}
