@@ -59,9 +59,13 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cell", default=DEFAULT_CELL, choices=sorted(gen.CELLS))
-    ap.add_argument("--op", choices=["nested", "transposed"], default="nested",
+    ap.add_argument("--op", choices=["nested", "transposed", "int8prep"], default="nested",
                     help="nested: dq4_nested (flat output); transposed: dq4_nested_transposed "
-                         "(W^T output of the rows x cols weight)")
+                         "(W^T output of the rows x cols weight); int8prep: LLM.int8 "
+                         "correction-operand preparation (--m, --kn, --l)")
+    ap.add_argument("--m", type=int, default=2048, help="int8prep: activation rows M")
+    ap.add_argument("--kn", type=int, default=14336, help="int8prep: K = N")
+    ap.add_argument("--l", type=int, default=64, help="int8prep: outlier columns L")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--compare-batches", type=int, default=7)
     ap.add_argument("--sets", type=int, default=N_SETS,
@@ -543,10 +547,82 @@ def run_reference(args):
     }), flush=True)
 
 
+def run_int8prep(args):
+    """Time dq4_int8_correction_prep on one (M, K = N, L) cell of the preparation grid."""
+    import torch
+
+    import quantized_weight_dequantization_gb300 as dq
+
+    dev = torch.device("cuda:0")
+    M, KN, L = args.m, args.kn, args.l
+    sets = []
+    for k in range(3):  # the gathered CB sectors (N * L * 32 B) would otherwise stay in L2
+        p = gen.make_int8_problem(M, KN, KN, L, seed=100 + k)
+        sets.append(dict(p=p, A=torch.from_numpy(p.A_bits).to(dev).view(torch.float16),
+                         CB=torch.from_numpy(p.CB).to(dev), SCB=torch.from_numpy(p.SCB).to(dev),
+                         cols=torch.from_numpy(p.cols).to(dev),
+                         subA=torch.empty((M, L), dtype=torch.float16, device=dev),
+                         subB=torch.empty((L, KN), dtype=torch.float16, device=dev)))
+    L_ = dq.get_lib()
+    sh = torch.cuda.current_stream(dev).cuda_stream
+
+    def call(i):
+        t = sets[i % 3]
+        return L_.dq4_int8_correction_prep(t["A"].data_ptr(), t["CB"].data_ptr(),
+                                           t["SCB"].data_ptr(), t["cols"].data_ptr(), M, KN, KN,
+                                           L, t["subA"].data_ptr(), t["subB"].data_ptr(), None, sh)
+
+    # correctness gate
+    import oracle
+    assert call(0) == 0
+    torch.cuda.synchronize(dev)
+    p0 = sets[0]["p"]
+    wa, wb = oracle.int8_correction_prep(p0.A_bits, p0.CB, p0.SCB, p0.cols)
+    ga = sets[0]["subA"].cpu().view(torch.int16).numpy().view(np.uint16)
+    gb = sets[0]["subB"].cpu().view(torch.int16).numpy().view(np.uint16)
+    if not (np.array_equal(ga, wa) and np.array_equal(gb, wb)):
+        raise SystemExit("int8 preparation differs from the oracle; refusing to time")
+    for i in range(args.warmup):
+        call(i)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record()
+    bad = 0
+    for i in range(args.steps):
+        bad |= call(i)
+    e1.record()
+    torch.cuda.synchronize(dev)
+    if bad:
+        raise SystemExit(f"status {bad}")
+    us = e0.elapsed_time(e1) / args.steps * 1e3
+    outs = M * L + L * KN
+    alg = M * L * 2 * 2 + KN * L * 1 + KN * 4 + L * 8 + L * KN * 2
+    sector = M * L * 32 + M * L * 2 + KN * L * 32 + KN * 4 + L * 8 + L * KN * 2
+    t0 = time.perf_counter()
+    for _ in range(3):
+        oracle.int8_correction_prep(p0.A_bits, p0.CB, p0.SCB, p0.cols)
+    cpu_s = (time.perf_counter() - t0) / 3
+    print(json.dumps({
+        "metric": "LLM.int8 correction-operand preparation (subA + subB outputs/s)",
+        "value": outs / (us / 1e6), "unit": "outputs/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": us / 1e3, "us_per_call": us,
+        "higher_is_better": True, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"int8 correction prep M={M} K=N={KN} L={L}", "M": M, "K": KN,
+                   "N": KN, "L": L, "l2": "3 rotating input sets"},
+        "algorithmic_gbs": alg / (us / 1e6) / 1e9,
+        "sector_gbs": sector / (us / 1e6) / 1e9,
+        "gpu_launches": args.steps,
+        "cpu_baseline": {"value": outs / cpu_s, "unit": "outputs/s", "cores": 1,
+                         "kind": "oracle", "sample": "the same cell, median of 3"},
+    }), flush=True)
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.op == "int8prep":
+        run_int8prep(args)
     else:
         run_ours(args)
 

@@ -174,6 +174,31 @@ int dq4_nested_unfused_static(const uint8_t* packed, const uint8_t* scale_codes,
                               int32_t blocksize, int32_t nested_blocksize, int32_t out_dtype,
                               void* out, void* stream);
 
+/*
+ * LLM.int8 correction-operand preparation in one launch.  Source: "Fuse
+ * LLM.int8 correction operand preparation into one CUDA kernel"
+ * (bitsandbytes issue #16), sections "Summary", "Bounded method" and
+ * "Exact correctness oracle":
+ *   subA[m][l] = A[m][cols[l]]                      (16-bit copy, bit for bit)
+ *   subB[l][n] = RN16( RN32( RN32(CB[n][cols[l]] * SCB[n]) * RN32(1/127) ) )
+ *   A        uint16[M][K]  16-bit activations (FP16 or BF16 bits), row-major
+ *   CB       int8[N][K]    int8 weights, row-major
+ *   SCB      float[N]      per-row statistics
+ *   cols     int64[L]      outlier column indices; repeats allowed
+ *   subA     uint16[M][L]  written row-major (the gather of A's columns)
+ *   subB     uint16[L][N]  FP16, written row-major (the transposed dequantized
+ *                          columns, the layout the correction GEMM consumes)
+ *   bad_cols optional device int (NULL to skip): incremented once per index
+ *            outside [0, K); such an index reads nothing and yields zeros.
+ * L == 0 (no outliers) is a successful no-op.  M, N, K, L >= 0 and K >= 1
+ * when L > 0 (DQ4_ERR_N otherwise).  Pointers aligned to their element
+ * types (DQ4_ERR_ALIGN).  Fastest when N is even and subB 4-byte / SCB
+ * 8-byte aligned.
+ */
+int dq4_int8_correction_prep(const uint16_t* A, const int8_t* CB, const float* SCB,
+                             const int64_t* cols, int64_t M, int64_t N, int64_t K, int64_t L,
+                             uint16_t* subA, uint16_t* subB, int* bad_cols, void* stream);
+
 /* A static, human-readable string for a status code (never NULL). */
 const char* dq4_status_string(int status);
 

@@ -59,6 +59,8 @@ def _load() -> ctypes.CDLL:
     L.dq4_nested_unfused.restype = ctypes.c_int
     L.dq4_nested_unfused_static.argtypes = [p, p, p, p, p, f32, i64, i32, i32, i32, p, p]
     L.dq4_nested_unfused_static.restype = ctypes.c_int
+    L.dq4_int8_correction_prep.argtypes = [p, p, p, p, i64, i64, i64, i64, p, p, p, p]
+    L.dq4_int8_correction_prep.restype = ctypes.c_int
     L.dq4_status_string.argtypes = [ctypes.c_int]
     L.dq4_status_string.restype = ctypes.c_char_p
     L.dq4_last_cuda_error.argtypes = []
@@ -273,3 +275,45 @@ def dq4_nested_unfused_static(packed: torch.Tensor, scale_codes: torch.Tensor,
     if st:
         raise Dq4Error(st, "dq4_nested_unfused_static")
     return res
+
+
+def int8_correction_prep(A: torch.Tensor, CB: torch.Tensor, SCB: torch.Tensor,
+                         cols: torch.Tensor, subA: Optional[torch.Tensor] = None,
+                         subB: Optional[torch.Tensor] = None,
+                         bad_cols: Optional[torch.Tensor] = None, stream=None):
+    """LLM.int8 correction operands in one launch: returns (subA[M, L], subB[L, N]).
+
+    "Fuse LLM.int8 correction operand preparation into one CUDA kernel"
+    (bitsandbytes issue #16): subA = A[:, cols] (bit for bit); subB is the
+    FP16 dequantization RN16(RN32(RN32(CB * SCB) * RN32(1/127))) of CB's
+    columns ``cols``, transposed.  ``bad_cols`` (an int32 CUDA tensor of one
+    element) counts indices outside [0, K).
+    """
+    if A.dim() != 2 or CB.dim() != 2:
+        raise ValueError("A and CB must be 2-D")
+    device = A.device
+    M, K = A.shape
+    N = CB.shape[0]
+    if CB.shape[1] != K:
+        raise ValueError(f"CB has {CB.shape[1]} columns, A has {K}")
+    Lc = cols.numel()
+    if A.dtype not in (torch.float16, torch.bfloat16):
+        raise TypeError("A must be float16 or bfloat16")
+    _check(A, "A", A.dtype, M * K, device)
+    _check(CB, "CB", torch.int8, N * K, device)
+    _check(SCB, "SCB", torch.float32, N, device)
+    _check(cols, "cols", torch.int64, Lc, device)
+    if subA is None:
+        subA = torch.empty((M, Lc), dtype=A.dtype, device=device)
+    if subB is None:
+        subB = torch.empty((Lc, N), dtype=torch.float16, device=device)
+    _check(subA, "subA", A.dtype, M * Lc, device)
+    _check(subB, "subB", torch.float16, Lc * N, device)
+    if bad_cols is not None:
+        _check(bad_cols, "bad_cols", torch.int32, 1, device)
+    st = get_lib().dq4_int8_correction_prep(
+        _ptr(A), _ptr(CB), _ptr(SCB), _ptr(cols), M, N, K, Lc, _ptr(subA), _ptr(subB),
+        _ptr(bad_cols), _stream_handle(stream, device))
+    if st:
+        raise Dq4Error(st, "dq4_int8_correction_prep")
+    return subA, subB
