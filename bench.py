@@ -59,13 +59,18 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cell", default=DEFAULT_CELL, choices=sorted(gen.CELLS))
-    ap.add_argument("--op", choices=["nested", "transposed", "int8prep"], default="nested",
+    ap.add_argument("--op", choices=["nested", "transposed", "int8prep", "outprod"],
+                    default="nested",
                     help="nested: dq4_nested (flat output); transposed: dq4_nested_transposed "
                          "(W^T output of the rows x cols weight); int8prep: LLM.int8 "
                          "correction-operand preparation (--m, --kn, --l)")
     ap.add_argument("--m", type=int, default=2048, help="int8prep: activation rows M")
     ap.add_argument("--kn", type=int, default=14336, help="int8prep: K = N")
     ap.add_argument("--l", type=int, default=64, help="int8prep: outlier columns L")
+    ap.add_argument("--rows", type=int, default=600000, help="outprod: rows of W (summed over)")
+    ap.add_argument("--cols", type=int, default=256, help="outprod: columns of W")
+    ap.add_argument("--ncols", type=int, default=256, help="outprod: columns of G")
+    ap.add_argument("--transient-mib", type=int, default=256, help="outprod: transient bound")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--compare-batches", type=int, default=7)
     ap.add_argument("--sets", type=int, default=N_SETS,
@@ -617,12 +622,74 @@ def run_int8prep(args):
     }), flush=True)
 
 
+def run_outprod(args):
+    """Time dq4_nested_out_prod (row blocks, bounded transient) against the whole-copy path."""
+    import torch
+
+    import quantized_weight_dequantization_gb300 as dq
+
+    dev = torch.device("cuda:0")
+    rows, cols, ncols = args.rows, args.cols, args.ncols
+    p = gen.make_problem(rows * cols, 64, 256, "nf4", 0.5, 0.0371, seed=7)
+    t = {k: torch.from_numpy(np.ascontiguousarray(getattr(p, k))).to(dev)
+         for k in ("packed", "scale_codes", "nested_absmax", "scale_codebook", "value_codebook")}
+    G = torch.from_numpy(gen.make_normal_g(rows, ncols, seed=8)).to(dev)
+    dst = torch.empty((cols, ncols), dtype=torch.float32, device=dev)
+    budget = args.transient_mib << 20
+    transient = torch.empty(max(1, min(rows, budget // (4 * cols))) * cols, dtype=torch.float32,
+                            device=dev)
+
+    def blocked():
+        dq.out_prod(t["packed"], t["scale_codes"], t["nested_absmax"], t["scale_codebook"],
+                    t["value_codebook"], float(p.offset), rows, cols, G, dst=dst,
+                    transient=transient, transient_bytes=budget)
+
+    full = torch.empty((rows, cols), dtype=torch.float32, device=dev)
+
+    def whole():  # dequantize all of W to FP32, then one GEMM
+        dq.dq4_nested(t["packed"], t["scale_codes"], t["nested_absmax"], t["scale_codebook"],
+                      t["value_codebook"], float(p.offset), rows * cols, 64, 256, torch.float32,
+                      out=full.view(-1))
+        torch.mm(full.t(), G, out=dst)
+
+    def timeit(fn, k):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record()
+        for _ in range(k):
+            fn()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / k
+
+    k = max(1, args.steps)
+    ms_blocked = timeit(blocked, k)
+    ms_whole = timeit(whole, k)
+    flops = 2.0 * rows * cols * ncols
+    nblocks = -(-rows // max(1, transient.numel() // cols))
+    print(json.dumps({
+        "metric": "row-blocked dequant + GEMM (dst = W^T G) time",
+        "value": ms_blocked, "unit": "ms", "higher_is_better": False, "n_gpus": 1,
+        "steps": k, "warmup": args.warmup, "ms_per_step": ms_blocked,
+        "config": {"workload": f"out_prod rows={rows} cols={cols} ncols={ncols}, transient "
+                               f"<= {args.transient_mib} MiB ({nblocks} blocks)"},
+        "gemm_tflops": flops / (ms_blocked / 1e3) / 1e12,
+        "whole_copy_ms": ms_whole,
+        "transient_bytes": transient.numel() * 4, "whole_copy_bytes": rows * cols * 4,
+        "gpu_launches_per_step": 2 * nblocks,
+    }), flush=True)
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
     elif args.op == "int8prep":
         run_int8prep(args)
+    elif args.op == "outprod":
+        run_outprod(args)
     else:
         run_ours(args)
 

@@ -352,3 +352,35 @@ def make_int8_problem(M: int, N: int, K: int, L: int, seed: int = 0,
 INT8_GRID_M = (1, 8, 64, 512, 2048)
 INT8_GRID_KN = (3584, 4096, 8192, 14336)
 INT8_GRID_L = (0, 1, 5, 16, 64)
+
+
+# ------------------------------------------ dequantization feeding a GEMM
+STREAM_G = 21
+
+
+def make_integer_problem(rows: int, cols: int, blocksize: int = 64, nested_blocksize: int = 256,
+                         seed: int = 0) -> Problem:
+    """A nested problem whose dequantized values are small integers (|w| <= 16).
+
+    Value codebook entries are integers in [-4, 3], scale codebook entries
+    integers in [-4, 4], nested absmax 1 and offset 0, so every scale and
+    every value is an exact integer.
+    """
+    p = make_problem(rows * cols, blocksize, nested_blocksize, "nf4", 0.5, 0.0, seed)
+    vcb = (np.arange(16) % 8 - 4).astype(np.float32)
+    scb = (np.arange(256) % 9 - 4).astype(np.float32)
+    return dataclasses.replace(p, value_codebook=vcb, scale_codebook=scb,
+                               nested_absmax=np.ones_like(p.nested_absmax),
+                               offset=np.float32(0.0))
+
+
+def make_ternary_g(rows: int, ncols: int, seed: int = 0) -> np.ndarray:
+    """rows x ncols FP32 matrix of values in {-1, 0, 1}."""
+    w = splitmix64(seed, STREAM_G, rows * ncols)
+    return ((w % np.uint64(3)).astype(np.int64) - 1).astype(np.float32).reshape(rows, ncols)
+
+
+def make_normal_g(rows: int, ncols: int, seed: int = 0) -> np.ndarray:
+    """rows x ncols FP32 standard normal matrix (Box-Muller, float64, rounded once)."""
+    return np.log(lognormal_f32(seed, STREAM_G, rows * ncols, 1.0).astype(np.float64)
+                  ).astype(np.float32).reshape(rows, ncols)

@@ -68,7 +68,8 @@ extern "C" {
 #define DQ4_ERR_DEVICE 7           /* no current CUDA device could be queried */
 #define DQ4_ERR_ARCH 8             /* current device is not compute capability 10.3 */
 #define DQ4_ERR_LAUNCH 9           /* the CUDA runtime reported an error at launch */
-#define DQ4_ERR_TOO_LARGE 10       /* n needs more scratch than the library's static array */
+#define DQ4_ERR_TOO_LARGE 10       /* more scratch needed than given (static array, transient) */
+#define DQ4_ERR_CUBLAS 11          /* cuBLAS could not be loaded or reported an error */
 
 /* Version of this interface (incremented on any change of a signature). */
 int dq4_abi_version(void);
@@ -198,6 +199,33 @@ int dq4_nested_unfused_static(const uint8_t* packed, const uint8_t* scale_codes,
 int dq4_int8_correction_prep(const uint16_t* A, const int8_t* CB, const float* SCB,
                              const int64_t* cols, int64_t M, int64_t N, int64_t K, int64_t L,
                              uint16_t* subA, uint16_t* subB, int* bad_cols, void* stream);
+
+/*
+ * Row-blocked dequantization feeding a GEMM, with a bounded transient:
+ *   dst = W^T * G       W = the FP32 dequantization of the rows x cols weight
+ * (dq4_nested's values read row-major), G a rows x ncols FP32 matrix, dst a
+ * cols x ncols FP32 matrix, all row-major.  The sum runs over W's rows, in
+ * blocks of as many rows as `transient` holds (at least one row): each block
+ * is dequantized to FP32 into `transient` and a cuBLAS GEMM accumulates it
+ * into dst with beta = 0 for the first block and 1 after.  Source: "cuda:
+ * out_prod dequantizes a 2D weight in row blocks" (llama.cpp pull request
+ * #4), sections "What" and the approving review (the blocked sum, beta 0 then
+ * 1, the transient bound of at most 256 MiB).
+ *   transient        device float buffer of transient_bytes (>= 4 * cols)
+ *   cublas_handle    a cublasHandle_t of the cuBLAS already loaded in the
+ *                    process (e.g. the framework's); its stream is set to
+ *                    `stream`; GEMMs run with FP32 compute
+ * The dequantized blocks are bit-identical to dq4_nested's FP32 output; the
+ * GEMM follows cuBLAS's FP32 accumulation.  rows == 0 zero-fills dst.
+ * DQ4_ERR_TOO_LARGE if transient_bytes < 4 * cols; DQ4_ERR_CUBLAS if cuBLAS
+ * cannot be loaded or fails; cols, ncols must fit in int32.
+ */
+int dq4_nested_out_prod(const uint8_t* packed, const uint8_t* scale_codes,
+                        const float* nested_absmax, const float* scale_codebook,
+                        const float* value_codebook, float offset, int64_t rows, int64_t cols,
+                        int32_t blocksize, int32_t nested_blocksize, const float* G,
+                        int64_t ncols, float* dst, float* transient, int64_t transient_bytes,
+                        void* cublas_handle, void* stream);
 
 /* A static, human-readable string for a status code (never NULL). */
 const char* dq4_status_string(int status);

@@ -221,3 +221,15 @@ def int8_correction_prep(A_bits: np.ndarray, CB: np.ndarray, SCB: np.ndarray, co
         lib.oracle_int8_correction_prep(_ptr(A_bits), _ptr(CB), _ptr(SCB), _ptr(cols), M, N, K,
                                         L, _ptr(subA), _ptr(subB))
     return subA, subB
+
+
+def out_prod(problem, rows: int, cols: int, G: np.ndarray, threads: int = 8, lib=None):
+    """dst = W^T G in float64: W is the oracle's FP32 dequantization (rows x cols).
+
+    The FP32 values of W are exact in float64; numpy's float64 matmul (a
+    library primitive) is the contraction.  Reading: "cuda: out_prod
+    dequantizes a 2D weight in row blocks" (llama.cpp pull request #4),
+    section "What": out_prod sums over the weight's rows.
+    """
+    w = dq4_nested(problem, "f32", threads=threads, lib=lib).reshape(rows, cols)
+    return w.astype(np.float64).T @ np.asarray(G, dtype=np.float64)

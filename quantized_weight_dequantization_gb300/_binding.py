@@ -24,6 +24,7 @@ STATUS_NAMES = {
     0: "DQ4_OK", 1: "DQ4_ERR_NULL", 2: "DQ4_ERR_N", 3: "DQ4_ERR_BLOCKSIZE",
     4: "DQ4_ERR_NESTED_BLOCKSIZE", 5: "DQ4_ERR_DTYPE", 6: "DQ4_ERR_ALIGN",
     7: "DQ4_ERR_DEVICE", 8: "DQ4_ERR_ARCH", 9: "DQ4_ERR_LAUNCH", 10: "DQ4_ERR_TOO_LARGE",
+    11: "DQ4_ERR_CUBLAS",
 }
 
 
@@ -61,6 +62,9 @@ def _load() -> ctypes.CDLL:
     L.dq4_nested_unfused_static.restype = ctypes.c_int
     L.dq4_int8_correction_prep.argtypes = [p, p, p, p, i64, i64, i64, i64, p, p, p, p]
     L.dq4_int8_correction_prep.restype = ctypes.c_int
+    L.dq4_nested_out_prod.argtypes = [p, p, p, p, p, f32, i64, i64, i32, i32, p, i64, p, p, i64,
+                                      p, p]
+    L.dq4_nested_out_prod.restype = ctypes.c_int
     L.dq4_status_string.argtypes = [ctypes.c_int]
     L.dq4_status_string.restype = ctypes.c_char_p
     L.dq4_last_cuda_error.argtypes = []
@@ -317,3 +321,50 @@ def int8_correction_prep(A: torch.Tensor, CB: torch.Tensor, SCB: torch.Tensor,
     if st:
         raise Dq4Error(st, "dq4_int8_correction_prep")
     return subA, subB
+
+
+TRANSIENT_BYTES_DEFAULT = 256 << 20
+
+
+def out_prod(packed: torch.Tensor, scale_codes: torch.Tensor, nested_absmax: torch.Tensor,
+             scale_codebook: torch.Tensor, value_codebook: torch.Tensor, offset: float,
+             rows: int, cols: int, G: torch.Tensor, blocksize: int = 64,
+             nested_blocksize: int = 256, dst: Optional[torch.Tensor] = None,
+             transient: Optional[torch.Tensor] = None,
+             transient_bytes: int = TRANSIENT_BYTES_DEFAULT, stream=None) -> torch.Tensor:
+    """dst = W^T G with W the rows x cols dequantized weight, in bounded row blocks.
+
+    "cuda: out_prod dequantizes a 2D weight in row blocks" (llama.cpp pull
+    request #4): each block of rows is dequantized to FP32 into ``transient``
+    (at most ``transient_bytes``) and accumulated into dst by a cuBLAS GEMM,
+    beta 0 for the first block and 1 after.  Returns dst (cols x ncols, FP32).
+    """
+    device = packed.device
+    n = rows * cols
+    npk, nb, ng = sizes(n, blocksize, nested_blocksize)
+    _check(packed, "packed", torch.uint8, npk, device)
+    _check(scale_codes, "scale_codes", torch.uint8, nb, device)
+    _check(nested_absmax, "nested_absmax", torch.float32, ng, device)
+    _check(scale_codebook, "scale_codebook", torch.float32, 256, device)
+    _check(value_codebook, "value_codebook", torch.float32, 16, device)
+    if G.dim() != 2 or G.shape[0] != rows:
+        raise ValueError(f"G must be rows x ncols ({rows} x ...), got {tuple(G.shape)}")
+    ncols = G.shape[1]
+    _check(G, "G", torch.float32, rows * ncols, device)
+    if dst is None:
+        dst = torch.empty((cols, ncols), dtype=torch.float32, device=device)
+    _check(dst, "dst", torch.float32, cols * ncols, device)
+    if transient is None:
+        rb = max(1, min(rows, transient_bytes // max(1, 4 * cols)))
+        transient = torch.empty(max(1, rb * cols), dtype=torch.float32, device=device)
+    _check(transient, "transient", torch.float32, 1, device)
+    transient_bytes = min(transient_bytes, transient.numel() * 4)
+    handle = torch.cuda.current_blas_handle()
+    st = get_lib().dq4_nested_out_prod(
+        _ptr(packed), _ptr(scale_codes), _ptr(nested_absmax), _ptr(scale_codebook),
+        _ptr(value_codebook), float(offset), rows, cols, blocksize, nested_blocksize, _ptr(G),
+        ncols, _ptr(dst), _ptr(transient), transient_bytes, handle,
+        _stream_handle(stream, device))
+    if st:
+        raise Dq4Error(st, "dq4_nested_out_prod")
+    return dst

@@ -42,9 +42,13 @@
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
 
+#include <cublas_v2.h>  // types only: cuBLAS is reached through dlopen / dlsym
+#include <dlfcn.h>
+
 #include <atomic>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <utility>
 
 #include "dq4.h"
@@ -71,6 +75,7 @@ struct Args {
   const float* vcb;       // value codebook
   void* out;
   int64_t n;
+  int64_t first;  // per-value kernel: output i is the value first + i (0 elsewhere)
   int64_t nblocks;
   float offset;
   int log2_bs;
@@ -683,7 +688,7 @@ __global__ void __launch_bounds__(kThreads) dq4_scalar_kernel(const Args a) {
   stage_codebooks<NESTED>(a, s_vcb, s_scb);
   const int64_t stride = int64_t(gridDim.x) * kThreads;
   for (int64_t i = int64_t(blockIdx.x) * kThreads + threadIdx.x; i < a.n; i += stride)
-    store_one<OUT>(a.out, i, value_at<NESTED>(a, s_scb, s_vcb, i));
+    store_one<OUT>(a.out, i, value_at<NESTED>(a, s_scb, s_vcb, a.first + i));
 }
 
 // Unfused step 1: FP32 scale buffer from the codes (no offset yet).
@@ -888,6 +893,7 @@ Args make_args(const uint8_t* packed, const uint8_t* codes, const float* absmax,
   a.vcb = vcb;
   a.out = out;
   a.n = n;
+  a.first = 0;
   a.nblocks = (n + blocksize - 1) / blocksize;
   a.offset = offset;
   a.log2_bs = log2_exact(blocksize);
@@ -1025,6 +1031,133 @@ int dq4_int8_correction_prep(const uint16_t* A, const int8_t* CB, const float* S
   return launch_kernel(int8_prep_kernel<false>, grid, st, p);
 }
 
+}  // extern "C"
+
+// --------------------------------------------- row-blocked dequant + GEMM
+namespace {
+
+using CublasSetStream = cublasStatus_t (*)(cublasHandle_t, cudaStream_t);
+using CublasGemmEx = cublasStatus_t (*)(cublasHandle_t, cublasOperation_t, cublasOperation_t,
+                                        int, int, int, const void*, const void*, cudaDataType,
+                                        int, const void*, cudaDataType, int, const void*, void*,
+                                        cudaDataType, int, cublasComputeType_t,
+                                        cublasGemmAlgo_t);
+struct CublasApi {
+  CublasSetStream set_stream = nullptr;
+  CublasGemmEx gemm = nullptr;
+};
+
+// The cuBLAS already loaded in the process (the one the caller's handle
+// belongs to), else the system's; resolved once.
+const CublasApi* cublas_api() {
+  static std::once_flag once;
+  static CublasApi api;
+  std::call_once(once, [] {
+    void* h = dlopen("libcublas.so.13", RTLD_NOW | RTLD_NOLOAD);
+    if (!h) h = dlopen("libcublas.so.13", RTLD_NOW);
+    if (!h) h = dlopen("libcublas.so", RTLD_NOW);
+    if (!h) return;
+    api.set_stream = reinterpret_cast<CublasSetStream>(dlsym(h, "cublasSetStream_v2"));
+    api.gemm = reinterpret_cast<CublasGemmEx>(dlsym(h, "cublasGemmEx"));
+  });
+  return (api.set_stream && api.gemm) ? &api : nullptr;
+}
+
+int64_t gcd64(int64_t x, int64_t y) {
+  while (y) {
+    const int64_t t = x % y;
+    x = y;
+    y = t;
+  }
+  return x;
+}
+
+// FP32 values [first, first + count) of the flat problem, one by one (for
+// row blocks that do not start on a nested-group boundary).
+int launch_range_f32(Args a, int64_t first, int64_t count, float* out, cudaStream_t stream) {
+  int dev = 0, sms = 0;
+  if (int st = current_device(&dev, &sms)) return st;
+  a.first = first;
+  a.n = count;
+  a.out = out;
+  static std::atomic<int> occ_cache[kMaxDevices];
+  auto kernel = dq4_scalar_kernel<DQ4_OUT_F32, true>;
+  int64_t grid = (count + kThreads - 1) / kThreads;
+  const int64_t cap = int64_t(sms) * ctas_per_sm(kernel, dev, occ_cache);
+  if (grid > cap) grid = cap;
+  kernel<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(a);
+  return check_launch();
+}
+
+}  // namespace
+
+extern "C" {
+
+int dq4_nested_out_prod(const uint8_t* packed, const uint8_t* scale_codes,
+                        const float* nested_absmax, const float* scale_codebook,
+                        const float* value_codebook, float offset, int64_t rows, int64_t cols,
+                        int32_t blocksize, int32_t nested_blocksize, const float* G,
+                        int64_t ncols, float* dst, float* transient, int64_t transient_bytes,
+                        void* cublas_handle, void* stream) {
+  if (rows < 0 || cols < 0 || ncols < 0) return DQ4_ERR_N;
+  if (cols > 0 && rows > INT64_MAX / cols) return DQ4_ERR_N;
+  const int64_t n = rows * cols;
+  if (int st = validate(n, blocksize, nested_blocksize, true, DQ4_OUT_F32)) return st;
+  if (cols == 0 || ncols == 0) return DQ4_OK;
+  if (cols > INT32_MAX || ncols > INT32_MAX) return DQ4_ERR_N;  // cuBLAS dimensions
+  if (!dst) return DQ4_ERR_NULL;
+  if (misaligned(dst, 4)) return DQ4_ERR_ALIGN;
+  const auto st = static_cast<cudaStream_t>(stream);
+  if (rows == 0) {  // an empty sum
+    const cudaError_t e = cudaMemsetAsync(dst, 0, size_t(cols) * size_t(ncols) * 4, st);
+    return e == cudaSuccess ? DQ4_OK : fail_cuda(DQ4_ERR_LAUNCH, e);
+  }
+  if (!packed || !scale_codes || !nested_absmax || !scale_codebook || !value_codebook || !G ||
+      !transient || !cublas_handle)
+    return DQ4_ERR_NULL;
+  if (misaligned(nested_absmax, 4) || misaligned(scale_codebook, 4) ||
+      misaligned(value_codebook, 4) || misaligned(G, 4) || misaligned(transient, 4))
+    return DQ4_ERR_ALIGN;
+  const int64_t row_bytes = cols * 4;
+  if (transient_bytes < row_bytes) return DQ4_ERR_TOO_LARGE;  // at least one row
+  int64_t rb = transient_bytes / row_bytes;
+  if (rb > rows) rb = rows;
+  if (rb > INT32_MAX) rb = INT32_MAX;
+  // keep block starts on nested-group boundaries when the budget allows it,
+  // so every block takes the vector path
+  const int64_t unit = int64_t(blocksize) * nested_blocksize;
+  const int64_t ralign = unit / gcd64(cols % unit ? cols % unit : unit, unit);
+  if (rb >= ralign) rb -= rb % ralign;
+  const CublasApi* cb = cublas_api();
+  if (!cb) return DQ4_ERR_CUBLAS;
+  const auto h = static_cast<cublasHandle_t>(cublas_handle);
+  if (cb->set_stream(h, st) != CUBLAS_STATUS_SUCCESS) return DQ4_ERR_CUBLAS;
+  Args base = make_args(packed, scale_codes, nested_absmax, scale_codebook, value_codebook,
+                        offset, n, blocksize, nested_blocksize, transient);
+  for (int64_t r0 = 0; r0 < rows; r0 += rb) {
+    const int64_t nr = rows - r0 < rb ? rows - r0 : rb;
+    const int64_t first = r0 * cols, count = nr * cols;
+    int status;
+    if (first % unit == 0) {
+      status = dq4_nested(packed + first / 2, scale_codes + first / blocksize,
+                          nested_absmax + first / unit, scale_codebook, value_codebook, offset,
+                          count, blocksize, nested_blocksize, DQ4_OUT_F32, transient, stream);
+    } else {
+      status = launch_range_f32(base, first, count, transient, st);
+    }
+    if (status) return status;
+    // dst (cols x ncols, row-major) += W_blk^T (cols x nr) * G_blk (nr x ncols); in
+    // cuBLAS's column-major terms: dst^T = G_blk^T * W_blk
+    const float alpha = 1.f, beta = r0 == 0 ? 0.f : 1.f;
+    const cublasStatus_t cs =
+        cb->gemm(h, CUBLAS_OP_N, CUBLAS_OP_T, int(ncols), int(cols), int(nr), &alpha,
+                 G + r0 * ncols, CUDA_R_32F, int(ncols), transient, CUDA_R_32F, int(cols), &beta,
+                 dst, CUDA_R_32F, int(ncols), CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
+    if (cs != CUBLAS_STATUS_SUCCESS) return DQ4_ERR_CUBLAS;
+  }
+  return DQ4_OK;
+}
+
 const char* dq4_status_string(int status) {
   switch (status) {
     case DQ4_OK: return "ok";
@@ -1038,7 +1171,9 @@ const char* dq4_status_string(int status) {
     case DQ4_ERR_ARCH: return "the current device is not compute capability 10.3 (GB300)";
     case DQ4_ERR_LAUNCH: return "the CUDA runtime reported an error at kernel launch";
     case DQ4_ERR_TOO_LARGE:
-      return "ceil(n / blocksize) exceeds DQ4_STATIC_SCRATCH_BLOCKS (the static scratch array)";
+      return "the problem needs more scratch than given (DQ4_STATIC_SCRATCH_BLOCKS for the "
+             "static array; one row of W for a transient buffer)";
+    case DQ4_ERR_CUBLAS: return "cuBLAS could not be loaded or reported an error";
     default: return "unknown status";
   }
 }

@@ -37,7 +37,7 @@ def test_header_declares_the_boundary():
     assert names == sorted(["dq4_abi_version", "dq4_nested", "dq4_nested_transposed", "dq4",
                             "dq4_nested_unfused",
                             "dq4_nested_unfused_static", "dq4_status_string",
-                            "dq4_int8_correction_prep",
+                            "dq4_int8_correction_prep", "dq4_nested_out_prod",
                             "dq4_last_cuda_error"]), names
 
 
@@ -64,7 +64,7 @@ def test_header_constants_match_binding(dq):
 
 
 def test_status_strings(dq):
-    for code in range(0, 11):
+    for code in range(0, 12):
         s = dq.lib.dq4_status_string(code)
         assert s and s != b"unknown status", code
     assert dq.lib.dq4_status_string(1234) == b"unknown status"
@@ -119,6 +119,13 @@ def test_host_validation_before_any_cuda_call(dq):
     assert P(None, nz, nz, nz, 4, 4, 4, 2, nz, nz, None, None) == 1
     assert P(nz, nz, nz, nz + 4, 4, 4, 4, 2, nz, nz, None, None) == 6
     assert P(nz, nz, nz + 2, nz, 4, 4, 4, 2, nz, nz, None, None) == 6
+    # row-blocked dequant + GEMM: shape, budget and pointers on the host
+    O = L.dq4_nested_out_prod
+    assert O(nz, nz, nz, nz, nz, 0.0, -1, 8, 64, 256, nz, 4, nz, nz, 1 << 20, nz, None) == 2
+    assert O(nz, nz, nz, nz, nz, 0.0, 8, 8, 64, 256, nz, 0, nz, nz, 1 << 20, nz, None) == 0
+    assert O(nz, nz, nz, nz, nz, 0.0, 8, 256, 64, 256, nz, 4, nz, nz, 1000, nz, None) == 10
+    assert O(nz, nz, nz, nz, nz, 0.0, 8, 8, 64, 256, nz, 4, nz, nz, 1 << 20, None, None) == 1
+    assert O(nz, nz, nz, nz, nz, 0.0, 8, 8, 48, 256, nz, 4, nz, nz, 1 << 20, nz, None) == 3
     # allocation-free form: the static scratch limit is checked before anything else runs
     limit = _declared_constants()["DQ4_STATIC_SCRATCH_BLOCKS"]
     assert L.dq4_nested_unfused_static(nz, nz, nz, nz, nz, 0.0, 64 * limit + 1, 64, 256, 0, nz,
