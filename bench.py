@@ -48,7 +48,9 @@ UNIT = "elements/s"
 DEFAULT_CELL = "C4a"
 N_SETS = 3
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SRC = os.path.join(ROOT, "quantized_weight_dequantization_gb300", "csrc", "dq4.cu")
+# the sources of the flat dequantization kernels (the ncu traffic record is tied to them)
+KERNEL_SRCS = [os.path.join(ROOT, "quantized_weight_dequantization_gb300", "csrc", f)
+               for f in ("common.cuh", "flat.cu")]
 PROFILES = os.path.join(ROOT, "profiles")
 
 
@@ -103,8 +105,11 @@ def read_peaks():
 
 
 def source_sha256() -> str:
-    with open(KERNEL_SRC, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()
+    h = hashlib.sha256()
+    for path in KERNEL_SRCS:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 def traffic_record(cell: str):

@@ -2,6 +2,7 @@
 
 from __future__ import annotations
 
+import concurrent.futures
 import os
 import subprocess
 import sys
@@ -9,8 +10,10 @@ from typing import Optional
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
-SOURCES = [os.path.join(PKG, "csrc", "dq4.cu")]
-HEADERS = [os.path.join(ROOT, "include", "dq4.h")]
+CSRC = os.path.join(PKG, "csrc")
+SOURCES = [os.path.join(CSRC, f) for f in
+           ("flat.cu", "transposed.cu", "int8_prep.cu", "out_prod.cu", "host.cu")]
+HEADERS = [os.path.join(ROOT, "include", "dq4.h"), os.path.join(CSRC, "common.cuh")]
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libdq4.so")
 
@@ -18,8 +21,7 @@ NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
     "-O3", "-lineinfo", "-std=c++17",
     "-fmad=false",            # no contraction anywhere (the kernels also use __fmul_rn/__fadd_rn)
-    "-Xcompiler", "-fPIC", "-shared",
-    "-Xptxas", "-v",
+    "-Xcompiler", "-fPIC",
 ]
 
 
@@ -39,21 +41,53 @@ def _stale(dst: str) -> bool:
 
 
 def build(force: bool = False, out: Optional[str] = None, extra_flags=()) -> str:
-    """Build libdq4.so (if stale) and return its path.  ptxas's report goes to _build/."""
+    """Build libdq4.so (if stale) and return its path.
+
+    The translation units compile in parallel (one nvcc each), then link into
+    one shared library; ptxas's register report goes to ptxas.txt beside it.
+    """
     dst = out or LIB_PATH
     if not force and not _stale(dst):
         return dst
-    os.makedirs(os.path.dirname(dst), exist_ok=True)
-    tmp = f"{dst}.{os.getpid()}.tmp"
-    cmd = [nvcc(), *NVCC_FLAGS, *extra_flags, "-I", os.path.join(ROOT, "include"),
-           *SOURCES, "-o", tmp]
-    res = subprocess.run(cmd, capture_output=True, text=True)
-    with open(os.path.join(os.path.dirname(dst), "ptxas.txt"), "w") as f:
-        f.write(" ".join(cmd) + "\n" + res.stdout + res.stderr)
-    if res.returncode != 0:
-        sys.stderr.write(res.stdout + res.stderr)
-        raise RuntimeError(f"nvcc failed ({res.returncode}) building {dst}")
-    os.replace(tmp, dst)
+    bdir = os.path.dirname(dst)
+    os.makedirs(bdir, exist_ok=True)
+    tag = f"{os.getpid()}"
+    incs = ["-I", os.path.join(ROOT, "include"), "-I", CSRC]
+
+    def compile_one(src):
+        obj = os.path.join(bdir, f"{os.path.basename(src)}.{tag}.o")
+        cmd = [nvcc(), *NVCC_FLAGS, *extra_flags, *incs, "-Xptxas", "-v", "-c", src, "-o", obj]
+        res = subprocess.run(cmd, capture_output=True, text=True)
+        return src, obj, cmd, res
+
+    with concurrent.futures.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
+        results = list(ex.map(compile_one, SOURCES))
+    report = []
+    failed = False
+    for src, obj, cmd, res in results:
+        report.append(" ".join(cmd) + "\n" + res.stdout + res.stderr)
+        if res.returncode != 0:
+            sys.stderr.write(res.stdout + res.stderr)
+            failed = True
+    objs = [obj for _, obj, _, _ in results]
+    try:
+        if failed:
+            raise RuntimeError(f"nvcc failed building {dst}")
+        tmp = f"{dst}.{tag}.tmp"
+        link = [nvcc(), "-gencode", "arch=compute_103a,code=sm_103a", "-shared", *objs,
+                "-o", tmp, "-ldl"]
+        res = subprocess.run(link, capture_output=True, text=True)
+        report.append(" ".join(link) + "\n" + res.stdout + res.stderr)
+        if res.returncode != 0:
+            sys.stderr.write(res.stdout + res.stderr)
+            raise RuntimeError(f"link failed building {dst}")
+        os.replace(tmp, dst)
+    finally:
+        with open(os.path.join(bdir, "ptxas.txt"), "w") as f:
+            f.write("\n".join(report))
+        for obj in objs:
+            if os.path.exists(obj):
+                os.remove(obj)
     return dst
 
 

@@ -1,0 +1,254 @@
+// Transposed-output path of the dq4 library: dq4_nested_transposed.
+#include "common.cuh"
+
+namespace dq4d {
+
+// ------------------------------------------------------ transposed output
+// The flat values are the row-major rows x cols weight W; the output is W^T
+// row-major: element (r, c) of W goes to out[c * rows + r].
+// A warp owns a tile of 64 rows x 64 columns of W, and lane p owns the rows
+// r0 + 2p and r0 + 2p + 1 of it: it reads the 32-byte packed segment of each
+// of its two rows (two 16-byte loads per row) and decodes 8 columns at a
+// time.  For every column c the warp then holds the whole 64-value output
+// segment out[c * rows + r0 .. + 64), and lane p writes its pair (rows 2p,
+// 2p + 1) with one 4-byte store (8 bytes for FP32): 128 B (256 B)
+// contiguous per warp store instruction, with no shared-memory staging.
+// Tiles are walked in column-major order (consecutive warps go down a
+// column band), so consecutive warps extend the same output rows.
+// kLoadVec: cols % 32 == 0 and `packed` 16-byte aligned (every row segment
+// is two aligned 16-byte loads); otherwise values are read one by one.
+// kStoreVec: rows is even and `out` is aligned to two elements (pair
+// stores); otherwise elements are stored one by one.
+constexpr int kTR = 64;  // warp-tile rows of W
+constexpr int kTC = 64;  // warp-tile columns of W
+
+template <int OUT>
+__device__ __forceinline__ uint32_t out_bits(float v) {
+  if constexpr (OUT == DQ4_OUT_F16) {
+    return __half_as_ushort(__float2half_rn(v));
+  } else if constexpr (OUT == DQ4_OUT_BF16) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+  } else {
+    return __float_as_uint(v);
+  }
+}
+
+// Store the values of rows (r, r + 1) at column c of W into W^T.
+// `o` is the element index of (r, c) in W^T: c * rows + r.
+template <int OUT, bool kStoreVec>
+__device__ __forceinline__ void store_pair(void* out, int64_t o, float v0, float v1, bool has0,
+                                           bool has1) {
+  if constexpr (OUT == DQ4_OUT_F32) {
+    if (kStoreVec && has1) {
+      __stcs(reinterpret_cast<uint2*>(static_cast<float*>(out) + o),
+             make_uint2(__float_as_uint(v0), __float_as_uint(v1)));
+    } else {
+      if (has0) static_cast<float*>(out)[o] = v0;
+      if (has1) static_cast<float*>(out)[o + 1] = v1;
+    }
+  } else {
+    if (kStoreVec && has1) {
+      __stcs(reinterpret_cast<unsigned int*>(static_cast<uint16_t*>(out) + o),
+             pack2<OUT>(v0, v1));  // one conversion for the pair; row r at the lower address
+    } else {
+      if (has0) static_cast<uint16_t*>(out)[o] = uint16_t(out_bits<OUT>(v0));
+      if (has1) static_cast<uint16_t*>(out)[o + 1] = uint16_t(out_bits<OUT>(v1));
+    }
+  }
+}
+
+// Staged form (cols % 32 == 0, `packed` 16-byte aligned).  A CTA owns 128 rows
+// x 256 columns of W: its packed bytes (128 B per row, whole cache lines) and
+// the scales of its 32-value row segments are first loaded cooperatively and
+// coalesced into shared memory; then each warp decodes one 64 x 64 warp tile
+// from shared memory and stores it as above.  CTAs are walked in column-major
+// order.
+constexpr int kSR = 128;                 // CTA tile rows
+constexpr int kSC = 256;                 // CTA tile columns (128 packed bytes per row)
+constexpr int kSRowBytes = kSC / 2;      // smem row: 8 chunks of 16 B, XOR-swizzled
+constexpr int kSSeg = kSC / 32;          // 32-value scale segments per row
+
+// 16-byte chunk `ch` of staged row `rr` sits at chunk position ch ^ key(rr):
+// lanes reading rows 2p (and 2p + 1) of 8 consecutive p then hit 8 distinct
+// chunk positions, i.e. all 32 banks.
+__device__ __forceinline__ int swz(int rr, int ch) { return ch ^ ((rr >> 1) & 7); }
+
+// minimum resident CTAs per SM the staged transposed kernel is compiled for
+#ifndef DQ4_T_MIN_CTAS
+#define DQ4_T_MIN_CTAS 8
+#endif
+
+template <int OUT, bool kStoreVec>
+__global__ void __launch_bounds__(kThreads, DQ4_T_MIN_CTAS)
+    dq4_transposed_kernel(const Args a, int64_t rows, int64_t cols, uint32_t tiles_r) {
+  __shared__ float s_vcb[16];
+  __shared__ float s_scb[256];
+  __shared__ __align__(16) uint8_t s_pk[kSR][kSRowBytes];
+  // [segment][row]: a lane's 2 rows are one float2; the 4-float pad puts a warp's
+  // 8 segments x 4 rows of stores in 32 distinct banks
+  __shared__ __align__(8) float s_sc[kSSeg][kSR + 4];
+#if DQ4_PDL
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+#endif
+  if (threadIdx.x < 16) s_vcb[threadIdx.x] = __ldg(a.vcb + threadIdx.x);
+  for (int k = threadIdx.x; k < 256; k += kThreads) s_scb[k] = __ldg(a.scb + k);
+  const int64_t r0 = int64_t(blockIdx.x % tiles_r) * kSR;  // column-major CTA order
+  const int64_t c0 = int64_t(blockIdx.x / tiles_r) * kSC;
+
+  // packed rows: 8 x 16 B per row; a warp reads 4 whole rows per instruction
+#pragma unroll
+  for (int k = 0; k < kSR * 8 / kThreads; ++k) {
+    const int id = threadIdx.x + kThreads * k;
+    const int rr = id >> 3, ch = id & 7;
+    const int64_t r = r0 + rr, c = c0 + 32 * ch;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (r < rows && c < cols)
+      v = __ldcs(reinterpret_cast<const uint4*>(a.packed + ((r * cols + c) >> 1)));
+    *reinterpret_cast<uint4*>(&s_pk[rr][16 * swz(rr, ch)]) = v;
+  }
+  __syncthreads();  // codebooks staged
+  // scales of the 32-value segments (bs >= 32 and cols % 32 == 0: one block each)
+#pragma unroll
+  for (int k = 0; k < kSR * kSSeg / kThreads; ++k) {
+    const int id = threadIdx.x + kThreads * k;
+    const int rr = id / kSSeg, q = id % kSSeg;  // a warp: 4 rows x 8 segments (codes coalesced)
+    const int64_t r = r0 + rr, c = c0 + 32 * q;
+    s_sc[q][rr] = (r < rows && c < cols) ? nested_scale(a, s_scb, (r * cols + c) >> a.log2_bs)
+                                         : 0.f;
+  }
+  __syncthreads();
+
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wr = 64 * (w >> 2);  // warp tile: rows wr .. +64, columns wc .. +64 of the CTA tile
+  const int wc = 64 * (w & 3);
+  const int64_t ra = r0 + wr + 2 * lane;  // this lane's rows: ra, ra + 1
+  const bool has0 = ra < rows, has1 = ra + 1 < rows;
+  if (!has0) return;
+  const int64_t cbase = c0 + wc;
+  const int ncol = int(cols - cbase < 64 ? cols - cbase : 64);
+  if (ncol <= 0) return;
+  const int lr = wr + 2 * lane;  // local row of ra
+  int64_t o = cbase * rows + ra;  // W^T index of (ra, column); advances by rows per column
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    if (32 * q >= ncol) break;
+    const int ch = wc / 32 + q;  // 16-byte chunk of this 32-column half
+    const uint4 s0 = *reinterpret_cast<const uint4*>(&s_pk[lr][16 * swz(lr, ch)]);
+    const uint4 s1 = *reinterpret_cast<const uint4*>(&s_pk[lr + 1][16 * swz(lr + 1, ch)]);
+    const float2 scp = *reinterpret_cast<const float2*>(&s_sc[ch][lr]);
+    const float sc0 = scp.x, sc1 = scp.y;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {  // packed word k: 8 columns
+      const uint32_t w0 = k == 0 ? s0.x : k == 1 ? s0.y : k == 2 ? s0.z : s0.w;
+      const uint32_t w1 = k == 0 ? s1.x : k == 1 ? s1.y : k == 2 ? s1.z : s1.w;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {  // value j of a word: byte j/2, high nibble first
+        const int sh = 8 * (j >> 1) + ((j & 1) ? 0 : 4);
+        const float v0 = __fmul_rn(s_vcb[(w0 >> sh) & 0xFu], sc0);
+        const float v1 = __fmul_rn(s_vcb[(w1 >> sh) & 0xFu], sc1);
+        store_pair<OUT, kStoreVec>(a.out, o, v0, v1, has0, has1);
+        o += rows;
+      }
+    }
+  }
+}
+
+// Per-value form for other shapes: a warp owns 64 rows x 64 columns, lane p
+// the rows r0 + 2p and r0 + 2p + 1, read value by value.
+template <int OUT, bool kStoreVec>
+__global__ void __launch_bounds__(kThreads)
+    dq4_transposed_any_kernel(const Args a, int64_t rows, int64_t cols, uint32_t tiles_r,
+                              uint32_t n_tiles) {
+  __shared__ float s_vcb[16];
+  __shared__ float s_scb[256];
+#if DQ4_PDL
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+#endif
+  stage_codebooks<true>(a, s_vcb, s_scb);
+  const uint32_t t = blockIdx.x * uint32_t(kWarpsPerCta) + (threadIdx.x >> 5);
+  if (t >= n_tiles) return;
+  const int lane = threadIdx.x & 31;
+  const int64_t r0 = int64_t(t % tiles_r) * kTR;  // column-major tile order
+  const int64_t c0 = int64_t(t / tiles_r) * kTC;
+  const int64_t ra = r0 + 2 * lane;
+  const bool has0 = ra < rows, has1 = ra + 1 < rows;
+  if (!has0) return;
+  const int ncol = int(cols - c0 < kTC ? cols - c0 : kTC);
+  // each row's scale is rebuilt only when the row crosses into a new block
+  const int64_t i0 = ra * cols + c0, i1 = i0 + cols;
+  int64_t b0 = -1, b1 = -1;
+  float sc0 = 0.f, sc1 = 0.f;
+  int64_t o = c0 * rows + ra;
+  for (int cc = 0; cc < ncol; ++cc) {
+    const int64_t ia = i0 + cc, ib = i1 + cc;
+    if ((ia >> a.log2_bs) != b0) { b0 = ia >> a.log2_bs; sc0 = nested_scale(a, s_scb, b0); }
+    const uint32_t ba = a.packed[ia >> 1];
+    const float v0 = __fmul_rn(s_vcb[(ia & 1) ? (ba & 0xFu) : (ba >> 4)], sc0);
+    float v1 = 0.f;
+    if (has1) {
+      if ((ib >> a.log2_bs) != b1) { b1 = ib >> a.log2_bs; sc1 = nested_scale(a, s_scb, b1); }
+      const uint32_t bb = a.packed[ib >> 1];
+      v1 = __fmul_rn(s_vcb[(ib & 1) ? (bb & 0xFu) : (bb >> 4)], sc1);
+    }
+    store_pair<OUT, kStoreVec>(a.out, o, v0, v1, has0, has1);
+    o += rows;
+  }
+}
+
+template <int OUT>
+int launch_transposed(const Args& a, int64_t rows, int64_t cols, cudaStream_t stream) {
+  int dev = 0, sms = 0;
+  if (int st = current_device(&dev, &sms)) return st;
+  constexpr uintptr_t osz = (OUT == DQ4_OUT_F32) ? 4 : 2;
+  const bool sv = rows % 2 == 0 && reinterpret_cast<uintptr_t>(a.out) % (2 * osz) == 0;
+  if (cols % 32 == 0 && reinterpret_cast<uintptr_t>(a.packed) % 16 == 0) {
+    const int64_t tiles_r = (rows + kSR - 1) / kSR;
+    const int64_t grid = tiles_r * ((cols + kSC - 1) / kSC);
+    if (grid > int64_t(UINT32_MAX)) return DQ4_ERR_N;  // 32-bit tile ids
+    const uint32_t tr = uint32_t(tiles_r);
+    if (sv) return launch_kernel(dq4_transposed_kernel<OUT, true>, grid, stream, a, rows, cols, tr);
+    return launch_kernel(dq4_transposed_kernel<OUT, false>, grid, stream, a, rows, cols, tr);
+  }
+  const int64_t tiles_r = (rows + kTR - 1) / kTR;
+  const int64_t n_tiles = tiles_r * ((cols + kTC - 1) / kTC);
+  if (n_tiles > int64_t(UINT32_MAX) - kWarpsPerCta) return DQ4_ERR_N;  // 32-bit tile ids
+  const int64_t grid = (n_tiles + kWarpsPerCta - 1) / kWarpsPerCta;
+  const uint32_t tr = uint32_t(tiles_r), nt = uint32_t(n_tiles);
+  if (sv) return launch_kernel(dq4_transposed_any_kernel<OUT, true>, grid, stream, a, rows, cols, tr, nt);
+  return launch_kernel(dq4_transposed_any_kernel<OUT, false>, grid, stream, a, rows, cols, tr, nt);
+}
+
+}  // namespace dq4d
+
+using namespace dq4d;
+
+extern "C" {
+
+int dq4_nested_transposed(const uint8_t* packed, const uint8_t* scale_codes,
+                          const float* nested_absmax, const float* scale_codebook,
+                          const float* value_codebook, float offset, int64_t rows,
+                          int64_t cols, int32_t blocksize, int32_t nested_blocksize,
+                          int32_t out_dtype, void* out, void* stream) {
+  if (rows < 0 || cols < 0) return DQ4_ERR_N;
+  if (cols > 0 && rows > INT64_MAX / cols) return DQ4_ERR_N;
+  const int64_t n = rows * cols;
+  if (int st = validate(n, blocksize, nested_blocksize, true, out_dtype)) return st;
+  if (n == 0) return DQ4_OK;
+  if (!packed || !scale_codes || !nested_absmax || !scale_codebook || !value_codebook || !out)
+    return DQ4_ERR_NULL;
+  if (misaligned(nested_absmax, 4) || misaligned(scale_codebook, 4) ||
+      misaligned(value_codebook, 4) || misaligned(out, out_itemsize(out_dtype)))
+    return DQ4_ERR_ALIGN;
+  const Args a = make_args(packed, scale_codes, nested_absmax, scale_codebook, value_codebook,
+                           offset, n, blocksize, nested_blocksize, out);
+  const auto st = static_cast<cudaStream_t>(stream);
+  switch (out_dtype) {
+    case DQ4_OUT_F16: return launch_transposed<DQ4_OUT_F16>(a, rows, cols, st);
+    case DQ4_OUT_BF16: return launch_transposed<DQ4_OUT_BF16>(a, rows, cols, st);
+    default: return launch_transposed<DQ4_OUT_F32>(a, rows, cols, st);
+  }
+}
+
+}  // extern "C"
