@@ -61,7 +61,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cell", default=DEFAULT_CELL, choices=sorted(gen.CELLS))
-    ap.add_argument("--op", choices=["nested", "transposed", "int8prep", "outprod"],
+    ap.add_argument("--op", choices=["nested", "transposed", "int8prep", "outprod", "linear"],
                     default="nested",
                     help="nested: dq4_nested (flat output); transposed: dq4_nested_transposed "
                          "(W^T output of the rows x cols weight); int8prep: LLM.int8 "
@@ -73,6 +73,10 @@ def parse_args():
     ap.add_argument("--cols", type=int, default=256, help="outprod: columns of W")
     ap.add_argument("--ncols", type=int, default=256, help="outprod: columns of G")
     ap.add_argument("--transient-mib", type=int, default=256, help="outprod: transient bound")
+    ap.add_argument("--lin-m", default="16,128,512,2048,4096",
+                    help="linear: comma-separated M values (activation rows)")
+    ap.add_argument("--lin-n", type=int, default=11008, help="linear: N (weight rows)")
+    ap.add_argument("--lin-k", type=int, default=4096, help="linear: K")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--compare-batches", type=int, default=7)
     ap.add_argument("--sets", type=int, default=N_SETS,
@@ -687,6 +691,71 @@ def run_outprod(args):
     }), flush=True)
 
 
+def run_linear(args):
+    """Fused nested dequant + tcgen05 GEMM against dequantize-then-cuBLAS, over M."""
+    import torch
+
+    import quantized_weight_dequantization_gb300 as dq
+
+    dev = torch.device("cuda:0")
+    N, K = args.lin_n, args.lin_k
+    p = gen.make_problem(N * K, 64, 256, "nf4", 1.0, 0.0371, seed=31)
+    t = {k: torch.from_numpy(np.ascontiguousarray(getattr(p, k))).to(dev)
+         for k in ("packed", "scale_codes", "nested_absmax", "scale_codebook", "value_codebook")}
+    Wd = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
+    peak_tflops = None
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak_tflops = float(json.load(f)["bf16_tflops"])
+    except (OSError, KeyError, ValueError):
+        peak_tflops = 1900.0
+    cells = []
+    for M in [int(x) for x in args.lin_m.split(",")]:
+        X = torch.from_numpy(gen.make_normal_g(M, K, seed=32)).to(torch.bfloat16).to(dev)
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+
+        def fused():
+            dq.linear(X, t["packed"], t["scale_codes"], t["nested_absmax"], t["scale_codebook"],
+                      t["value_codebook"], float(p.offset), N, 64, 256, Y=Y)
+
+        def unfused():
+            dq.dq4_nested(t["packed"], t["scale_codes"], t["nested_absmax"],
+                          t["scale_codebook"], t["value_codebook"], float(p.offset), N * K, 64,
+                          256, torch.bfloat16, out=Wd.view(-1))
+            torch.matmul(X, Wd.t(), out=Y)
+
+        def gemm_only():
+            torch.matmul(X, Wd.t(), out=Y)
+
+        res = {}
+        for name, fn in (("fused", fused), ("unfused", unfused), ("cublas_gemm_only", gemm_only)):
+            for _ in range(max(3, args.warmup)):
+                fn()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(dev)
+            e0.record()
+            k = max(1, args.steps)
+            for _ in range(k):
+                fn()
+            e1.record()
+            torch.cuda.synchronize(dev)
+            res[name] = e0.elapsed_time(e1) / k * 1e3
+        flops = 2.0 * M * N * K
+        wbytes = (N * K) // 2 + N * K // 64 + 4 * (N * K // 16384)
+        cells.append({"M": M, "fused_us": res["fused"], "unfused_us": res["unfused"],
+                      "cublas_gemm_only_us": res["cublas_gemm_only"],
+                      "fused_tflops": flops / (res["fused"] / 1e6) / 1e12,
+                      "fused_frac_of_bf16_peak": flops / (res["fused"] / 1e6) / 1e12 / peak_tflops,
+                      "fused_weight_gbs": wbytes / (res["fused"] / 1e6) / 1e9,
+                      "speedup_vs_unfused": res["unfused"] / res["fused"]})
+    print(json.dumps({
+        "metric": "fused nested dequant + tcgen05 GEMM (Y = X W^T) time", "unit": "us",
+        "higher_is_better": False, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "config": {"workload": f"linear N={N} K={K} NF4-style nested (bs 64, nested 256), "
+                               "BF16 X and Y", "bf16_peak_tflops": peak_tflops},
+        "cells": cells}), flush=True)
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
@@ -695,6 +764,8 @@ def main():
         run_int8prep(args)
     elif args.op == "outprod":
         run_outprod(args)
+    elif args.op == "linear":
+        run_linear(args)
     else:
         run_ours(args)
 

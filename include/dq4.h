@@ -227,6 +227,31 @@ int dq4_nested_out_prod(const uint8_t* packed, const uint8_t* scale_codes,
                         int64_t ncols, float* dst, float* transient, int64_t transient_bytes,
                         void* cublas_handle, void* stream);
 
+/*
+ * Nested 4-bit dequantization fused into a tensor-core GEMM (one launch):
+ *   Y = X * W^T       X: M x K (BF16 or FP16, in_dtype), W: the N x K weight
+ * whose n = N * K values (row-major) are given as nested 4-bit codes exactly
+ * as for dq4_nested; W is decoded tile by tile into shared memory (the same
+ * operand bits dq4_nested writes for in_dtype) and never materialised.  Y is
+ * M x N row-major in out_dtype; the accumulation is FP32 (tcgen05, sm_103a).
+ * Source: "Fuse nested scale reconstruction into SM103 4-bit dequantization"
+ * (bitsandbytes issue #21), sections "Problem" and "B300 evidence plan" (the
+ * dequantize-plus-linear fallback, which rebuilds the scales, materialises
+ * the weight and calls F.linear).
+ *   in_dtype   DQ4_OUT_F16 or DQ4_OUT_BF16 (X's type; W is decoded to it)
+ *   K          a positive multiple of 64; M, N >= 0 (M <= INT32_MAX)
+ *   X          16-byte aligned
+ *   bad        optional device int (NULL to skip): counts bounded waits that
+ *              ran out (never expected; Y is then incomplete)
+ * DQ4_ERR_N for K not a multiple of 64.
+ */
+int dq4_nested_linear(const void* X, int32_t in_dtype, const uint8_t* packed,
+                      const uint8_t* scale_codes, const float* nested_absmax,
+                      const float* scale_codebook, const float* value_codebook, float offset,
+                      int64_t M, int64_t N, int64_t K, int32_t blocksize,
+                      int32_t nested_blocksize, int32_t out_dtype, void* Y, int* bad,
+                      void* stream);
+
 /* A static, human-readable string for a status code (never NULL). */
 const char* dq4_status_string(int status);
 

@@ -233,3 +233,21 @@ def out_prod(problem, rows: int, cols: int, G: np.ndarray, threads: int = 8, lib
     """
     w = dq4_nested(problem, "f32", threads=threads, lib=lib).reshape(rows, cols)
     return w.astype(np.float64).T @ np.asarray(G, dtype=np.float64)
+
+
+def linear(problem, X_bits: np.ndarray, in_dtype: str, N: int, K: int, threads: int = 8,
+           lib=None) -> np.ndarray:
+    """Y = X W^T in float64: W is the oracle's dequantization to ``in_dtype`` (N x K).
+
+    X_bits holds X's raw 16-bit values (M x K).  Both operands are exact in
+    float64; numpy's float64 matmul (a library primitive) is the contraction.
+    """
+    w = dq4_nested(problem, in_dtype, threads=threads, lib=lib).reshape(N, K)
+    return _bits16_to_f64(X_bits, in_dtype) @ _bits16_to_f64(w, in_dtype).T
+
+
+def _bits16_to_f64(bits: np.ndarray, dtype: str) -> np.ndarray:
+    bits = np.ascontiguousarray(bits, dtype=np.uint16)
+    if dtype == "f16":
+        return bits.view(np.float16).astype(np.float64)
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)

@@ -18,6 +18,7 @@ from ._binding import (  # noqa: F401
     dq4_nested_unfused_static,
     get_lib,
     int8_correction_prep,
+    linear,
     out_prod,
     sizes,
 )
@@ -30,5 +31,5 @@ def __getattr__(name):
 
 
 __all__ = ["dq4_nested", "dq4_nested_transposed", "dq4", "dq4_nested_unfused", "dq4_nested_unfused_static", "Dq4Error",
-           "get_lib", "sizes", "int8_correction_prep", "out_prod",
+           "get_lib", "sizes", "int8_correction_prep", "out_prod", "linear",
            "OUT_F16", "OUT_BF16", "OUT_F32"]

@@ -65,6 +65,9 @@ def _load() -> ctypes.CDLL:
     L.dq4_nested_out_prod.argtypes = [p, p, p, p, p, f32, i64, i64, i32, i32, p, i64, p, p, i64,
                                       p, p]
     L.dq4_nested_out_prod.restype = ctypes.c_int
+    L.dq4_nested_linear.argtypes = [p, i32, p, p, p, p, p, f32, i64, i64, i64, i32, i32, i32, p,
+                                    p, p]
+    L.dq4_nested_linear.restype = ctypes.c_int
     L.dq4_status_string.argtypes = [ctypes.c_int]
     L.dq4_status_string.restype = ctypes.c_char_p
     L.dq4_last_cuda_error.argtypes = []
@@ -368,3 +371,48 @@ def out_prod(packed: torch.Tensor, scale_codes: torch.Tensor, nested_absmax: tor
     if st:
         raise Dq4Error(st, "dq4_nested_out_prod")
     return dst
+
+
+def linear(X: torch.Tensor, packed: torch.Tensor, scale_codes: torch.Tensor,
+           nested_absmax: torch.Tensor, scale_codebook: torch.Tensor,
+           value_codebook: torch.Tensor, offset: float, N: int, blocksize: int = 64,
+           nested_blocksize: int = 256, out_dtype: Optional[torch.dtype] = None,
+           Y: Optional[torch.Tensor] = None, bad: Optional[torch.Tensor] = None,
+           stream=None) -> torch.Tensor:
+    """Y = X W^T with W (N x K) given as nested 4-bit codes, decoded inside a tcgen05 GEMM.
+
+    X is M x K (bfloat16 or float16); W's values are those dq4_nested gives
+    for X's dtype.  The dequantize-plus-linear path of issue #21 without the
+    materialised weight.  K must be a multiple of 64.
+    """
+    if X.dim() != 2:
+        raise ValueError("X must be 2-D (M x K)")
+    if X.dtype not in (torch.float16, torch.bfloat16):
+        raise TypeError("X must be float16 or bfloat16")
+    device = X.device
+    M, K = X.shape
+    npk, nb, ng = sizes(N * K, blocksize, nested_blocksize)
+    _check(X, "X", X.dtype, M * K, device)
+    _check(packed, "packed", torch.uint8, npk, device)
+    _check(scale_codes, "scale_codes", torch.uint8, nb, device)
+    _check(nested_absmax, "nested_absmax", torch.float32, ng, device)
+    _check(scale_codebook, "scale_codebook", torch.float32, 256, device)
+    _check(value_codebook, "value_codebook", torch.float32, 16, device)
+    if Y is not None:
+        out_dtype = Y.dtype
+    out_dtype = out_dtype or X.dtype
+    if out_dtype not in _DTYPE_CODE:
+        raise TypeError(f"out_dtype: unsupported {out_dtype}")
+    if Y is None:
+        Y = torch.empty((M, N), dtype=out_dtype, device=device)
+    _check(Y, "Y", out_dtype, M * N, device)
+    if bad is not None:
+        _check(bad, "bad", torch.int32, 1, device)
+    st = get_lib().dq4_nested_linear(
+        _ptr(X), _DTYPE_CODE[X.dtype], _ptr(packed), _ptr(scale_codes), _ptr(nested_absmax),
+        _ptr(scale_codebook), _ptr(value_codebook), float(offset), M, N, K, blocksize,
+        nested_blocksize, _DTYPE_CODE[out_dtype], _ptr(Y), _ptr(bad),
+        _stream_handle(stream, device))
+    if st:
+        raise Dq4Error(st, "dq4_nested_linear")
+    return Y

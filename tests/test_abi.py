@@ -38,6 +38,7 @@ def test_header_declares_the_boundary():
                             "dq4_nested_unfused",
                             "dq4_nested_unfused_static", "dq4_status_string",
                             "dq4_int8_correction_prep", "dq4_nested_out_prod",
+                            "dq4_nested_linear",
                             "dq4_last_cuda_error"]), names
 
 
@@ -126,6 +127,13 @@ def test_host_validation_before_any_cuda_call(dq):
     assert O(nz, nz, nz, nz, nz, 0.0, 8, 256, 64, 256, nz, 4, nz, nz, 1000, nz, None) == 10
     assert O(nz, nz, nz, nz, nz, 0.0, 8, 8, 64, 256, nz, 4, nz, nz, 1 << 20, None, None) == 1
     assert O(nz, nz, nz, nz, nz, 0.0, 8, 8, 48, 256, nz, 4, nz, nz, 1 << 20, nz, None) == 3
+    # fused dequant + GEMM: shapes, dtypes and alignment on the host
+    Lr = L.dq4_nested_linear
+    assert Lr(nz, 1, nz, nz, nz, nz, nz, 0.0, 4, 8, 100, 64, 256, 1, nz, None, None) == 2
+    assert Lr(nz, 2, nz, nz, nz, nz, nz, 0.0, 4, 8, 64, 64, 256, 1, nz, None, None) == 5
+    assert Lr(nz, 1, nz, nz, nz, nz, nz, 0.0, 0, 8, 64, 64, 256, 1, nz, None, None) == 0
+    assert Lr(None, 1, nz, nz, nz, nz, nz, 0.0, 4, 8, 64, 64, 256, 1, nz, None, None) == 1
+    assert Lr(nz + 8, 1, nz, nz, nz, nz, nz, 0.0, 4, 8, 64, 64, 256, 1, nz, None, None) == 6
     # allocation-free form: the static scratch limit is checked before anything else runs
     limit = _declared_constants()["DQ4_STATIC_SCRATCH_BLOCKS"]
     assert L.dq4_nested_unfused_static(nz, nz, nz, nz, nz, 0.0, 64 * limit + 1, 64, 256, 0, nz,

@@ -1,0 +1,113 @@
+"""Nested 4-bit dequantization fused into a tcgen05 GEMM (Y = X W^T), on the GPU.
+
+The dequantize-plus-linear path of "Fuse nested scale reconstruction into
+SM103 4-bit dequantization" (bitsandbytes issue #21, sections "Problem" and
+"B300 evidence plan") without the materialised weight.  Checks:
+(1) integer-valued W (|w| <= 16) and ternary X: every FP32 partial sum is an
+exact integer, so Y must equal the float64 oracle exactly (and its BF16/FP16
+rounding exactly);
+(2) realistic NF4 weights and normal activations within an FP32
+accumulation bound, after the operand bits themselves are pinned by the
+dequantization tests ("Correctness requirements": the dequantized tensor
+passes bitwise equality before any GEMM tolerance).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import dq4_inputs as gen
+import oracle
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+TDT = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}
+
+
+@pytest.fixture(scope="module")
+def dq():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import quantized_weight_dequantization_gb300 as m
+    return m
+
+
+def run(dq, p, X, N, K, out=None, bad=None):
+    t = {k: torch.from_numpy(np.ascontiguousarray(getattr(p, k))).to(DEV)
+         for k in ("packed", "scale_codes", "nested_absmax", "scale_codebook", "value_codebook")}
+    return dq.linear(X, t["packed"], t["scale_codes"], t["nested_absmax"], t["scale_codebook"],
+                     t["value_codebook"], float(p.offset), N, p.blocksize, p.nested_blocksize,
+                     out_dtype=out, bad=bad)
+
+
+def x_bits(X):
+    return X.cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def rounded(y64, out):
+    t = torch.from_numpy(y64)
+    return t.to(TDT[out]).to(torch.float64).numpy() if out != "f32" else \
+        t.to(torch.float32).to(torch.float64).numpy()
+
+
+SHAPES = [(1, 128, 64), (5, 200, 128), (127, 130, 192), (128, 256, 4096), (300, 1000, 512),
+          (129, 384, 1024), (2048, 768, 256)]
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+@pytest.mark.parametrize("xin", ["bf16", "f16"])
+def test_integer_exact(dq, M, N, K, xin):
+    p = gen.make_integer_problem(N, K, blocksize=64 if K % 64 == 0 else 32, seed=N + K)
+    X = torch.from_numpy(gen.make_ternary_g(M, K, seed=M)).to(TDT[xin]).to(DEV)
+    bad = torch.zeros(1, dtype=torch.int32, device=DEV)
+    want = oracle.linear(p, x_bits(X), xin, N, K, threads=16)
+    for out in ("f32", xin):
+        got = run(dq, p, X, N, K, out=TDT[out], bad=bad).to(torch.float64).cpu().numpy()
+        assert np.array_equal(got, rounded(want, out)), (M, N, K, xin, out,
+                                                          np.abs(got - want).max())
+    assert int(bad.item()) == 0
+
+
+@pytest.mark.parametrize("bs,nbs", [(32, 1), (4096, 256), (64, 2)])
+def test_blocksizes(dq, bs, nbs):
+    M, N, K = 256, 512, 4096
+    p = gen.make_integer_problem(N, K, blocksize=bs, nested_blocksize=nbs, seed=bs)
+    X = torch.from_numpy(gen.make_ternary_g(M, K, seed=3)).to(torch.bfloat16).to(DEV)
+    got = run(dq, p, X, N, K, out=torch.float32).double().cpu().numpy()
+    assert np.array_equal(got, oracle.linear(p, x_bits(X), "bf16", N, K, threads=16))
+
+
+@pytest.mark.parametrize("M", [16, 512])
+def test_realistic_llm_shape(dq, M):
+    """An 11008 x 4096 NF4-style nested weight (blocksize 64, nested 256)."""
+    N, K = 11008, 4096
+    p = gen.make_problem(N * K, 64, 256, "nf4", 1.0, 0.0371, seed=21)
+    X = torch.from_numpy(gen.make_normal_g(M, K, seed=22)).to(torch.bfloat16).to(DEV)
+    bad = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got = run(dq, p, X, N, K, out=torch.float32, bad=bad).double().cpu().numpy()
+    xb = x_bits(X)
+    want = oracle.linear(p, xb, "bf16", N, K, threads=16)
+    w = oracle._bits16_to_f64(oracle.dq4_nested(p, "bf16", threads=16), "bf16").reshape(N, K)
+    x = oracle._bits16_to_f64(xb, "bf16")
+    norm = np.sqrt((x * x) @ (w * w).T)  # sqrt(sum_k (x_k w_k)^2) per entry
+    tol = 16 * 2.0 ** -24 * K * norm + 1e-30
+    err = np.abs(got - want)
+    assert np.all(err <= tol), float((err / tol).max())
+    assert int(bad.item()) == 0
+
+
+def test_repeated_and_back_to_back(dq):
+    M, N, K = 200, 700, 512
+    p = gen.make_integer_problem(N, K, seed=9)
+    X = torch.from_numpy(gen.make_ternary_g(M, K, seed=10)).to(torch.bfloat16).to(DEV)
+    outs = [run(dq, p, X, N, K, out=torch.float32) for _ in range(4)]
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+
+
+def test_errors(dq):
+    p = gen.make_integer_problem(64, 100, blocksize=32, seed=1)
+    X = torch.zeros((4, 100), dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(dq.Dq4Error, match="DQ4_ERR_N"):
+        run(dq, p, X, 64, 100)
