@@ -239,11 +239,13 @@ int dq4_nested_out_prod(const uint8_t* packed, const uint8_t* scale_codes,
  * dequantize-plus-linear fallback, which rebuilds the scales, materialises
  * the weight and calls F.linear).
  *   in_dtype   DQ4_OUT_F16 or DQ4_OUT_BF16 (X's type; W is decoded to it)
- *   K          a positive multiple of 64; M, N >= 0 (M <= INT32_MAX)
- *   X          16-byte aligned
- *   bad        optional device int (NULL to skip): counts bounded waits that
- *              ran out (never expected; Y is then incomplete)
- * DQ4_ERR_N for K not a multiple of 64.
+ *   K          a positive multiple of 64; M, N >= 0 (M, N, K <= INT32_MAX)
+ *   X, packed  16-byte aligned (both are read by TMA)
+ *   bad        optional device int (NULL to skip): incremented by each part
+ *              of a CTA that stopped because a bounded wait ran out (never
+ *              expected; nonzero means Y is incomplete)
+ * DQ4_ERR_N for K not a multiple of 64; DQ4_ERR_ALIGN for a misaligned X or
+ * packed.
  */
 int dq4_nested_linear(const void* X, int32_t in_dtype, const uint8_t* packed,
                       const uint8_t* scale_codes, const float* nested_absmax,

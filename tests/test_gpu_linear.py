@@ -50,8 +50,12 @@ def rounded(y64, out):
         t.to(torch.float32).to(torch.float64).numpy()
 
 
+# The kernel picks its activation-tile width BX from M, N and the SM count; on a
+# 152-SM GB300 the last four shapes take BX = 32, 64, 128 and 256 (38 weight tiles,
+# the last one ragged), the others BX = 16 or 128.
 SHAPES = [(1, 128, 64), (5, 200, 128), (127, 130, 192), (128, 256, 4096), (300, 1000, 512),
-          (129, 384, 1024), (2048, 768, 256)]
+          (129, 384, 1024), (2048, 768, 256), (128, 4860, 192), (256, 4860, 128),
+          (512, 4860, 64), (1024, 4860, 256)]
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
@@ -111,3 +115,13 @@ def test_errors(dq):
     X = torch.zeros((4, 100), dtype=torch.bfloat16, device=DEV)
     with pytest.raises(dq.Dq4Error, match="DQ4_ERR_N"):
         run(dq, p, X, 64, 100)
+    # packed is read by TMA: a base that is not 16-byte aligned is refused on the host
+    p = gen.make_integer_problem(64, 128, seed=2)
+    X = torch.zeros((4, 128), dtype=torch.bfloat16, device=DEV)
+    t = {k: torch.from_numpy(np.ascontiguousarray(getattr(p, k))).to(DEV)
+         for k in ("scale_codes", "nested_absmax", "scale_codebook", "value_codebook")}
+    buf = torch.zeros(p.packed.size + 16, dtype=torch.uint8, device=DEV)
+    packed = buf[4:4 + p.packed.size]
+    with pytest.raises(dq.Dq4Error, match="DQ4_ERR_ALIGN"):
+        dq.linear(X, packed, t["scale_codes"], t["nested_absmax"], t["scale_codebook"],
+                  t["value_codebook"], 0.0, 64, 64, 256)
