@@ -13,19 +13,21 @@
 // tile, and a large batch decodes each weight tile once per 256 activations.
 // Eleven warps:
 //  * warp 9 (lane 0): streams the packed weight rows of the tile with TMA into
-//    a ring of raw 128 x 64-value stages (4 KB each), as far ahead as the
-//    ring allows;
+//    a ring of raw stages (two 128-row x 64-value boxes, 4 KB each), as far
+//    ahead as the ring allows;
 //  * warp 10 (lane 0): streams the activation tiles (BX rows x 64 K, 128-byte
 //    swizzle, rows past M zero-filled) with TMA into their own ring;
-//  * warps 0..7 (256 threads, two per weight row, 32 values each): per stage,
-//    the nested scale of the row's block (separately rounded FP32 multiply
-//    and add; the scale codes and absmax values are loaded 8 stages ahead
-//    into registers), the 32 values (FP32 product, RN to BF16 / FP16) written
-//    into the K-major 128-byte-swizzled A tile the MMA reads; afterwards the
-//    epilogue: tcgen05.ld of the accumulator, conversion, stores of Y;
-//  * warp 8: allocates the TMEM accumulator; lane 0 issues tcgen05.mma
-//    (M = 128, N = BX, K = 16) for each stage and commits the stage's weight
-//    and activation slots back to their producers.
+//  * warps 0..7: warp w owns TMEM lanes 32 (w % 4) .. (the weight rows) and
+//    half of every 64-value K step (w / 4).  Per K step a thread computes the
+//    nested scale of its row's block (separately rounded FP32 multiply and
+//    add; the scale codes and absmax values are loaded four stages ahead into
+//    registers) and its 32 values (FP32 products, RN to BF16 / FP16), and
+//    writes them to the weight ring in TMEM with one tcgen05.st; afterwards
+//    the epilogue: tcgen05.ld of the accumulator, conversion, stores of Y;
+//  * warp 8: allocates the TMEM; lane 0 issues tcgen05.mma (A = weights from
+//    TMEM, B = activations from shared memory, M = 128, N = BX, K = 16) for
+//    each K step and commits the weight and activation slots back to their
+//    producers.
 // Every W value is computed exactly as dq4_nested does, so the GEMM consumes
 // the same operand bits as "dequantize, then F.linear".  Waits on mbarriers
 // are bounded; a wait that runs out counts into *bad, raises a CTA-wide abort
@@ -39,13 +41,20 @@
 namespace dq4d {
 namespace {
 
-constexpr int kLinThreads = 352;  // 8 dequant/epilogue warps, MMA, weight-TMA, activation-TMA
-constexpr int kProducerWarps = 8;
+#ifndef DQ4_LIN_PWARPS
+#define DQ4_LIN_PWARPS 8  // dequantizing warps per CTA: 8 or 16
+#endif
+constexpr int kProducerWarps = DQ4_LIN_PWARPS;
+static_assert(kProducerWarps == 8 || kProducerWarps == 16, "2 or 4 threads per weight row");
+constexpr int kTPR = kProducerWarps / 4;           // producer threads per weight row
+constexpr int kWords = 8 / kTPR;                   // packed 32-bit words per thread and K step
+constexpr int kMmaWarp = kProducerWarps;           // also allocates TMEM
+constexpr int kRawWarp = kProducerWarps + 1;       // weight TMA
+constexpr int kXWarp = kProducerWarps + 2;         // activation TMA
+constexpr int kLinThreads = 32 * (kProducerWarps + 3);
 constexpr int kBW = 128;           // weight rows per CTA = MMA M = TMEM lanes
 constexpr int kBK = 64;            // 64 16-bit values = one 128-byte swizzle row
 constexpr int kRawBytes = kBW * kBK / 2;  // one raw stage: 128 rows x 32 packed bytes
-constexpr int kRaw = 16;           // raw weight stages in flight
-constexpr int kCodeAhead = 8;      // stages of scale codes / absmax held in registers
 // A wait gives up after kWaitNs of %globaltimer time (or kWaitLimit polls, should the
 // timer not advance); each poll may suspend the thread for up to kSuspendNs, and the
 // hardware resumes it as soon as the phase completes, so waiting warps do not spin on
@@ -86,6 +95,21 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
+// Poll two barriers at once (their round trips overlap); true when both phases completed.
+__device__ __forceinline__ bool mbar_try2(uint32_t bar_a, uint32_t par_a, uint32_t bar_b,
+                                          uint32_t par_b) {
+  uint32_t done;
+  asm volatile(
+      "{\n.reg .pred pa, pb;\n"
+      "mbarrier.try_wait.parity.shared::cta.b64 pa, [%1], %2, %5;\n"
+      "mbarrier.try_wait.parity.shared::cta.b64 pb, [%3], %4, %5;\n"
+      "and.pred pa, pa, pb;\n"
+      "selp.u32 %0, 1, 0, pa;\n}"
+      : "=r"(done) : "r"(bar_a), "r"(par_a), "r"(bar_b), "r"(par_b), "r"(kSuspendNs)
+      : "memory");
+  return done != 0;
+}
+
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -110,11 +134,15 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
 }
 
-// Arm `bar` for `bytes` of TMA data and start a 2-D tiled copy into `dst`.
-__device__ __forceinline__ void tma_2d(uint32_t dst, uint64_t tmap, int x, int y, uint32_t bar,
-                                       uint32_t bytes) {
+// Add `bytes` to the transaction count `bar` waits for, and arrive on it.
+__device__ __forceinline__ void mbar_expect(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
                :: "r"(bar), "r"(bytes) : "memory");
+}
+
+// A 2-D tiled TMA copy into shared memory at `dst`, completing on `bar`.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, uint64_t tmap, int x, int y,
+                                            uint32_t bar) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];"
@@ -140,9 +168,23 @@ __device__ __forceinline__ void mul2_rn(float a, float b, uint64_t s2, float& x,
   asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(r));
 }
 
-// Byte offset of 16-byte chunk `ch` of row `r` in a K-major 128-byte-swizzled tile.
-__device__ __forceinline__ int swz128(int r, int ch) {
-  return (r >> 3) * 1024 + (r & 7) * 128 + ((ch ^ (r & 7)) << 4);
+// Store N (8 or 16) consecutive 32-bit columns of this warp's 32 TMEM lanes.
+template <int N>
+__device__ __forceinline__ void tmem_st(uint32_t taddr, const uint32_t (&v)[N]) {
+  if constexpr (N == 16) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16};"
+        :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]),
+           "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]),
+           "r"(v[13]), "r"(v[14]), "r"(v[15]) : "memory");
+  } else {
+    static_assert(N == 8, "8 or 16 columns");
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+        :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]),
+           "r"(v[6]), "r"(v[7]) : "memory");
+  }
 }
 
 struct LinArgs {
@@ -154,36 +196,62 @@ struct LinArgs {
   int tiles_x;     // activation-row tiles of Y
 };
 
-// Three rings: dequantized weight tiles (A operand, written by the producers),
-// activation tiles (B operand, TMA) and raw packed weight stages (TMA).  The
-// activation ring is deeper where its tiles are small, so its TMA latency
-// stays hidden behind several stages of MMAs.
-#ifndef DQ4_LIN_AS_SMALL
-#define DQ4_LIN_AS_SMALL 8  // weight operand stages for BX <= 64
+// The dequantized weights (the MMA's A operand) live in TMEM: columns 0 ..
+// 255 hold the FP32 accumulator (BX of them used), columns 256 .. 511 a ring
+// of kAS weight stages of kSub 64-value K steps (32 columns each: 64 16-bit
+// values per lane = weight row).  Producers write them with tcgen05.st, so
+// shared memory only carries the activation ring (B operand, TMA) and the raw
+// packed weight ring (TMA), both as deep as the budget allows.  A weight stage
+// spans kSub K steps, so the per-stage barrier work of the producers is
+// shared by 32 * kSub values per thread.
+#ifndef DQ4_LIN_SUB
+#define DQ4_LIN_SUB 4
 #endif
-#ifndef DQ4_LIN_AS_LARGE
-#define DQ4_LIN_AS_LARGE 4  // weight operand stages for BX >= 128
-#endif
+constexpr int kSub = DQ4_LIN_SUB;         // 64-value K steps per weight stage
+constexpr uint32_t kTmemCols = 512;       // the whole TMEM of the SM
+// The accumulator takes columns 0 .. BX - 1; the weight ring the columns from
+// kATmem(BX) on, kAS(BX) stages of kSub K steps (32 columns each).
+__host__ __device__ constexpr uint32_t kATmem(int bx) { return bx <= 128 ? 128u : 256u; }
+__host__ __device__ constexpr int kASOf(int bx) {
+  return int((kTmemCols - kATmem(bx)) / 32) / kSub;
+}
 template <int BX>
 struct LinSmem {
-  static constexpr int kAS = BX <= 64 ? DQ4_LIN_AS_SMALL : DQ4_LIN_AS_LARGE;
-  static constexpr int kXS = BX <= 32 ? 8 : BX == 64 ? 6 : BX == 128 ? 4 : 3;
-  // raw weight stages: what the operand rings leave of a 220 KB budget, at most kRaw
-  static constexpr int kRawFit = (220 * 1024 - kAS * kBW * kBK * 2 - kXS * BX * kBK * 2) /
-                                 kRawBytes;
-  static constexpr int kRawS = kRawFit < kRaw ? kRawFit : kRaw;
+  static constexpr int kAS = kASOf(BX);              // weight stages in TMEM
+  static_assert(kAS >= 2, "double-buffered weight ring");
+  static_assert(kATmem(BX) + kAS * kSub * 32 <= kTmemCols, "weight ring fits TMEM");
+  static constexpr int kRawSlot = kSub * kRawBytes;
+  static constexpr int kB = BX * kBK * 2;           // one K step of activations
+  static constexpr int kXS = BX <= 32 ? 12 : BX == 64 ? 8 : BX == 128 ? 6 : 4;
+  // raw weight stages: what the activation ring leaves of a 220 KB budget, at most 16
+  static constexpr int kRawFit = (220 * 1024 - kXS * kB) / kRawSlot;
+  static constexpr int kRawS = kRawFit < 16 ? kRawFit : 16;
   static_assert(kRawS >= 4, "raw ring too shallow");
-  static constexpr int kA = kBW * kBK * 2;                         // dequantized weight tile
-  static constexpr int kB = BX * kBK * 2;                          // activation tile
-  static constexpr int kXOff = kAS * kA;
+  static constexpr int kXOff = 0;
   static constexpr int kRawOff = kXOff + kXS * kB;
-  static constexpr int kBarOff = kRawOff + kRawS * kRawBytes;
+  static constexpr int kBarOff = kRawOff + kRawS * kRawSlot;
   // full_w, empty_a per weight stage; full_x, empty_x per activation stage;
   // raw_full, raw_empty per raw stage; acc_full
   static constexpr int kBars = 2 * kAS + 2 * kXS + 2 * kRawS + 1;
-  static constexpr int kBytes = kBarOff + 8 * kBars + 16 + 1024;  // + slot, flag, alignment
+  static constexpr int kBytes = kBarOff + 8 * kBars + 1024;  // + alignment slack
   static_assert(kBytes <= 227 * 1024, "shared memory budget");
-  static_assert(kB % 1024 == 0 && kA % 1024 == 0, "swizzle atoms stay 1024-byte aligned");
+  // more than half an SM's shared memory: one CTA per SM, so the 512-column TMEM
+  // allocation never waits for another CTA
+  static_assert(kBytes > 116 * 1024, "one CTA per SM");
+  static_assert(kB % 1024 == 0, "swizzle atoms stay 1024-byte aligned");
+};
+
+// Slot and phase parity of a ring position, advanced without division.
+template <int kDepth>
+struct RingPos {
+  int slot = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ void next() {
+    if (++slot == kDepth) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
 };
 
 template <int BX, bool kBF16>
@@ -192,30 +260,32 @@ __global__ void __launch_bounds__(kLinThreads, 1)
                       const __grid_constant__ CUtensorMap tmap_w, const LinArgs p) {
   using S = LinSmem<BX>;
   constexpr int kAS = S::kAS, kXS = S::kXS, kRawS = S::kRawS;
+  constexpr uint32_t kATmemCol = kATmem(BX);
   constexpr int kOut = kBF16 ? DQ4_OUT_BF16 : DQ4_OUT_F16;
-  constexpr uint32_t kTmemCols = BX < 32 ? 32 : BX;  // a power of two >= 32
   constexpr unsigned kFull = 0xFFFFFFFFu;
   extern __shared__ uint8_t smem_raw[];
   __shared__ float s_vcb[16];
   __shared__ float s_scb[256];
+  __shared__ uint32_t s_tmem;          // TMEM base address from tcgen05.alloc
+  __shared__ volatile int s_abort;     // set when any wait of the CTA ran out
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(base);
   const uint32_t bar0 = sbase + S::kBarOff;
-  auto full_w = [&](int s) { return bar0 + 8 * s; };              // 8 producer warps
+  auto full_w = [&](int s) { return bar0 + 8 * s; };              // producer warps
   auto empty_a = [&](int s) { return bar0 + 8 * (kAS + s); };     // MMAs reading it done
   auto full_x = [&](int s) { return bar0 + 8 * (2 * kAS + s); };  // activation TMA
   auto empty_x = [&](int s) { return bar0 + 8 * (2 * kAS + kXS + s); };
   auto raw_full = [&](int s) { return bar0 + 8 * (2 * kAS + 2 * kXS + s); };
   auto raw_empty = [&](int s) { return bar0 + 8 * (2 * kAS + 2 * kXS + kRawS + s); };
   const uint32_t acc_full = bar0 + 8 * (2 * kAS + 2 * kXS + 2 * kRawS);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + S::kBarOff + 8 * S::kBars);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* abort_flag = &s_abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int tile_w = blockIdx.x / p.tiles_x, tile_x = blockIdx.x % p.tiles_x;
   const int64_t n0 = int64_t(tile_w) * kBW, m0 = int64_t(tile_x) * BX;
-  const int kt_count = int(p.K / kBK);
+  const int kt_count = int(p.K / kBK);                    // 64-value K steps
+  const int st_count = (kt_count + kSub - 1) / kSub;      // weight stages
   auto fail = [&]() {
     *abort_flag = 1;
     if (p.bad) atomicAdd(p.bad, 1);
@@ -227,9 +297,9 @@ __global__ void __launch_bounds__(kLinThreads, 1)
 #endif
   if (tid < 16) s_vcb[tid] = __ldg(p.w.vcb + tid);
   for (int k = tid; k < 256; k += kLinThreads) s_scb[k] = __ldg(p.w.scb + k);
-  if (warp == 8) {
+  if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-                 :: "r"(smem_u32(tmem_slot)), "r"(kTmemCols));
+                 :: "r"(smem_u32(&s_tmem)), "r"(kTmemCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     if (lane == 0) {
       for (int s = 0; s < kAS; ++s) {
@@ -254,70 +324,97 @@ __global__ void __launch_bounds__(kLinThreads, 1)
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-  const uint32_t tmem = *tmem_slot;
+  const uint32_t tmem = s_tmem;
 
-  if (warp == 9 || warp == 10) {
+  if (warp == kRawWarp) {
     if (lane == 0) {
-      // ---- TMA streams: warp 9 the packed weight rows n0 .. n0 + 127 (32 bytes = 64
-      // values per stage and row), warp 10 the activation rows m0 .. m0 + BX - 1 (64 K
-      // per stage).  Tile j goes to slot j % depth once the consumers of tile j - depth
-      // released it.
-      const bool raw = warp == 9;
-      const int depth = raw ? kRawS : kXS;
-      const uint64_t tmap = reinterpret_cast<uint64_t>(raw ? &tmap_w : &tmap_x);
-      int issued = 0;
-      for (; issued < kt_count; ++issued) {
-        const int slot = issued % depth;
-        if (issued >= depth) {
+      // ---- packed weight rows n0 .. n0 + 127: per stage kSub boxes of 128 rows x 32 bytes
+      // (64 values), each box unswizzled in its own 4 KB so the producers' reads of it
+      // stay conflict-free
+      const uint64_t tw = reinterpret_cast<uint64_t>(&tmap_w);
+      RingPos<kRawS> pos;
+      int i = 0;
+      for (; i < st_count; ++i, pos.next()) {
+        if (i >= kRawS) {
           if (*abort_flag) break;
-          const uint32_t par = ((issued / depth) - 1) & 1;
-          if (!mbar_wait(raw ? raw_empty(slot) : empty_x(slot), par)) {
+          if (!mbar_wait(raw_empty(pos.slot), pos.phase ^ 1u)) {
             fail();
             break;
           }
         }
-        if (raw)
-          tma_2d(sbase + S::kRawOff + slot * kRawBytes, tmap, issued * (kBK / 2), int(n0),
-                 raw_full(slot), kRawBytes);
-        else
-          tma_2d(sbase + S::kXOff + slot * S::kB, tmap, issued * kBK, int(m0), full_x(slot),
-                 S::kB);
+        const int ns = min(kSub, kt_count - i * kSub);
+        mbar_expect(raw_full(pos.slot), ns * kRawBytes);
+        for (int sub = 0; sub < ns; ++sub)
+          tma_load_2d(sbase + S::kRawOff + pos.slot * S::kRawSlot + sub * kRawBytes, tw,
+                      (i * kSub + sub) * (kBK / 2), int(n0), raw_full(pos.slot));
       }
       if (*abort_flag)  // copies still in flight land before the CTA leaves
-        for (int j = issued - 1; j >= 0 && j >= issued - depth; --j)
-          mbar_wait(raw ? raw_full(j % depth) : full_x(j % depth), (j / depth) & 1);
+        for (int j = i - 1; j >= 0 && j >= i - kRawS; --j)
+          mbar_wait(raw_full(j % kRawS), (j / kRawS) & 1);
     }
-  } else if (warp == 8) {
+  } else if (warp == kXWarp) {
     if (lane == 0) {
-      // ---- the MMA issue: stage kt reads weight slot kt % kAS and activation slot
-      // kt % kXS, and releases both when its MMAs complete
+      // ---- activation rows m0 .. m0 + BX - 1, one 64-value K step per slot
+      const uint64_t tx = reinterpret_cast<uint64_t>(&tmap_x);
+      RingPos<kXS> pos;
+      int j = 0;
+      for (; j < kt_count; ++j, pos.next()) {
+        if (j >= kXS) {
+          if (*abort_flag) break;
+          if (!mbar_wait(empty_x(pos.slot), pos.phase ^ 1u)) {
+            fail();
+            break;
+          }
+        }
+        mbar_expect(full_x(pos.slot), S::kB);
+        tma_load_2d(sbase + S::kXOff + pos.slot * S::kB, tx, j * kBK, int(m0),
+                    full_x(pos.slot));
+      }
+      if (*abort_flag)
+        for (int q = j - 1; q >= 0 && q >= j - kXS; --q)
+          mbar_wait(full_x(q % kXS), (q / kXS) & 1);
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      // ---- the MMA issue: K step j reads its weight columns of stage j / kSub and
+      // activation slot j % kXS; each slot is released when its MMAs complete
       const uint32_t idesc = instr_desc<BX>(kBF16);
-      for (int kt = 0; kt < kt_count; ++kt) {
-        const int sa = kt % kAS, sx = kt % kXS;
-        if (*abort_flag) break;
-        if (!mbar_wait(full_x(sx), (kt / kXS) & 1) || !mbar_wait(full_w(sa), (kt / kAS) & 1)) {
-          fail();
+      RingPos<kAS> apos;
+      RingPos<kXS> xpos;
+      bool stop = false;
+      for (int i = 0; i < st_count && !stop; ++i, apos.next()) {
+        if (*abort_flag || !mbar_wait(full_w(apos.slot), apos.phase)) {
+          if (!*abort_flag) fail();
           break;
         }
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const uint32_t a_addr = sbase + sa * S::kA;             // weights: M side
-        const uint32_t b_addr = sbase + S::kXOff + sx * S::kB;  // activations: N side
+        const int ns = min(kSub, kt_count - i * kSub);
+        for (int sub = 0; sub < ns; ++sub, xpos.next()) {
+          if (!mbar_wait(full_x(xpos.slot), xpos.phase)) {
+            fail();
+            stop = true;
+            break;
+          }
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          // weights (M side) from TMEM: 8 columns per 16-value K slice
+          const uint32_t a_tmem = tmem + kATmemCol + (apos.slot * kSub + sub) * 32;
+          const uint32_t b_addr = sbase + S::kXOff + xpos.slot * S::kB;  // activations: N
 #pragma unroll
-        for (int ks = 0; ks < kBK / 16; ++ks) {
-          const uint64_t da = smem_desc(a_addr + ks * 32);
-          const uint64_t db = smem_desc(b_addr + ks * 32);
-          const uint32_t acc = (kt > 0 || ks > 0) ? 1u : 0u;
+          for (int ks = 0; ks < kBK / 16; ++ks) {
+            const uint64_t db = smem_desc(b_addr + ks * 32);
+            const uint32_t acc = (i > 0 || sub > 0 || ks > 0) ? 1u : 0u;
+            asm volatile(
+                "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+                "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}"
+                :: "r"(tmem), "r"(a_tmem + ks * 8), "l"(db), "r"(idesc), "r"(acc));
+          }
           asm volatile(
-              "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-              "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}"
-              :: "r"(tmem), "l"(da), "l"(db), "r"(idesc), "r"(acc));
+              "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+              :: "r"(empty_x(xpos.slot)) : "memory");
         }
+        if (stop) break;
         asm volatile(
             "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-            :: "r"(empty_a(sa)) : "memory");
-        asm volatile(
-            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-            :: "r"(empty_x(sx)) : "memory");
+            :: "r"(empty_a(apos.slot)) : "memory");
       }
       // tracks every MMA issued above, aborted or not
       asm volatile(
@@ -326,72 +423,112 @@ __global__ void __launch_bounds__(kLinThreads, 1)
       mbar_wait(acc_full, 0);  // no MMA still writes TMEM when it is freed below
     }
   } else {
-    // ---- dequantize: thread tid owns weight row r = tid / 2, values 32 h .. 32 h + 31
-    // of every 64-value stage (one block, since blocksize >= 32)
-    const int r = tid >> 1, h = tid & 1;
+    // ---- dequantize: warp w writes TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31, i.e. weight
+    // row r = 32 (w % 4) + lane, values 8 kWords h .. 8 kWords (h + 1) - 1 (h = w / 4) of
+    // every 64-value K step (one block, since blocksize >= 32)
+    constexpr int kAhead = 4;  // weight stages of scale codes / absmax held in registers
+    const int quad = warp & 3, h = warp >> 2;
+    const int r = quad * 32 + lane;
     const int64_t n = n0 + r;
     const bool row_ok = n < p.N;
+    const int64_t idx0 = n * p.K + 8 * kWords * h;  // flat index of this thread's first value
     const float offset = p.w.offset;
-    bool failed = false;
-    uint32_t cq[kCodeAhead];  // scale code and absmax of stage kt live in slot kt % kCodeAhead
-    float aq[kCodeAhead];
-    auto fetch = [&](int kt, uint32_t& c, float& a) {
-      c = 0;
-      a = 0.f;
-      if (row_ok) {
-        const int64_t b = (n * p.K + int64_t(kt) * kBK + 32 * h) >> p.w.log2_bs;
-        c = __ldg(p.w.codes + b);
-        a = __ldg(p.w.absmax + (b >> p.w.log2_nbs));
+    const uint32_t t_row = tmem + (static_cast<uint32_t>(quad * 32) << 16) + kATmemCol +
+                           4 * kWords * h;  // this warp's lanes, its columns of a K step
+    uint32_t cq[kAhead][kSub];  // stage i's codes / absmax live in slot i % kAhead
+    float aq[kAhead][kSub];
+    auto fetch = [&](int i, uint32_t (&c)[kSub], float (&a)[kSub]) {
+#pragma unroll
+      for (int sub = 0; sub < kSub; ++sub) {
+        c[sub] = 0;
+        a[sub] = 0.f;
+        const int j = i * kSub + sub;
+        if (row_ok && j < kt_count) {
+          const int64_t b = (idx0 + int64_t(j) * kBK) >> p.w.log2_bs;
+          c[sub] = __ldg(p.w.codes + b);
+          a[sub] = __ldg(p.w.absmax + (b >> p.w.log2_nbs));
+        }
       }
     };
 #pragma unroll
-    for (int d = 0; d < kCodeAhead; ++d)
-      if (d < kt_count) fetch(d, cq[d], aq[d]);
-    for (int kb = 0; kb < kt_count && !failed; kb += kCodeAhead) {
+    for (int d = 0; d < kAhead; ++d) fetch(d, cq[d], aq[d]);
+    RingPos<kAS> apos;
+    RingPos<kRawS> rpos;
+    bool failed = false;
+    const char* vcb = reinterpret_cast<const char*>(s_vcb);
+    for (int ib = 0; ib < st_count && !failed; ib += kAhead) {
 #pragma unroll
-      for (int d = 0; d < kCodeAhead; ++d) {
-        const int kt = kb + d;
-        if (kt >= kt_count) break;
-        const float sc = __fadd_rn(__fmul_rn(s_scb[cq[d]], aq[d]), offset);  // two roundings
-        if (kt + kCodeAhead < kt_count) fetch(kt + kCodeAhead, cq[d], aq[d]);
-        const int s = kt % kAS, slot = kt % kRawS;
-        bool ok = !*abort_flag && mbar_wait(raw_full(slot), (kt / kRawS) & 1);
-        if (ok && kt >= kAS) ok = mbar_wait(empty_a(s), ((kt / kAS) - 1) & 1);
+      for (int d = 0; d < kAhead; ++d) {
+        const int i = ib + d;
+        if (i >= st_count) break;
+        float sc[kSub];
+#pragma unroll
+        for (int sub = 0; sub < kSub; ++sub)  // two roundings, never an FMA
+          sc[sub] = __fadd_rn(__fmul_rn(s_scb[cq[d][sub]], aq[d][sub]), offset);
+        fetch(i + kAhead, cq[d], aq[d]);
+        // the raw stage has landed and the MMAs that read this weight slot last completed
+        // (the first kAS stages have nothing to wait for: their empty phase reads as done)
+        bool ok = !*abort_flag &&
+                  (mbar_try2(raw_full(rpos.slot), rpos.phase, empty_a(apos.slot),
+                             i >= kAS ? apos.phase ^ 1u : 1u) ||
+                   (mbar_wait(raw_full(rpos.slot), rpos.phase) &&
+                    (i < kAS || mbar_wait(empty_a(apos.slot), apos.phase ^ 1u))));
         if (!__all_sync(kFull, ok)) {  // warp-uniform, so the warp stays converged
           failed = true;
           break;
         }
-        const uint4 w4 =
-            *reinterpret_cast<const uint4*>(base + S::kRawOff + slot * kRawBytes + tid * 16);
-        const uint32_t wd[4] = {w4.x, w4.y, w4.z, w4.w};
-        uint8_t* sA = base + s * S::kA;
-        uint64_t sc2;
-        asm("mov.b64 %0, {%1, %1};" : "=l"(sc2) : "f"(sc));
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const int ns = min(kSub, kt_count - i * kSub);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {  // 8 values: one 16-byte chunk of the swizzled row
-          uint32_t o[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {  // byte j: the high nibble is the earlier value
-            const uint32_t byte = (wd[e] >> (8 * j)) & 0xFFu;
-            float v0, v1;
-            mul2_rn(s_vcb[byte >> 4], s_vcb[byte & 0xFu], sc2, v0, v1);
-            o[j] = pack2<kOut>(v0, v1);
+        for (int sub = 0; sub < kSub; ++sub) {
+          if (sub >= ns) break;
+          // this row's packed words (rows are 32 bytes apart in the raw box)
+          const uint8_t* src = base + S::kRawOff + rpos.slot * S::kRawSlot + sub * kRawBytes +
+                               r * 32 + 4 * kWords * h;
+          uint32_t wd[kWords];
+          if constexpr (kWords == 4) {
+            const uint4 w4 = *reinterpret_cast<const uint4*>(src);
+            wd[0] = w4.x, wd[1] = w4.y, wd[2] = w4.z, wd[3] = w4.w;
+          } else {
+            const uint2 w2 = *reinterpret_cast<const uint2*>(src);
+            wd[0] = w2.x, wd[1] = w2.y;
           }
-          *reinterpret_cast<uint4*>(sA + swz128(r, 4 * h + e)) =
-              row_ok ? make_uint4(o[0], o[1], o[2], o[3]) : make_uint4(0, 0, 0, 0);
+          uint64_t sc2;
+          asm("mov.b64 %0, {%1, %1};" : "=l"(sc2) : "f"(sc[sub]));
+          uint32_t o[4 * kWords];  // 8 values per word, two per 32-bit TMEM column
+#pragma unroll
+          for (int e = 0; e < kWords; ++e) {
+            // nibble * 4 (the byte offset of its codebook entry) in each byte
+            const uint32_t hi4 = (wd[e] >> 2) & 0x3C3C3C3Cu;  // earlier value of each byte
+            const uint32_t lo4 = (wd[e] << 2) & 0x3C3C3C3Cu;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float a = *reinterpret_cast<const float*>(vcb + __byte_perm(hi4, 0, 0x4440 + j));
+              const float b = *reinterpret_cast<const float*>(vcb + __byte_perm(lo4, 0, 0x4440 + j));
+              float v0, v1;
+              mul2_rn(a, b, sc2, v0, v1);
+              o[4 * e + j] = pack2<kOut>(v0, v1);
+            }
+          }
+          // rows past N hold finite values (zero codes, zero-filled nibbles) and only
+          // feed accumulator lanes that are never stored
+          tmem_st<4 * kWords>(t_row + (apos.slot * kSub + sub) * 32, o);
         }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the MMA
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(full_w(s));
-          mbar_arrive(raw_empty(slot));
+          mbar_arrive(full_w(apos.slot));
+          mbar_arrive(raw_empty(rpos.slot));
         }
+        apos.next();
+        rpos.next();
       }
     }
     if (failed && lane == 0) fail();
-    // ---- epilogue: warps w and w + 4 read TMEM lanes 32 (w % 4) .. (weight rows), each
-    // half of the BX accumulator columns (activation rows)
-    bool ok = !failed && !*abort_flag && mbar_wait(acc_full, 0);
+    // ---- epilogue on warps 0..7: warps w and w + 4 read TMEM lanes 32 (w % 4) ..
+    // (weight rows), each half of the BX accumulator columns (activation rows)
+    bool ok = warp < 8 && !failed && !*abort_flag && mbar_wait(acc_full, 0);
     if (__all_sync(kFull, ok && !*abort_flag)) {
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       const int quad = warp & 3;
@@ -423,7 +560,7 @@ __global__ void __launch_bounds__(kLinThreads, 1)
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
-  if (warp == 8) {
+  if (warp == kMmaWarp) {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
                  :: "r"(tmem), "r"(kTmemCols));
