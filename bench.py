@@ -692,36 +692,59 @@ def run_outprod(args):
 
 
 def run_linear(args):
-    """Fused nested dequant + tcgen05 GEMM against dequantize-then-cuBLAS, over M."""
+    """Fused nested dequant + tcgen05 GEMM against dequantize-then-cuBLAS, over M.
+
+    Weight sets rotate (more bytes than L2 holds), so every call streams its
+    packed weight from HBM.  Per M the line gives both times, the cuBLAS GEMM
+    alone, and a roofline: the lower bound is the larger of the tensor time
+    (2 M N K at the measured bf16 peak) and the HBM time (packed weight, codes,
+    absmax, X and Y at the measured copy bandwidth).
+    """
     import torch
 
     import quantized_weight_dequantization_gb300 as dq
 
     dev = torch.device("cuda:0")
     N, K = args.lin_n, args.lin_k
-    p = gen.make_problem(N * K, 64, 256, "nf4", 1.0, 0.0371, seed=31)
-    t = {k: torch.from_numpy(np.ascontiguousarray(getattr(p, k))).to(dev)
-         for k in ("packed", "scale_codes", "nested_absmax", "scale_codebook", "value_codebook")}
-    Wd = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
-    peak_tflops = None
+    peaks = {"hbm_gbs": 6676.8, "bf16_tflops": 1900.0}
+    peak_src = "fallback"
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            peak_tflops = float(json.load(f)["bf16_tflops"])
+            mp = json.load(f)
+        peaks = {"hbm_gbs": float(mp["hbm_gbs"]), "bf16_tflops": float(mp["bf16_tflops"])}
+        peak_src = "measured"
     except (OSError, KeyError, ValueError):
-        peak_tflops = 1900.0
+        pass
+    wbytes = (N * K) // 2 + N * K // 64 + 4 * -(-(N * K // 64) // 256)
+    nsets = max(2, -(-(160 << 20) // wbytes) + 1)
+    sets = []
+    for i in range(nsets):
+        p = gen.make_problem(N * K, 64, 256, "nf4", 1.0, 0.0371, seed=31 + i) if i < 2 else None
+        src = p if p is not None else sets[i % 2]["p"]
+        sets.append({"p": src, **{k: torch.from_numpy(np.ascontiguousarray(getattr(src, k))).to(dev)
+                                  for k in ("packed", "scale_codes", "nested_absmax",
+                                            "scale_codebook", "value_codebook")}})
+    Wd = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
     cells = []
     for M in [int(x) for x in args.lin_m.split(",")]:
         X = torch.from_numpy(gen.make_normal_g(M, K, seed=32)).to(torch.bfloat16).to(dev)
         Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        state = {"i": 0}
+
+        def nxt():
+            state["i"] = (state["i"] + 1) % nsets
+            return sets[state["i"]]
 
         def fused():
+            t = nxt()
             dq.linear(X, t["packed"], t["scale_codes"], t["nested_absmax"], t["scale_codebook"],
-                      t["value_codebook"], float(p.offset), N, 64, 256, Y=Y)
+                      t["value_codebook"], float(t["p"].offset), N, 64, 256, Y=Y)
 
         def unfused():
+            t = nxt()
             dq.dq4_nested(t["packed"], t["scale_codes"], t["nested_absmax"],
-                          t["scale_codebook"], t["value_codebook"], float(p.offset), N * K, 64,
-                          256, torch.bfloat16, out=Wd.view(-1))
+                          t["scale_codebook"], t["value_codebook"], float(t["p"].offset), N * K,
+                          64, 256, torch.bfloat16, out=Wd.view(-1))
             torch.matmul(X, Wd.t(), out=Y)
 
         def gemm_only():
@@ -741,18 +764,31 @@ def run_linear(args):
             torch.cuda.synchronize(dev)
             res[name] = e0.elapsed_time(e1) / k * 1e3
         flops = 2.0 * M * N * K
-        wbytes = (N * K) // 2 + N * K // 64 + 4 * (N * K // 16384)
-        cells.append({"M": M, "fused_us": res["fused"], "unfused_us": res["unfused"],
-                      "cublas_gemm_only_us": res["cublas_gemm_only"],
-                      "fused_tflops": flops / (res["fused"] / 1e6) / 1e12,
-                      "fused_frac_of_bf16_peak": flops / (res["fused"] / 1e6) / 1e12 / peak_tflops,
-                      "fused_weight_gbs": wbytes / (res["fused"] / 1e6) / 1e9,
-                      "speedup_vs_unfused": res["unfused"] / res["fused"]})
+        nbytes = wbytes + 2 * M * K + 2 * M * N
+        t_tensor = flops / (peaks["bf16_tflops"] * 1e12) * 1e6
+        t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9) * 1e6
+        tensor_bound = t_tensor >= t_hbm
+        us = res["fused"]
+        cells.append({
+            "M": M, "fused_us": us, "unfused_us": res["unfused"],
+            "cublas_gemm_only_us": res["cublas_gemm_only"],
+            "speedup_vs_unfused": res["unfused"] / us,
+            "roofline": {"bound": "tensor" if tensor_bound else "hbm",
+                         "achieved": flops / us / 1e6 if tensor_bound else nbytes / us / 1e3,
+                         "peak": peaks["bf16_tflops"] if tensor_bound else peaks["hbm_gbs"],
+                         "unit": "TFLOP/s" if tensor_bound else "GB/s",
+                         "frac": max(t_tensor, t_hbm) / us,
+                         "traffic": None},
+            "weight_bytes": wbytes, "algorithmic_bytes": nbytes, "flops": flops})
     print(json.dumps({
         "metric": "fused nested dequant + tcgen05 GEMM (Y = X W^T) time", "unit": "us",
         "higher_is_better": False, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"linear N={N} K={K} NF4-style nested (bs 64, nested 256), "
-                               "BF16 X and Y", "bf16_peak_tflops": peak_tflops},
+                               "BF16 X and Y",
+                   "l2": f"{nsets} rotating weight sets of {wbytes} bytes (> L2)",
+                   "peaks": peak_src, **peaks},
+        "gpu_launches_per_step": 1,
         "cells": cells}), flush=True)
 
 

@@ -17,13 +17,16 @@
 //    ahead as the ring allows;
 //  * warp 10 (lane 0): streams the activation tiles (BX rows x 64 K, 128-byte
 //    swizzle, rows past M zero-filled) with TMA into their own ring;
-//  * warps 0..7: warp w owns TMEM lanes 32 (w % 4) .. (the weight rows) and
-//    half of every 64-value K step (w / 4).  Per K step a thread computes the
-//    nested scale of its row's block (separately rounded FP32 multiply and
-//    add; the scale codes and absmax values are loaded four stages ahead into
-//    registers) and its 32 values (FP32 products, RN to BF16 / FP16), and
+//  * warps 0..7, two groups of four that take alternate weight stages (so one
+//    group's barrier polls overlap the other's arithmetic): warp w owns TMEM
+//    lanes 32 (w % 4) .. (the weight rows), a thread one row.  Per 64-value K
+//    step it computes the nested scales of its row's two 32-value halves
+//    (separately rounded FP32 multiply and add; a stage's scale codes come in
+//    one aligned load when the shape allows, held two own stages ahead in
+//    registers) and the 64 values (FP32 products, RN to BF16 / FP16), and
 //    writes them to the weight ring in TMEM with one tcgen05.st; afterwards
-//    the epilogue: tcgen05.ld of the accumulator, conversion, stores of Y;
+//    warps 0..7 run the epilogue: tcgen05.ld of the accumulator, conversion,
+//    stores of Y;
 //  * warp 8: allocates the TMEM; lane 0 issues tcgen05.mma (A = weights from
 //    TMEM, B = activations from shared memory, M = 128, N = BX, K = 16) for
 //    each K step and commits the weight and activation slots back to their
@@ -44,10 +47,17 @@ namespace {
 #ifndef DQ4_LIN_PWARPS
 #define DQ4_LIN_PWARPS 8  // dequantizing warps per CTA: 8 or 16
 #endif
+#ifndef DQ4_LIN_GROUPS
+#define DQ4_LIN_GROUPS 2  // producer groups that take alternate weight stages: 1 or 2
+#endif
 constexpr int kProducerWarps = DQ4_LIN_PWARPS;
-static_assert(kProducerWarps == 8 || kProducerWarps == 16, "2 or 4 threads per weight row");
-constexpr int kTPR = kProducerWarps / 4;           // producer threads per weight row
+constexpr int kGroups = DQ4_LIN_GROUPS;
+constexpr int kGroupWarps = kProducerWarps / kGroups;  // warps writing one weight stage
+static_assert(kProducerWarps == 8 || kProducerWarps == 16, "8 or 16 producer warps");
+static_assert(kGroupWarps == 4 || kGroupWarps == 8 || kGroupWarps == 16, "whole quadrants");
+constexpr int kTPR = kGroupWarps / 4;              // producer threads per weight row
 constexpr int kWords = 8 / kTPR;                   // packed 32-bit words per thread and K step
+constexpr int kHalves = kWords >= 8 ? 2 : 1;       // 32-value halves per thread and K step
 constexpr int kMmaWarp = kProducerWarps;           // also allocates TMEM
 constexpr int kRawWarp = kProducerWarps + 1;       // weight TMA
 constexpr int kXWarp = kProducerWarps + 2;         // activation TMA
@@ -168,22 +178,33 @@ __device__ __forceinline__ void mul2_rn(float a, float b, uint64_t s2, float& x,
   asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(r));
 }
 
-// Store N (8 or 16) consecutive 32-bit columns of this warp's 32 TMEM lanes.
+// Store N (8, 16 or 32) consecutive 32-bit columns of this warp's 32 TMEM lanes.  It
+// reads registers only, so it carries no memory clobber and the compiler may move
+// shared-memory loads across it; tcgen05.wait::st (volatile, in order) completes it.
 template <int N>
 __device__ __forceinline__ void tmem_st(uint32_t taddr, const uint32_t (&v)[N]) {
-  if constexpr (N == 16) {
+  if constexpr (N == 32) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+        :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]),
+           "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]),
+           "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]),
+           "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]),
+           "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31]));
+  } else if constexpr (N == 16) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
         "%13,%14,%15,%16};"
         :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]),
            "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]),
-           "r"(v[13]), "r"(v[14]), "r"(v[15]) : "memory");
+           "r"(v[13]), "r"(v[14]), "r"(v[15]));
   } else {
-    static_assert(N == 8, "8 or 16 columns");
+    static_assert(N == 8, "8, 16 or 32 columns");
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
         :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]),
-           "r"(v[6]), "r"(v[7]) : "memory");
+           "r"(v[6]), "r"(v[7]));
   }
 }
 
@@ -194,6 +215,9 @@ struct LinArgs {
   int* bad;        // optional device counter of timed-out waits
   int out_dtype;
   int tiles_x;     // activation-row tiles of Y
+  // bytes of scale codes one weight stage (64 kSub values of a row) spans, when those
+  // codes form one aligned window with one absmax group (else 0: one load per K step)
+  int code_window;
 };
 
 // The dequantized weights (the MMA's A operand) live in TMEM: columns 0 ..
@@ -303,7 +327,7 @@ __global__ void __launch_bounds__(kLinThreads, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     if (lane == 0) {
       for (int s = 0; s < kAS; ++s) {
-        mbar_init(full_w(s), kProducerWarps);
+        mbar_init(full_w(s), kGroupWarps);
         mbar_init(empty_a(s), 1);
       }
       for (int s = 0; s < kXS; ++s) {
@@ -312,7 +336,7 @@ __global__ void __launch_bounds__(kLinThreads, 1)
       }
       for (int s = 0; s < kRawS; ++s) {
         mbar_init(raw_full(s), 1);
-        mbar_init(raw_empty(s), kProducerWarps);
+        mbar_init(raw_empty(s), kGroupWarps);
       }
       mbar_init(acc_full, 1);
       *abort_flag = 0;
@@ -423,11 +447,14 @@ __global__ void __launch_bounds__(kLinThreads, 1)
       mbar_wait(acc_full, 0);  // no MMA still writes TMEM when it is freed below
     }
   } else {
-    // ---- dequantize: warp w writes TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31, i.e. weight
-    // row r = 32 (w % 4) + lane, values 8 kWords h .. 8 kWords (h + 1) - 1 (h = w / 4) of
-    // every 64-value K step (one block, since blocksize >= 32)
-    constexpr int kAhead = 4;  // weight stages of scale codes / absmax held in registers
-    const int quad = warp & 3, h = warp >> 2;
+    // ---- dequantize.  Producer group `group` (kGroupWarps warps) takes weight stages
+    // group, group + kGroups, ...; within it, warp w writes TMEM lanes 32 (w % 4) ..
+    // (weight row r = 32 (w % 4) + lane) and values 8 kWords h .. 8 kWords (h + 1) - 1
+    // of every 64-value K step, h = (w % kGroupWarps) / 4.  kHalves 32-value halves
+    // per K step each lie in one block (blocksize >= 32).
+    constexpr int kAhead = kGroups == 1 ? 4 : 2;  // own stages of codes held in registers
+    const int gw = warp % kGroupWarps, group = warp / kGroupWarps;
+    const int quad = gw & 3, h = gw >> 2;
     const int r = quad * 32 + lane;
     const int64_t n = n0 + r;
     const bool row_ok = n < p.N;
@@ -435,37 +462,72 @@ __global__ void __launch_bounds__(kLinThreads, 1)
     const float offset = p.w.offset;
     const uint32_t t_row = tmem + (static_cast<uint32_t>(quad * 32) << 16) + kATmemCol +
                            4 * kWords * h;  // this warp's lanes, its columns of a K step
-    uint32_t cq[kAhead][kSub];  // stage i's codes / absmax live in slot i % kAhead
-    float aq[kAhead][kSub];
-    auto fetch = [&](int i, uint32_t (&c)[kSub], float (&a)[kSub]) {
-#pragma unroll
-      for (int sub = 0; sub < kSub; ++sub) {
-        c[sub] = 0;
-        a[sub] = 0.f;
-        const int j = i * kSub + sub;
-        if (row_ok && j < kt_count) {
-          const int64_t b = (idx0 + int64_t(j) * kBK) >> p.w.log2_bs;
-          c[sub] = __ldg(p.w.codes + b);
-          a[sub] = __ldg(p.w.absmax + (b >> p.w.log2_nbs));
+    uint32_t cq[kAhead][kSub][kHalves];  // own stage q's codes / absmax in slot q % kAhead
+    float aq[kAhead][kSub][kHalves];
+    auto fetch = [&](int i, uint32_t (&c)[kSub][kHalves], float (&a)[kSub][kHalves]) {
+      if (p.code_window != 0) {
+        // the stage's codes of this row in one aligned load, its absmax in another
+        uint64_t win = 0;
+        float am = 0.f;
+        const int j0 = i * kSub;
+        if (row_ok && j0 < kt_count) {
+          const int64_t b00 = (n * p.K + int64_t(j0) * kBK) >> p.w.log2_bs;
+          const uint8_t* cp = p.w.codes + b00;
+          switch (p.code_window) {
+            case 8: win = __ldg(reinterpret_cast<const unsigned long long*>(cp)); break;
+            case 4: win = __ldg(reinterpret_cast<const unsigned int*>(cp)); break;
+            case 2: win = __ldg(reinterpret_cast<const unsigned short*>(cp)); break;
+            default: win = __ldg(cp); break;
+          }
+          am = __ldg(p.w.absmax + (b00 >> p.w.log2_nbs));
         }
+#pragma unroll
+        for (int sub = 0; sub < kSub; ++sub)
+#pragma unroll
+          for (int hh = 0; hh < kHalves; ++hh) {
+            const int off = (kBK * sub + 32 * hh + 8 * kWords * h) >> p.w.log2_bs;
+            c[sub][hh] = static_cast<uint32_t>(win >> (8 * off)) & 0xFFu;  // off < window
+            a[sub][hh] = am;
+          }
+        return;
       }
+#pragma unroll
+      for (int sub = 0; sub < kSub; ++sub)
+#pragma unroll
+        for (int hh = 0; hh < kHalves; ++hh) {
+          c[sub][hh] = 0;
+          a[sub][hh] = 0.f;
+          const int j = i * kSub + sub;
+          if (row_ok && j < kt_count) {
+            const int64_t b = (idx0 + int64_t(j) * kBK + 32 * hh) >> p.w.log2_bs;
+            c[sub][hh] = __ldg(p.w.codes + b);
+            a[sub][hh] = __ldg(p.w.absmax + (b >> p.w.log2_nbs));
+          }
+        }
     };
 #pragma unroll
-    for (int d = 0; d < kAhead; ++d) fetch(d, cq[d], aq[d]);
+    for (int d = 0; d < kAhead; ++d) fetch(group + d * kGroups, cq[d], aq[d]);
     RingPos<kAS> apos;
     RingPos<kRawS> rpos;
+    for (int g = 0; g < group; ++g) {  // this group's first stage
+      apos.next();
+      rpos.next();
+    }
     bool failed = false;
     const char* vcb = reinterpret_cast<const char*>(s_vcb);
-    for (int ib = 0; ib < st_count && !failed; ib += kAhead) {
+    for (int qb = 0; !failed; qb += kAhead) {
+      if (group + qb * kGroups >= st_count) break;
 #pragma unroll
       for (int d = 0; d < kAhead; ++d) {
-        const int i = ib + d;
+        const int i = group + (qb + d) * kGroups;  // global weight stage
         if (i >= st_count) break;
-        float sc[kSub];
+        float sc[kSub][kHalves];
 #pragma unroll
-        for (int sub = 0; sub < kSub; ++sub)  // two roundings, never an FMA
-          sc[sub] = __fadd_rn(__fmul_rn(s_scb[cq[d][sub]], aq[d][sub]), offset);
-        fetch(i + kAhead, cq[d], aq[d]);
+        for (int sub = 0; sub < kSub; ++sub)
+#pragma unroll
+          for (int hh = 0; hh < kHalves; ++hh)  // two roundings, never an FMA
+            sc[sub][hh] = __fadd_rn(__fmul_rn(s_scb[cq[d][sub][hh]], aq[d][sub][hh]), offset);
+        fetch(i + kAhead * kGroups, cq[d], aq[d]);
         // the raw stage has landed and the MMAs that read this weight slot last completed
         // (the first kAS stages have nothing to wait for: their empty phase reads as done)
         bool ok = !*abort_flag &&
@@ -479,22 +541,39 @@ __global__ void __launch_bounds__(kLinThreads, 1)
         }
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const int ns = min(kSub, kt_count - i * kSub);
+        // all of the stage's packed words of this row first: one shared-memory latency
+        uint32_t wds[kSub][kWords];
+#pragma unroll
+        for (int sub = 0; sub < kSub; ++sub) {
+          // rows are 32 bytes apart in each raw box, whose 32-byte swizzle stores the
+          // 16-byte chunk c of row r at chunk c ^ ((r >> 2) & 1): the 8 rows a quarter
+          // warp reads then fill all 32 banks.  A partial last stage reads a box that
+          // holds stale bytes, whose values are never stored.
+          const uint8_t* row = base + S::kRawOff + rpos.slot * S::kRawSlot + sub * kRawBytes +
+                               r * 32;
+          const int flip = (r >> 2) & 1;
+#pragma unroll
+          for (int v = 0; v < (kWords + 3) / 4; ++v) {
+            const int chunk = (kWords * h) / 4 + v;       // logical 16-byte chunk of the row
+            const uint8_t* src = row + (((chunk ^ flip) & 1) << 4) + ((kWords * h) % 4) * 4;
+            if constexpr (kWords >= 4) {
+              const uint4 w4 = *reinterpret_cast<const uint4*>(src);
+              wds[sub][4 * v] = w4.x, wds[sub][4 * v + 1] = w4.y;
+              wds[sub][4 * v + 2] = w4.z, wds[sub][4 * v + 3] = w4.w;
+            } else {
+              const uint2 w2 = *reinterpret_cast<const uint2*>(src);
+              wds[sub][0] = w2.x, wds[sub][1] = w2.y;
+            }
+          }
+        }
 #pragma unroll
         for (int sub = 0; sub < kSub; ++sub) {
           if (sub >= ns) break;
-          // this row's packed words (rows are 32 bytes apart in the raw box)
-          const uint8_t* src = base + S::kRawOff + rpos.slot * S::kRawSlot + sub * kRawBytes +
-                               r * 32 + 4 * kWords * h;
-          uint32_t wd[kWords];
-          if constexpr (kWords == 4) {
-            const uint4 w4 = *reinterpret_cast<const uint4*>(src);
-            wd[0] = w4.x, wd[1] = w4.y, wd[2] = w4.z, wd[3] = w4.w;
-          } else {
-            const uint2 w2 = *reinterpret_cast<const uint2*>(src);
-            wd[0] = w2.x, wd[1] = w2.y;
-          }
-          uint64_t sc2;
-          asm("mov.b64 %0, {%1, %1};" : "=l"(sc2) : "f"(sc[sub]));
+          const uint32_t (&wd)[kWords] = wds[sub];
+          uint64_t sc2[kHalves];
+#pragma unroll
+          for (int hh = 0; hh < kHalves; ++hh)
+            asm("mov.b64 %0, {%1, %1};" : "=l"(sc2[hh]) : "f"(sc[sub][hh]));
           uint32_t o[4 * kWords];  // 8 values per word, two per 32-bit TMEM column
 #pragma unroll
           for (int e = 0; e < kWords; ++e) {
@@ -506,7 +585,7 @@ __global__ void __launch_bounds__(kLinThreads, 1)
               const float a = *reinterpret_cast<const float*>(vcb + __byte_perm(hi4, 0, 0x4440 + j));
               const float b = *reinterpret_cast<const float*>(vcb + __byte_perm(lo4, 0, 0x4440 + j));
               float v0, v1;
-              mul2_rn(a, b, sc2, v0, v1);
+              mul2_rn(a, b, sc2[e / 4 < kHalves ? e / 4 : 0], v0, v1);
               o[4 * e + j] = pack2<kOut>(v0, v1);
             }
           }
@@ -521,8 +600,11 @@ __global__ void __launch_bounds__(kLinThreads, 1)
           mbar_arrive(full_w(apos.slot));
           mbar_arrive(raw_empty(rpos.slot));
         }
-        apos.next();
-        rpos.next();
+#pragma unroll
+        for (int g = 0; g < kGroups; ++g) {
+          apos.next();
+          rpos.next();
+        }
       }
     }
     if (failed && lane == 0) fail();
@@ -703,13 +785,13 @@ int dq4_nested_linear(const void* X, int32_t in_dtype, const uint8_t* packed,
                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return fail_cuda(DQ4_ERR_LAUNCH, cudaErrorInvalidValue);
-  // the packed weight as N rows of K / 2 bytes: 32 x 128 boxes, unswizzled
+  // the packed weight as N rows of K / 2 bytes: 32 x 128 boxes, 32-byte swizzle
   CUtensorMap tw;
   const cuuint64_t wdim[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(N)};
   const cuuint64_t wstride[1] = {static_cast<cuuint64_t>(K / 2)};
   const cuuint32_t wbox[2] = {kBK / 2, kBW};
   cr = encode(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(packed), wdim,
-              wstride, wbox, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              wstride, wbox, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return fail_cuda(DQ4_ERR_LAUNCH, cudaErrorInvalidValue);
 
@@ -723,6 +805,18 @@ int dq4_nested_linear(const void* X, int32_t in_dtype, const uint8_t* packed,
   p.bad = bad;
   p.out_dtype = out_dtype;
   p.tiles_x = static_cast<int>(tiles_x);
+  {
+    // a stage covers 64 kSub values of a row, starting at a multiple of that when K is
+    // one; its codes are then blocks b00 .. b00 + window - 1 with b00 a multiple of the
+    // window, all in one absmax group when the window is at most nested_blocksize
+    const int64_t span = int64_t(kBK) * kSub;
+    int64_t window = span / blocksize;
+    if (window < 1) window = 1;
+    p.code_window = (K % span == 0 && window <= nested_blocksize && window <= 8 &&
+                     !misaligned(scale_codes, static_cast<int>(window)))
+                        ? static_cast<int>(window)
+                        : 0;
+  }
   const auto st = static_cast<cudaStream_t>(stream);
   const int64_t grid = tiles_x * tiles_w;
   return in_dtype == DQ4_OUT_BF16 ? launch_bx<true>(bx, tx, tw, p, grid, st, dev)

@@ -72,13 +72,33 @@ def test_integer_exact(dq, M, N, K, xin):
     assert int(bad.item()) == 0
 
 
-@pytest.mark.parametrize("bs,nbs", [(32, 1), (4096, 256), (64, 2)])
+# With K a multiple of 256 the kernel reads each row's scale codes for four K
+# steps in one aligned load of 256 / blocksize bytes (8, 4, 2 or 1) when one
+# absmax group covers them; (32, 1) and (64, 2) take the per-K-step loads.
+@pytest.mark.parametrize("bs,nbs", [(32, 1), (4096, 256), (64, 2), (32, 256), (128, 4),
+                                    (256, 1), (64, 4)])
 def test_blocksizes(dq, bs, nbs):
     M, N, K = 256, 512, 4096
     p = gen.make_integer_problem(N, K, blocksize=bs, nested_blocksize=nbs, seed=bs)
     X = torch.from_numpy(gen.make_ternary_g(M, K, seed=3)).to(torch.bfloat16).to(DEV)
     got = run(dq, p, X, N, K, out=torch.float32).double().cpu().numpy()
     assert np.array_equal(got, oracle.linear(p, x_bits(X), "bf16", N, K, threads=16))
+
+
+def test_unaligned_scale_codes(dq):
+    """Codes at an odd address: the per-K-step loads, same result."""
+    M, N, K = 64, 384, 1024
+    p = gen.make_integer_problem(N, K, seed=5)
+    X = torch.from_numpy(gen.make_ternary_g(M, K, seed=6)).to(torch.bfloat16).to(DEV)
+    t = {k: torch.from_numpy(np.ascontiguousarray(getattr(p, k))).to(DEV)
+         for k in ("packed", "nested_absmax", "scale_codebook", "value_codebook")}
+    buf = torch.zeros(p.scale_codes.size + 1, dtype=torch.uint8, device=DEV)
+    codes = buf[1:]
+    codes.copy_(torch.from_numpy(p.scale_codes))
+    got = dq.linear(X, t["packed"], codes, t["nested_absmax"], t["scale_codebook"],
+                    t["value_codebook"], 0.0, N, 64, 256, out_dtype=torch.float32)
+    want = oracle.linear(p, x_bits(X), "bf16", N, K, threads=16)
+    assert np.array_equal(got.double().cpu().numpy(), want)
 
 
 @pytest.mark.parametrize("M", [16, 512])
