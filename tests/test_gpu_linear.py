@@ -51,11 +51,12 @@ def rounded(y64, out):
 
 
 # The kernel picks its activation-tile width BX from M, N and the SM count; on a
-# 152-SM GB300 the last four shapes take BX = 32, 64, 128 and 256 (38 weight tiles,
-# the last one ragged), the others BX = 16 or 128.
+# 152-SM GB300 the shapes with N = 4860 take BX = 32, 64, 128 and 256 (38 weight tiles,
+# the last one ragged), the others BX = 16 or 128; N = 4700 gives an odd count of
+# weight tiles (37) at BX = 128 and 256.
 SHAPES = [(1, 128, 64), (5, 200, 128), (127, 130, 192), (128, 256, 4096), (300, 1000, 512),
           (129, 384, 1024), (2048, 768, 256), (128, 4860, 192), (256, 4860, 128),
-          (512, 4860, 64), (1024, 4860, 256)]
+          (512, 4860, 64), (1024, 4860, 256), (512, 4700, 128), (2048, 4700, 64)]
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
