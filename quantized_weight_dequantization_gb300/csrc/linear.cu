@@ -48,12 +48,13 @@ namespace {
 #define DQ4_LIN_PWARPS 8  // dequantizing warps per CTA: 8 or 16
 #endif
 #ifndef DQ4_LIN_GROUPS
-#define DQ4_LIN_GROUPS 2  // producer groups that take alternate weight stages: 1 or 2
+#define DQ4_LIN_GROUPS 2  // producer groups that take turns on weight stages: 1, 2 or 4
 #endif
 constexpr int kProducerWarps = DQ4_LIN_PWARPS;
 constexpr int kGroups = DQ4_LIN_GROUPS;
 constexpr int kGroupWarps = kProducerWarps / kGroups;  // warps writing one weight stage
 static_assert(kProducerWarps == 8 || kProducerWarps == 16, "8 or 16 producer warps");
+static_assert(kGroups == 1 || kGroups == 2 || kGroups == 4, "1, 2 or 4 producer groups");
 static_assert(kGroupWarps == 4 || kGroupWarps == 8 || kGroupWarps == 16, "whole quadrants");
 constexpr int kTPR = kGroupWarps / 4;              // producer threads per weight row
 constexpr int kWords = 8 / kTPR;                   // packed 32-bit words per thread and K step
@@ -243,13 +244,21 @@ template <int BX>
 struct LinSmem {
   static constexpr int kAS = kASOf(BX);              // weight stages in TMEM
   static_assert(kAS >= 2, "double-buffered weight ring");
+  // mbarrier waits test a phase's parity, so a waiter must never be two phases ahead
+  // of the barrier.  A group at stage i waits for the MMAs of stage i - kAS and knows,
+  // from its previous wait, that those of stage i - kGroups - kAS completed (MMAs
+  // complete in order): kAS >= kGroups keeps it at most one phase ahead.
+  static_assert(kAS >= kGroups, "no producer group runs two weight phases ahead");
   static_assert(kATmem(BX) + kAS * kSub * 32 <= kTmemCols, "weight ring fits TMEM");
   static constexpr int kRawSlot = kSub * kRawBytes;
   static constexpr int kB = BX * kBK * 2;           // one K step of activations
   static constexpr int kXS = BX <= 32 ? 12 : BX == 64 ? 8 : BX == 128 ? 6 : 4;
   // raw weight stages: what the activation ring leaves of a 220 KB budget, at most 16
   static constexpr int kRawFit = (220 * 1024 - kXS * kB) / kRawSlot;
-  static constexpr int kRawS = kRawFit < 16 ? kRawFit : 16;
+  // A group waits for the raw load of its stage i; the load into the same slot before it
+  // (stage i - kRawS) must be known complete, which holds when that stage is the group's
+  // own: kRawS a multiple of kGroups (TMA loads need not complete in issue order).
+  static constexpr int kRawS = (kRawFit < 16 ? kRawFit : 16) / kGroups * kGroups;
   static_assert(kRawS >= 4, "raw ring too shallow");
   static constexpr int kXOff = 0;
   static constexpr int kRawOff = kXOff + kXS * kB;
@@ -452,7 +461,6 @@ __global__ void __launch_bounds__(kLinThreads, 1)
     // (weight row r = 32 (w % 4) + lane) and values 8 kWords h .. 8 kWords (h + 1) - 1
     // of every 64-value K step, h = (w % kGroupWarps) / 4.  kHalves 32-value halves
     // per K step each lie in one block (blocksize >= 32).
-    constexpr int kAhead = kGroups == 1 ? 4 : 2;  // own stages of codes held in registers
     const int gw = warp % kGroupWarps, group = warp / kGroupWarps;
     const int quad = gw & 3, h = gw >> 2;
     const int r = quad * 32 + lane;
@@ -462,8 +470,6 @@ __global__ void __launch_bounds__(kLinThreads, 1)
     const float offset = p.w.offset;
     const uint32_t t_row = tmem + (static_cast<uint32_t>(quad * 32) << 16) + kATmemCol +
                            4 * kWords * h;  // this warp's lanes, its columns of a K step
-    uint32_t cq[kAhead][kSub][kHalves];  // own stage q's codes / absmax in slot q % kAhead
-    float aq[kAhead][kSub][kHalves];
     auto fetch = [&](int i, uint32_t (&c)[kSub][kHalves], float (&a)[kSub][kHalves]) {
       if (p.code_window != 0) {
         // the stage's codes of this row in one aligned load, its absmax in another
@@ -505,8 +511,12 @@ __global__ void __launch_bounds__(kLinThreads, 1)
           }
         }
     };
-#pragma unroll
-    for (int d = 0; d < kAhead; ++d) fetch(group + d * kGroups, cq[d], aq[d]);
+    // the codes / absmax of this group's next two stages, rotated every stage (no
+    // unrolling over stages: the loop body stays small enough for the instruction cache)
+    uint32_t cA[kSub][kHalves], cB[kSub][kHalves];
+    float aA[kSub][kHalves], aB[kSub][kHalves];
+    fetch(group, cA, aA);
+    fetch(group + kGroups, cB, aB);
     RingPos<kAS> apos;
     RingPos<kRawS> rpos;
     for (int g = 0; g < group; ++g) {  // this group's first stage
@@ -515,96 +525,91 @@ __global__ void __launch_bounds__(kLinThreads, 1)
     }
     bool failed = false;
     const char* vcb = reinterpret_cast<const char*>(s_vcb);
-    for (int qb = 0; !failed; qb += kAhead) {
-      if (group + qb * kGroups >= st_count) break;
+    const int flip = (r >> 2) & 1;  // the raw boxes' 32-byte swizzle for this row
+    for (int i = group; i < st_count; i += kGroups) {  // global weight stage i
+      float sc[kSub][kHalves];
 #pragma unroll
-      for (int d = 0; d < kAhead; ++d) {
-        const int i = group + (qb + d) * kGroups;  // global weight stage
-        if (i >= st_count) break;
-        float sc[kSub][kHalves];
+      for (int sub = 0; sub < kSub; ++sub)
 #pragma unroll
-        for (int sub = 0; sub < kSub; ++sub)
-#pragma unroll
-          for (int hh = 0; hh < kHalves; ++hh)  // two roundings, never an FMA
-            sc[sub][hh] = __fadd_rn(__fmul_rn(s_scb[cq[d][sub][hh]], aq[d][sub][hh]), offset);
-        fetch(i + kAhead * kGroups, cq[d], aq[d]);
-        // the raw stage has landed and the MMAs that read this weight slot last completed
-        // (the first kAS stages have nothing to wait for: their empty phase reads as done)
-        bool ok = !*abort_flag &&
-                  (mbar_try2(raw_full(rpos.slot), rpos.phase, empty_a(apos.slot),
-                             i >= kAS ? apos.phase ^ 1u : 1u) ||
-                   (mbar_wait(raw_full(rpos.slot), rpos.phase) &&
-                    (i < kAS || mbar_wait(empty_a(apos.slot), apos.phase ^ 1u))));
-        if (!__all_sync(kFull, ok)) {  // warp-uniform, so the warp stays converged
-          failed = true;
-          break;
+        for (int hh = 0; hh < kHalves; ++hh) {  // two roundings, never an FMA
+          sc[sub][hh] = __fadd_rn(__fmul_rn(s_scb[cA[sub][hh]], aA[sub][hh]), offset);
+          cA[sub][hh] = cB[sub][hh];
+          aA[sub][hh] = aB[sub][hh];
         }
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const int ns = min(kSub, kt_count - i * kSub);
-        // all of the stage's packed words of this row first: one shared-memory latency
-        uint32_t wds[kSub][kWords];
+      fetch(i + 2 * kGroups, cB, aB);
+      // the raw stage has landed and the MMAs that read this weight slot last completed
+      // (the first kAS stages have nothing to wait for: their empty phase reads as done)
+      bool ok = !*abort_flag &&
+                (mbar_try2(raw_full(rpos.slot), rpos.phase, empty_a(apos.slot),
+                           i >= kAS ? apos.phase ^ 1u : 1u) ||
+                 (mbar_wait(raw_full(rpos.slot), rpos.phase) &&
+                  (i < kAS || mbar_wait(empty_a(apos.slot), apos.phase ^ 1u))));
+      if (!__all_sync(kFull, ok)) {  // warp-uniform, so the warp stays converged
+        failed = true;
+        break;
+      }
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const int ns = min(kSub, kt_count - i * kSub);
+      // rows are 32 bytes apart in each raw box, whose 32-byte swizzle stores the 16-byte
+      // chunk c of row r at chunk c ^ ((r >> 2) & 1): the 8 rows a quarter warp reads then
+      // fill all 32 banks
+      const uint8_t* raw_row = base + S::kRawOff + rpos.slot * S::kRawSlot + r * 32;
+      const uint32_t t_stage = t_row + apos.slot * kSub * 32;
+#pragma unroll 1
+      for (int sub = 0; sub < ns; ++sub) {
+        // this K step's scales, picked by selects rather than a register-array index
+        uint64_t sc2[kHalves];
 #pragma unroll
-        for (int sub = 0; sub < kSub; ++sub) {
-          // rows are 32 bytes apart in each raw box, whose 32-byte swizzle stores the
-          // 16-byte chunk c of row r at chunk c ^ ((r >> 2) & 1): the 8 rows a quarter
-          // warp reads then fill all 32 banks.  A partial last stage reads a box that
-          // holds stale bytes, whose values are never stored.
-          const uint8_t* row = base + S::kRawOff + rpos.slot * S::kRawSlot + sub * kRawBytes +
-                               r * 32;
-          const int flip = (r >> 2) & 1;
+        for (int hh = 0; hh < kHalves; ++hh) {
+          float v = sc[0][hh];
 #pragma unroll
-          for (int v = 0; v < (kWords + 3) / 4; ++v) {
-            const int chunk = (kWords * h) / 4 + v;       // logical 16-byte chunk of the row
-            const uint8_t* src = row + (((chunk ^ flip) & 1) << 4) + ((kWords * h) % 4) * 4;
-            if constexpr (kWords >= 4) {
-              const uint4 w4 = *reinterpret_cast<const uint4*>(src);
-              wds[sub][4 * v] = w4.x, wds[sub][4 * v + 1] = w4.y;
-              wds[sub][4 * v + 2] = w4.z, wds[sub][4 * v + 3] = w4.w;
-            } else {
-              const uint2 w2 = *reinterpret_cast<const uint2*>(src);
-              wds[sub][0] = w2.x, wds[sub][1] = w2.y;
-            }
+          for (int k = 1; k < kSub; ++k) v = sub == k ? sc[k][hh] : v;
+          asm("mov.b64 %0, {%1, %1};" : "=l"(sc2[hh]) : "f"(v));
+        }
+        uint32_t wd[kWords];
+        const uint8_t* row = raw_row + sub * kRawBytes;
+#pragma unroll
+        for (int v = 0; v < (kWords + 3) / 4; ++v) {
+          const int chunk = (kWords * h) / 4 + v;  // logical 16-byte chunk of the row
+          const uint8_t* src = row + (((chunk ^ flip) & 1) << 4) + ((kWords * h) % 4) * 4;
+          if constexpr (kWords >= 4) {
+            const uint4 w4 = *reinterpret_cast<const uint4*>(src);
+            wd[4 * v] = w4.x, wd[4 * v + 1] = w4.y, wd[4 * v + 2] = w4.z, wd[4 * v + 3] = w4.w;
+          } else {
+            const uint2 w2 = *reinterpret_cast<const uint2*>(src);
+            wd[0] = w2.x, wd[1] = w2.y;
           }
         }
+        uint32_t o[4 * kWords];  // 8 values per word, two per 32-bit TMEM column
 #pragma unroll
-        for (int sub = 0; sub < kSub; ++sub) {
-          if (sub >= ns) break;
-          const uint32_t (&wd)[kWords] = wds[sub];
-          uint64_t sc2[kHalves];
+        for (int e = 0; e < kWords; ++e) {
+          // nibble * 4 (the byte offset of its codebook entry) in each byte
+          const uint32_t hi4 = (wd[e] >> 2) & 0x3C3C3C3Cu;  // earlier value of each byte
+          const uint32_t lo4 = (wd[e] << 2) & 0x3C3C3C3Cu;
 #pragma unroll
-          for (int hh = 0; hh < kHalves; ++hh)
-            asm("mov.b64 %0, {%1, %1};" : "=l"(sc2[hh]) : "f"(sc[sub][hh]));
-          uint32_t o[4 * kWords];  // 8 values per word, two per 32-bit TMEM column
-#pragma unroll
-          for (int e = 0; e < kWords; ++e) {
-            // nibble * 4 (the byte offset of its codebook entry) in each byte
-            const uint32_t hi4 = (wd[e] >> 2) & 0x3C3C3C3Cu;  // earlier value of each byte
-            const uint32_t lo4 = (wd[e] << 2) & 0x3C3C3C3Cu;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const float a = *reinterpret_cast<const float*>(vcb + __byte_perm(hi4, 0, 0x4440 + j));
-              const float b = *reinterpret_cast<const float*>(vcb + __byte_perm(lo4, 0, 0x4440 + j));
-              float v0, v1;
-              mul2_rn(a, b, sc2[e / 4 < kHalves ? e / 4 : 0], v0, v1);
-              o[4 * e + j] = pack2<kOut>(v0, v1);
-            }
+          for (int j = 0; j < 4; ++j) {
+            const float a = *reinterpret_cast<const float*>(vcb + __byte_perm(hi4, 0, 0x4440 + j));
+            const float b = *reinterpret_cast<const float*>(vcb + __byte_perm(lo4, 0, 0x4440 + j));
+            float v0, v1;
+            mul2_rn(a, b, sc2[e / 4 < kHalves ? e / 4 : 0], v0, v1);
+            o[4 * e + j] = pack2<kOut>(v0, v1);
           }
-          // rows past N hold finite values (zero codes, zero-filled nibbles) and only
-          // feed accumulator lanes that are never stored
-          tmem_st<4 * kWords>(t_row + (apos.slot * kSub + sub) * 32, o);
         }
-        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(full_w(apos.slot));
-          mbar_arrive(raw_empty(rpos.slot));
-        }
+        // rows past N hold finite values (zero codes, zero-filled nibbles) and only feed
+        // accumulator lanes that are never stored
+        tmem_st<4 * kWords>(t_stage + sub * 32, o);
+      }
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(full_w(apos.slot));
+        mbar_arrive(raw_empty(rpos.slot));
+      }
 #pragma unroll
-        for (int g = 0; g < kGroups; ++g) {
-          apos.next();
-          rpos.next();
-        }
+      for (int g = 0; g < kGroups; ++g) {
+        apos.next();
+        rpos.next();
       }
     }
     if (failed && lane == 0) fail();
