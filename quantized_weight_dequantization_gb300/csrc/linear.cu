@@ -170,6 +170,14 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// The FP32 word at shared-memory byte address `addr` (a 32-bit shared address, so the
+// load is a shared-memory load whatever the compiler infers about the pointer).
+__device__ __forceinline__ float lds_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
+}
+
 // (a * s, b * s), each product rounded to nearest FP32 on its own (one packed
 // f32x2 multiply; no contraction, so the bits equal two __fmul_rn).
 __device__ __forceinline__ void mul2_rn(float a, float b, uint64_t s2, float& x, float& y) {
@@ -524,7 +532,7 @@ __global__ void __launch_bounds__(kLinThreads, 1)
       rpos.next();
     }
     bool failed = false;
-    const char* vcb = reinterpret_cast<const char*>(s_vcb);
+    const uint32_t vcb = smem_u32(s_vcb);  // codebook entries at vcb + 4 * nibble
     const int flip = (r >> 2) & 1;  // the raw boxes' 32-byte swizzle for this row
     for (int i = group; i < st_count; i += kGroups) {  // global weight stage i
       float sc[kSub][kHalves];
@@ -588,8 +596,8 @@ __global__ void __launch_bounds__(kLinThreads, 1)
           const uint32_t lo4 = (wd[e] << 2) & 0x3C3C3C3Cu;
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const float a = *reinterpret_cast<const float*>(vcb + __byte_perm(hi4, 0, 0x4440 + j));
-            const float b = *reinterpret_cast<const float*>(vcb + __byte_perm(lo4, 0, 0x4440 + j));
+            const float a = lds_f32(vcb + __byte_perm(hi4, 0, 0x4440 + j));
+            const float b = lds_f32(vcb + __byte_perm(lo4, 0, 0x4440 + j));
             float v0, v1;
             mul2_rn(a, b, sc2[e / 4 < kHalves ? e / 4 : 0], v0, v1);
             o[4 * e + j] = pack2<kOut>(v0, v1);
