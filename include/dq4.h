@@ -241,18 +241,36 @@ int dq4_nested_out_prod(const uint8_t* packed, const uint8_t* scale_codes,
  *   in_dtype   DQ4_OUT_F16 or DQ4_OUT_BF16 (X's type; W is decoded to it)
  *   K          a positive multiple of 64; M, N >= 0 (M, N, K <= INT32_MAX)
  *   X, packed  16-byte aligned (both are read by TMA)
+ *   workspace  optional device memory (NULL to skip), 256-byte aligned, of
+ *              workspace_bytes bytes, zero-filled before its first use.  When
+ *              there are fewer output tiles than SMs and workspace_bytes is at
+ *              least dq4_nested_linear_workspace_bytes(M, N, K), the SMs share
+ *              the tiles' K ranges: partial FP32 tiles meet in the workspace
+ *              and are summed in K order (deterministic).  A completed call
+ *              leaves its counters zero again, so it can be reused by later
+ *              calls of any shape in the same stream (not by concurrent calls).  Without it each tile
+ *              runs on one CTA; the result is the same up to FP32 summation
+ *              order.
  *   bad        optional device int (NULL to skip): incremented by each part
  *              of a CTA that stopped because a bounded wait ran out (never
- *              expected; nonzero means Y is incomplete)
- * DQ4_ERR_N for K not a multiple of 64; DQ4_ERR_ALIGN for a misaligned X or
- * packed.
+ *              expected; nonzero means Y is incomplete and the workspace must
+ *              be zero-filled again before its next use)
+ * DQ4_ERR_N for K not a multiple of 64; DQ4_ERR_ALIGN for a misaligned X,
+ * packed or workspace.
  */
 int dq4_nested_linear(const void* X, int32_t in_dtype, const uint8_t* packed,
                       const uint8_t* scale_codes, const float* nested_absmax,
                       const float* scale_codebook, const float* value_codebook, float offset,
                       int64_t M, int64_t N, int64_t K, int32_t blocksize,
-                      int32_t nested_blocksize, int32_t out_dtype, void* Y, int* bad,
-                      void* stream);
+                      int32_t nested_blocksize, int32_t out_dtype, void* Y, void* workspace,
+                      int64_t workspace_bytes, int* bad, void* stream);
+
+/*
+ * The workspace bytes dq4_nested_linear uses for an M x K by N x K problem on
+ * the current device (0 when it would not use one); -DQ4_ERR_DEVICE without a
+ * CC 10.3 device.  Shapes dq4_nested_linear rejects give 0.
+ */
+int64_t dq4_nested_linear_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 /* A static, human-readable string for a status code (never NULL). */
 const char* dq4_status_string(int status);

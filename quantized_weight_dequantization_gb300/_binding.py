@@ -66,8 +66,10 @@ def _load() -> ctypes.CDLL:
                                       p, p]
     L.dq4_nested_out_prod.restype = ctypes.c_int
     L.dq4_nested_linear.argtypes = [p, i32, p, p, p, p, p, f32, i64, i64, i64, i32, i32, i32, p,
-                                    p, p]
+                                    p, i64, p, p]
     L.dq4_nested_linear.restype = ctypes.c_int
+    L.dq4_nested_linear_workspace_bytes.argtypes = [i64, i64, i64]
+    L.dq4_nested_linear_workspace_bytes.restype = ctypes.c_int64
     L.dq4_status_string.argtypes = [ctypes.c_int]
     L.dq4_status_string.restype = ctypes.c_char_p
     L.dq4_last_cuda_error.argtypes = []
@@ -95,6 +97,23 @@ def __getattr__(name):
 # ------------------------------------------------------------- helpers
 def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
     return None if t is None else t.data_ptr()
+
+
+_WORKSPACES = {}
+
+
+def _linear_workspace(M: int, N: int, K: int, device, handle) -> torch.Tensor:
+    """The cached zero-filled workspace of (device, stream), grown to this problem's size."""
+    need = int(get_lib().dq4_nested_linear_workspace_bytes(M, N, K))
+    key = (device.index, handle)
+    ws = _WORKSPACES.get(key)
+    if need <= 0:
+        return ws if ws is not None else torch.empty(0, dtype=torch.uint8, device=device)
+    if ws is None or ws.numel() < need:
+        ws = torch.zeros(need, dtype=torch.uint8, device=device)
+        torch.cuda.synchronize(device)  # zero-filled before any stream uses it
+        _WORKSPACES[key] = ws
+    return ws
 
 
 def _check(t: torch.Tensor, name: str, dtype: torch.dtype, numel: int, device) -> None:
@@ -378,12 +397,16 @@ def linear(X: torch.Tensor, packed: torch.Tensor, scale_codes: torch.Tensor,
            value_codebook: torch.Tensor, offset: float, N: int, blocksize: int = 64,
            nested_blocksize: int = 256, out_dtype: Optional[torch.dtype] = None,
            Y: Optional[torch.Tensor] = None, bad: Optional[torch.Tensor] = None,
-           stream=None) -> torch.Tensor:
+           stream=None, workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
     """Y = X W^T with W (N x K) given as nested 4-bit codes, decoded inside a tcgen05 GEMM.
 
     X is M x K (bfloat16 or float16); W's values are those dq4_nested gives
     for X's dtype.  The dequantize-plus-linear path of issue #21 without the
     materialised weight.  K must be a multiple of 64.
+
+    ``workspace`` (uint8, zero-filled before first use) lets the SMs share the
+    tiles' K ranges when there are fewer tiles than SMs; by default a cached
+    buffer per (device, stream) is used, and an empty tensor disables it.
     """
     if X.dim() != 2:
         raise ValueError("X must be 2-D (M x K)")
@@ -408,11 +431,18 @@ def linear(X: torch.Tensor, packed: torch.Tensor, scale_codes: torch.Tensor,
     _check(Y, "Y", out_dtype, M * N, device)
     if bad is not None:
         _check(bad, "bad", torch.int32, 1, device)
+    handle = _stream_handle(stream, device)
+    if workspace is None:
+        workspace = _linear_workspace(M, N, K, device, handle)
+    elif workspace.numel() > 0:
+        if workspace.device != device or workspace.dtype != torch.uint8:
+            raise ValueError("workspace must be a uint8 tensor on X's device")
     st = get_lib().dq4_nested_linear(
         _ptr(X), _DTYPE_CODE[X.dtype], _ptr(packed), _ptr(scale_codes), _ptr(nested_absmax),
         _ptr(scale_codebook), _ptr(value_codebook), float(offset), M, N, K, blocksize,
-        nested_blocksize, _DTYPE_CODE[out_dtype], _ptr(Y), _ptr(bad),
-        _stream_handle(stream, device))
+        nested_blocksize, _DTYPE_CODE[out_dtype], _ptr(Y),
+        _ptr(workspace) if workspace.numel() > 0 else None, workspace.numel(), _ptr(bad),
+        handle)
     if st:
         raise Dq4Error(st, "dq4_nested_linear")
     return Y

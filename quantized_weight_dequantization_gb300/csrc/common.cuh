@@ -32,7 +32,7 @@ constexpr int kThreads = DQ4_THREADS;
 constexpr int kWarpsPerCta = kThreads / 32;
 constexpr int kMaxDevices = 64;
 constexpr int64_t kMaxGrid = 2147483647;  // gridDim.x limit
-constexpr int kAbiVersion = 1;
+constexpr int kAbiVersion = 2;
 
 
 // ------------------------------------------------------------------ args

@@ -170,6 +170,16 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Named barrier 1 over the 256 epilogue threads, AND-reducing a predicate.
+__device__ __forceinline__ bool bar_and_256(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.and.pred q, 1, 256, p;\n"
+      "selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r) : "r"(static_cast<uint32_t>(v)) : "memory");
+  return r != 0;
+}
+
 // The FP32 word at shared-memory byte address `addr` (a 32-bit shared address, so the
 // load is a shared-memory load whatever the compiler infers about the pointer).
 __device__ __forceinline__ float lds_f32(uint32_t addr) {
@@ -227,7 +237,26 @@ struct LinArgs {
   // bytes of scale codes one weight stage (64 kSub values of a row) spans, when those
   // codes form one aligned window with one absmax group (else 0: one load per K step)
   int code_window;
+  // The work is units = tiles x stages, tile-major (tile t = tile_w * tiles_x + tile_x).
+  // Without split, CTA c takes tile c whole.  With split, CTA c takes units
+  // c units / ctas .. (c + 1) units / ctas - 1, which span at most two tiles (there are
+  // fewer tiles than CTAs); a tile that several CTAs share is summed from their FP32
+  // partial tiles in ws_part by the last of them to arrive (ws_count), in K order.
+  int64_t units;
+  int ctas;
+  int split;
+  int max_parts;   // most CTAs sharing one tile
+  float* ws_part;  // [tiles][max_parts][BX][128] partial accumulators
+  int* ws_count;   // [tiles] arrivals, zero before and after a completed call
 };
+
+// First unit of CTA c, and the CTA that holds unit u, under the split work division.
+__host__ __device__ __forceinline__ int64_t split_begin(int64_t c, int64_t units, int ctas) {
+  return c * units / ctas;
+}
+__host__ __device__ __forceinline__ int64_t split_cta_of(int64_t u, int64_t units, int ctas) {
+  return ((u + 1) * ctas - 1) / units;
+}
 
 // The dequantized weights (the MMA's A operand) live in TMEM: columns 0 ..
 // 255 hold the FP32 accumulator (BX of them used), columns 256 .. 511 a ring
@@ -242,9 +271,11 @@ struct LinArgs {
 #endif
 constexpr int kSub = DQ4_LIN_SUB;         // 64-value K steps per weight stage
 constexpr uint32_t kTmemCols = 512;       // the whole TMEM of the SM
-// The accumulator takes columns 0 .. BX - 1; the weight ring the columns from
-// kATmem(BX) on, kAS(BX) stages of kSub K steps (32 columns each).
-__host__ __device__ constexpr uint32_t kATmem(int bx) { return bx <= 128 ? 128u : 256u; }
+// The accumulators take columns 0 .. 2 BX - 1 (two of them when a CTA's units span two
+// tiles; one, 0 .. 255, at BX = 256), the weight ring the columns from kATmem(BX) on:
+// kAS(BX) stages of kSub K steps (32 columns each).
+__host__ __device__ constexpr uint32_t kATmem(int bx) { return bx <= 64 ? 128u : 256u; }
+__host__ __device__ constexpr bool kCanSplit(int bx) { return bx <= 128; }
 __host__ __device__ constexpr int kASOf(int bx) {
   return int((kTmemCols - kATmem(bx)) / 32) / kSub;
 }
@@ -272,8 +303,8 @@ struct LinSmem {
   static constexpr int kRawOff = kXOff + kXS * kB;
   static constexpr int kBarOff = kRawOff + kRawS * kRawSlot;
   // full_w, empty_a per weight stage; full_x, empty_x per activation stage;
-  // raw_full, raw_empty per raw stage; acc_full
-  static constexpr int kBars = 2 * kAS + 2 * kXS + 2 * kRawS + 1;
+  // raw_full, raw_empty per raw stage; acc_full for two segments; acc_done
+  static constexpr int kBars = 2 * kAS + 2 * kXS + 2 * kRawS + 3;
   static constexpr int kBytes = kBarOff + 8 * kBars + 1024;  // + alignment slack
   static_assert(kBytes <= 227 * 1024, "shared memory budget");
   // more than half an SM's shared memory: one CTA per SM, so the 512-column TMEM
@@ -309,6 +340,7 @@ __global__ void __launch_bounds__(kLinThreads, 1)
   __shared__ float s_scb[256];
   __shared__ uint32_t s_tmem;          // TMEM base address from tcgen05.alloc
   __shared__ volatile int s_abort;     // set when any wait of the CTA ran out
+  __shared__ int s_last;               // this CTA completes a shared tile
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(base);
@@ -319,14 +351,45 @@ __global__ void __launch_bounds__(kLinThreads, 1)
   auto empty_x = [&](int s) { return bar0 + 8 * (2 * kAS + kXS + s); };
   auto raw_full = [&](int s) { return bar0 + 8 * (2 * kAS + 2 * kXS + s); };
   auto raw_empty = [&](int s) { return bar0 + 8 * (2 * kAS + 2 * kXS + kRawS + s); };
-  const uint32_t acc_full = bar0 + 8 * (2 * kAS + 2 * kXS + 2 * kRawS);
+  // acc_full(0), acc_full(1): a segment's accumulator is final; acc_done: every MMA done
+  auto acc_full = [&](int g) { return bar0 + 8 * (2 * kAS + 2 * kXS + 2 * kRawS + g); };
+  const uint32_t acc_done = acc_full(2);
   volatile int* abort_flag = &s_abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int tile_w = blockIdx.x / p.tiles_x, tile_x = blockIdx.x % p.tiles_x;
-  const int64_t n0 = int64_t(tile_w) * kBW, m0 = int64_t(tile_x) * BX;
   const int kt_count = int(p.K / kBK);                    // 64-value K steps
-  const int st_count = (kt_count + kSub - 1) / kSub;      // weight stages
+  const int st_count = (kt_count + kSub - 1) / kSub;      // weight stages per tile
+  // this CTA's units u0 .. u1 - 1 (tile-major), in at most two tiles: segment 0 in tile
+  // t0, segment 1 (if any) in tile t0 + 1 from its stage 0
+  int64_t u0, u1;
+  if (kCanSplit(BX) && p.split) {
+    u0 = split_begin(blockIdx.x, p.units, p.ctas);
+    u1 = split_begin(blockIdx.x + 1, p.units, p.ctas);
+  } else {
+    u0 = int64_t(blockIdx.x) * st_count;
+    u1 = u0 + st_count;
+  }
+  const int nl = int(u1 - u0);                            // local stages
+  const int64_t t0 = u0 / st_count;
+  const int nseg = (u1 - 1) / st_count != t0 ? 2 : 1;
+  const int l_split = nseg == 2 ? int((t0 + 1) * st_count - u0) : nl;  // segment 1's first
+  struct StageRef {
+    int64_t n0, m0;  // first weight row and activation row of the tile
+    int stage;       // stage within the tile
+    int seg;         // segment (accumulator) 0 or 1
+    bool first;      // first stage of its segment
+  };
+  auto stage_ref = [&](int l) {
+    StageRef r;
+    const int64_t u = u0 + l, t = u / st_count;
+    r.stage = int(u - t * st_count);
+    r.seg = l >= l_split ? 1 : 0;
+    r.first = l == 0 || l == l_split;
+    const int64_t tw = t / p.tiles_x;
+    r.n0 = tw * kBW;
+    r.m0 = (t - tw * p.tiles_x) * BX;
+    return r;
+  };
   auto fail = [&]() {
     *abort_flag = 1;
     if (p.bad) atomicAdd(p.bad, 1);
@@ -355,7 +418,7 @@ __global__ void __launch_bounds__(kLinThreads, 1)
         mbar_init(raw_full(s), 1);
         mbar_init(raw_empty(s), kGroupWarps);
       }
-      mbar_init(acc_full, 1);
+      for (int g = 0; g < 3; ++g) mbar_init(acc_full(g), 1);
       *abort_flag = 0;
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
       asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmap_x)));
@@ -369,66 +432,75 @@ __global__ void __launch_bounds__(kLinThreads, 1)
 
   if (warp == kRawWarp) {
     if (lane == 0) {
-      // ---- packed weight rows n0 .. n0 + 127: per stage kSub boxes of 128 rows x 32 bytes
-      // (64 values), each box unswizzled in its own 4 KB so the producers' reads of it
-      // stay conflict-free
+      // ---- packed weight rows of each local stage's tile: kSub boxes of 128 rows x 32
+      // bytes (64 values) per stage, 32-byte swizzled, each in its own 4 KB
       const uint64_t tw = reinterpret_cast<uint64_t>(&tmap_w);
       RingPos<kRawS> pos;
-      int i = 0;
-      for (; i < st_count; ++i, pos.next()) {
-        if (i >= kRawS) {
+      int l = 0;
+      for (; l < nl; ++l, pos.next()) {
+        if (l >= kRawS) {
           if (*abort_flag) break;
           if (!mbar_wait(raw_empty(pos.slot), pos.phase ^ 1u)) {
             fail();
             break;
           }
         }
-        const int ns = min(kSub, kt_count - i * kSub);
+        const StageRef sr = stage_ref(l);
+        const int ns = min(kSub, kt_count - sr.stage * kSub);
         mbar_expect(raw_full(pos.slot), ns * kRawBytes);
         for (int sub = 0; sub < ns; ++sub)
           tma_load_2d(sbase + S::kRawOff + pos.slot * S::kRawSlot + sub * kRawBytes, tw,
-                      (i * kSub + sub) * (kBK / 2), int(n0), raw_full(pos.slot));
+                      (sr.stage * kSub + sub) * (kBK / 2), int(sr.n0), raw_full(pos.slot));
       }
       if (*abort_flag)  // copies still in flight land before the CTA leaves
-        for (int j = i - 1; j >= 0 && j >= i - kRawS; --j)
+        for (int j = l - 1; j >= 0 && j >= l - kRawS; --j)
           mbar_wait(raw_full(j % kRawS), (j / kRawS) & 1);
     }
   } else if (warp == kXWarp) {
     if (lane == 0) {
-      // ---- activation rows m0 .. m0 + BX - 1, one 64-value K step per slot
+      // ---- activation rows of each local stage's tile, one 64-value K step per slot
       const uint64_t tx = reinterpret_cast<uint64_t>(&tmap_x);
       RingPos<kXS> pos;
-      int j = 0;
-      for (; j < kt_count; ++j, pos.next()) {
-        if (j >= kXS) {
-          if (*abort_flag) break;
-          if (!mbar_wait(empty_x(pos.slot), pos.phase ^ 1u)) {
-            fail();
-            break;
+      int q = 0;  // K steps requested
+      bool stop = false;
+      for (int l = 0; l < nl && !stop; ++l) {
+        const StageRef sr = stage_ref(l);
+        const int ns = min(kSub, kt_count - sr.stage * kSub);
+        for (int sub = 0; sub < ns; ++sub, ++q, pos.next()) {
+          if (q >= kXS) {
+            if (*abort_flag || !mbar_wait(empty_x(pos.slot), pos.phase ^ 1u)) {
+              if (!*abort_flag) fail();
+              stop = true;
+              break;
+            }
           }
+          mbar_expect(full_x(pos.slot), S::kB);
+          tma_load_2d(sbase + S::kXOff + pos.slot * S::kB, tx, (sr.stage * kSub + sub) * kBK,
+                      int(sr.m0), full_x(pos.slot));
         }
-        mbar_expect(full_x(pos.slot), S::kB);
-        tma_load_2d(sbase + S::kXOff + pos.slot * S::kB, tx, j * kBK, int(m0),
-                    full_x(pos.slot));
       }
       if (*abort_flag)
-        for (int q = j - 1; q >= 0 && q >= j - kXS; --q)
-          mbar_wait(full_x(q % kXS), (q / kXS) & 1);
+        for (int j = q - 1; j >= 0 && j >= q - kXS; --j)
+          mbar_wait(full_x(j % kXS), (j / kXS) & 1);
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
-      // ---- the MMA issue: K step j reads its weight columns of stage j / kSub and
-      // activation slot j % kXS; each slot is released when its MMAs complete
+      // ---- the MMA issue: local stage l reads its weight slot (l % kAS) and one
+      // activation slot per K step, accumulating into its segment's accumulator
+      // (columns seg * BX ..); each slot is released when its MMAs complete
       const uint32_t idesc = instr_desc<BX>(kBF16);
       RingPos<kAS> apos;
       RingPos<kXS> xpos;
       bool stop = false;
-      for (int i = 0; i < st_count && !stop; ++i, apos.next()) {
+      int committed = 0;  // segments whose accumulator was committed
+      for (int l = 0; l < nl && !stop; ++l, apos.next()) {
         if (*abort_flag || !mbar_wait(full_w(apos.slot), apos.phase)) {
           if (!*abort_flag) fail();
           break;
         }
-        const int ns = min(kSub, kt_count - i * kSub);
+        const StageRef sr = stage_ref(l);
+        const int ns = min(kSub, kt_count - sr.stage * kSub);
+        const uint32_t d_tmem = tmem + sr.seg * BX;
         for (int sub = 0; sub < ns; ++sub, xpos.next()) {
           if (!mbar_wait(full_x(xpos.slot), xpos.phase)) {
             fail();
@@ -442,11 +514,11 @@ __global__ void __launch_bounds__(kLinThreads, 1)
 #pragma unroll
           for (int ks = 0; ks < kBK / 16; ++ks) {
             const uint64_t db = smem_desc(b_addr + ks * 32);
-            const uint32_t acc = (i > 0 || sub > 0 || ks > 0) ? 1u : 0u;
+            const uint32_t acc = (sr.first && sub == 0 && ks == 0) ? 0u : 1u;
             asm volatile(
                 "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}"
-                :: "r"(tmem), "r"(a_tmem + ks * 8), "l"(db), "r"(idesc), "r"(acc));
+                :: "r"(d_tmem), "r"(a_tmem + ks * 8), "l"(db), "r"(idesc), "r"(acc));
           }
           asm volatile(
               "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
@@ -456,45 +528,62 @@ __global__ void __launch_bounds__(kLinThreads, 1)
         asm volatile(
             "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
             :: "r"(empty_a(apos.slot)) : "memory");
+        if (l == nl - 1 || l + 1 == l_split) {  // the segment's last stage
+          asm volatile(
+              "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+              :: "r"(acc_full(sr.seg)) : "memory");
+          ++committed;
+        }
       }
-      // tracks every MMA issued above, aborted or not
+      // after a failure, release the epilogue's waits (each barrier gets one arrival)
+      for (; committed < nseg; ++committed)
+        asm volatile(
+            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+            :: "r"(acc_full(committed)) : "memory");
+      // tracks every MMA issued above: no MMA still writes TMEM when it is freed below
       asm volatile(
           "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-          :: "r"(acc_full) : "memory");
-      mbar_wait(acc_full, 0);  // no MMA still writes TMEM when it is freed below
+          :: "r"(acc_done) : "memory");
+      mbar_wait(acc_done, 0);
     }
   } else {
-    // ---- dequantize.  Producer group `group` (kGroupWarps warps) takes weight stages
+    // ---- dequantize.  Producer group `group` (kGroupWarps warps) takes local stages
     // group, group + kGroups, ...; within it, warp w writes TMEM lanes 32 (w % 4) ..
-    // (weight row r = 32 (w % 4) + lane) and values 8 kWords h .. 8 kWords (h + 1) - 1
-    // of every 64-value K step, h = (w % kGroupWarps) / 4.  kHalves 32-value halves
-    // per K step each lie in one block (blocksize >= 32).
+    // (weight row r = 32 (w % 4) + lane of the stage's tile) and values 8 kWords h ..
+    // 8 kWords (h + 1) - 1 of every 64-value K step, h = (w % kGroupWarps) / 4.
+    // kHalves 32-value halves per K step each lie in one block (blocksize >= 32).
     const int gw = warp % kGroupWarps, group = warp / kGroupWarps;
     const int quad = gw & 3, h = gw >> 2;
     const int r = quad * 32 + lane;
-    const int64_t n = n0 + r;
-    const bool row_ok = n < p.N;
-    const int64_t idx0 = n * p.K + 8 * kWords * h;  // flat index of this thread's first value
     const float offset = p.w.offset;
     const uint32_t t_row = tmem + (static_cast<uint32_t>(quad * 32) << 16) + kATmemCol +
                            4 * kWords * h;  // this warp's lanes, its columns of a K step
-    auto fetch = [&](int i, uint32_t (&c)[kSub][kHalves], float (&a)[kSub][kHalves]) {
+    // the scale codes / absmax of local stage l for this thread's row
+    auto fetch = [&](int l, uint32_t (&c)[kSub][kHalves], float (&a)[kSub][kHalves]) {
+#pragma unroll
+      for (int sub = 0; sub < kSub; ++sub)
+#pragma unroll
+        for (int hh = 0; hh < kHalves; ++hh) {
+          c[sub][hh] = 0;
+          a[sub][hh] = 0.f;
+        }
+      if (l >= nl) return;
+      const StageRef sr = stage_ref(l);
+      const int64_t n = sr.n0 + r;
+      if (n >= p.N) return;
+      const int j0 = sr.stage * kSub;
       if (p.code_window != 0) {
         // the stage's codes of this row in one aligned load, its absmax in another
-        uint64_t win = 0;
-        float am = 0.f;
-        const int j0 = i * kSub;
-        if (row_ok && j0 < kt_count) {
-          const int64_t b00 = (n * p.K + int64_t(j0) * kBK) >> p.w.log2_bs;
-          const uint8_t* cp = p.w.codes + b00;
-          switch (p.code_window) {
-            case 8: win = __ldg(reinterpret_cast<const unsigned long long*>(cp)); break;
-            case 4: win = __ldg(reinterpret_cast<const unsigned int*>(cp)); break;
-            case 2: win = __ldg(reinterpret_cast<const unsigned short*>(cp)); break;
-            default: win = __ldg(cp); break;
-          }
-          am = __ldg(p.w.absmax + (b00 >> p.w.log2_nbs));
+        const int64_t b00 = (n * p.K + int64_t(j0) * kBK) >> p.w.log2_bs;
+        const uint8_t* cp = p.w.codes + b00;
+        uint64_t win;
+        switch (p.code_window) {
+          case 8: win = __ldg(reinterpret_cast<const unsigned long long*>(cp)); break;
+          case 4: win = __ldg(reinterpret_cast<const unsigned int*>(cp)); break;
+          case 2: win = __ldg(reinterpret_cast<const unsigned short*>(cp)); break;
+          default: win = __ldg(cp); break;
         }
+        const float am = __ldg(p.w.absmax + (b00 >> p.w.log2_nbs));
 #pragma unroll
         for (int sub = 0; sub < kSub; ++sub)
 #pragma unroll
@@ -505,14 +594,13 @@ __global__ void __launch_bounds__(kLinThreads, 1)
           }
         return;
       }
+      const int64_t idx0 = n * p.K + 8 * kWords * h;  // this thread's first value
 #pragma unroll
       for (int sub = 0; sub < kSub; ++sub)
 #pragma unroll
         for (int hh = 0; hh < kHalves; ++hh) {
-          c[sub][hh] = 0;
-          a[sub][hh] = 0.f;
-          const int j = i * kSub + sub;
-          if (row_ok && j < kt_count) {
+          const int j = j0 + sub;
+          if (j < kt_count) {
             const int64_t b = (idx0 + int64_t(j) * kBK + 32 * hh) >> p.w.log2_bs;
             c[sub][hh] = __ldg(p.w.codes + b);
             a[sub][hh] = __ldg(p.w.absmax + (b >> p.w.log2_nbs));
@@ -534,7 +622,7 @@ __global__ void __launch_bounds__(kLinThreads, 1)
     bool failed = false;
     const uint32_t vcb = smem_u32(s_vcb);  // codebook entries at vcb + 4 * nibble
     const int flip = (r >> 2) & 1;  // the raw boxes' 32-byte swizzle for this row
-    for (int i = group; i < st_count; i += kGroups) {  // global weight stage i
+    for (int l = group; l < nl; l += kGroups) {  // local stage l
       float sc[kSub][kHalves];
 #pragma unroll
       for (int sub = 0; sub < kSub; ++sub)
@@ -544,20 +632,20 @@ __global__ void __launch_bounds__(kLinThreads, 1)
           cA[sub][hh] = cB[sub][hh];
           aA[sub][hh] = aB[sub][hh];
         }
-      fetch(i + 2 * kGroups, cB, aB);
+      fetch(l + 2 * kGroups, cB, aB);
       // the raw stage has landed and the MMAs that read this weight slot last completed
       // (the first kAS stages have nothing to wait for: their empty phase reads as done)
       bool ok = !*abort_flag &&
                 (mbar_try2(raw_full(rpos.slot), rpos.phase, empty_a(apos.slot),
-                           i >= kAS ? apos.phase ^ 1u : 1u) ||
+                           l >= kAS ? apos.phase ^ 1u : 1u) ||
                  (mbar_wait(raw_full(rpos.slot), rpos.phase) &&
-                  (i < kAS || mbar_wait(empty_a(apos.slot), apos.phase ^ 1u))));
+                  (l < kAS || mbar_wait(empty_a(apos.slot), apos.phase ^ 1u))));
       if (!__all_sync(kFull, ok)) {  // warp-uniform, so the warp stays converged
         failed = true;
         break;
       }
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const int ns = min(kSub, kt_count - i * kSub);
+      const int ns = min(kSub, kt_count - stage_ref(l).stage * kSub);
       // rows are 32 bytes apart in each raw box, whose 32-byte swizzle stores the 16-byte
       // chunk c of row r at chunk c ^ ((r >> 2) & 1): the 8 rows a quarter warp reads then
       // fill all 32 banks
@@ -621,35 +709,92 @@ __global__ void __launch_bounds__(kLinThreads, 1)
       }
     }
     if (failed && lane == 0) fail();
-    // ---- epilogue on warps 0..7: warps w and w + 4 read TMEM lanes 32 (w % 4) ..
-    // (weight rows), each half of the BX accumulator columns (activation rows)
-    bool ok = warp < 8 && !failed && !*abort_flag && mbar_wait(acc_full, 0);
-    if (__all_sync(kFull, ok && !*abort_flag)) {
-      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const int quad = warp & 3;
-      const int64_t ny = n0 + quad * 32 + lane;  // this lane's column of Y
+    // ---- epilogue on warps 0..7 (named barrier 1, 256 threads): per segment, warps w
+    // and w + 4 read TMEM lanes 32 (w % 4) .. (weight rows), each half of the segment's BX
+    // accumulator columns (activation rows)
+    if (warp < 8) {
+      const int eq = warp & 3;
       constexpr int kHalf = BX / 2;
       const int c_begin = (warp >> 2) * kHalf;
-#pragma unroll 1
-      for (int c = c_begin; c < c_begin + kHalf; c += 8) {
-        if (m0 + c >= p.M) break;  // warp-uniform
-        uint32_t v[8];
-        tmem_ld8(tmem + (static_cast<uint32_t>(quad * 32) << 16) + c, v);
-        if (ny >= p.N) continue;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int64_t m = m0 + c + j;
-          if (m >= p.M) break;
-          const float f = __uint_as_float(v[j]);
-          const int64_t o = m * p.N + ny;  // a warp writes 32 consecutive columns of row m
-          if (p.out_dtype == DQ4_OUT_F32) {
-            static_cast<float*>(p.Y)[o] = f;
-          } else if (p.out_dtype == DQ4_OUT_BF16) {
-            static_cast<__nv_bfloat16*>(p.Y)[o] = __float2bfloat16_rn(f);
-          } else {
-            static_cast<__half*>(p.Y)[o] = __float2half_rn(f);
-          }
+      auto store_y = [&](int64_t m, int64_t ny, float f) {
+        const int64_t o = m * p.N + ny;  // a warp writes 32 consecutive columns of row m
+        if (p.out_dtype == DQ4_OUT_F32) {
+          static_cast<float*>(p.Y)[o] = f;
+        } else if (p.out_dtype == DQ4_OUT_BF16) {
+          static_cast<__nv_bfloat16*>(p.Y)[o] = __float2bfloat16_rn(f);
+        } else {
+          static_cast<__half*>(p.Y)[o] = __float2half_rn(f);
         }
+      };
+      for (int seg = 0; seg < nseg; ++seg) {
+        const int64_t t = t0 + seg;
+        const int64_t tw = t / p.tiles_x;
+        const int64_t m0 = (t - tw * p.tiles_x) * BX;
+        const int64_t ny = tw * kBW + eq * 32 + lane;  // this lane's column of Y
+        const int64_t s_lo = seg == 0 ? u0 : (t0 + 1) * st_count;
+        const int64_t s_hi = seg == nseg - 1 ? u1 : (t0 + 1) * st_count;
+        const bool whole = s_lo == t * st_count && s_hi == (t + 1) * st_count;
+        const bool ok = bar_and_256(!failed && !*abort_flag && mbar_wait(acc_full(seg), 0) &&
+                                    !*abort_flag);
+        if (!ok) break;  // the same decision in all 256 threads
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t t_acc = tmem + (static_cast<uint32_t>(eq * 32) << 16) + seg * BX;
+        if (whole) {
+#pragma unroll 1
+          for (int c = c_begin; c < c_begin + kHalf; c += 8) {
+            if (m0 + c >= p.M) break;  // warp-uniform
+            uint32_t v[8];
+            tmem_ld8(t_acc + c, v);
+            if (ny >= p.N) continue;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              if (m0 + c + j >= p.M) break;
+              store_y(m0 + c + j, ny, __uint_as_float(v[j]));
+            }
+          }
+          continue;
+        }
+        // a shared tile: this CTA's FP32 partial into its slot (part = its rank among
+        // the tile's CTAs, which is their K order), then the last to arrive sums them
+        const int64_t c_first = split_cta_of(t * st_count, p.units, p.ctas);
+        const int part = int(blockIdx.x - c_first);
+        const int nparts =
+            int(split_cta_of((t + 1) * st_count - 1, p.units, p.ctas) - c_first + 1);
+        float* tile_ws = p.ws_part + t * p.max_parts * BX * kBW;  // [part][column][row]
+#pragma unroll 1
+        for (int c = c_begin; c < c_begin + kHalf; c += 8) {
+          uint32_t v[8];
+          tmem_ld8(t_acc + c, v);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            tile_ws[(part * BX + c + j) * kBW + eq * 32 + lane] = __uint_as_float(v[j]);
+        }
+        __threadfence();
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        if (tid == 0) s_last = atomicAdd(p.ws_count + t, 1) == nparts - 1;
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        if (!s_last) continue;
+        __threadfence();
+        // all of this thread's sums first (every load independent of every other), then
+        // the stores: parts are added in K order, part 0 first
+        const float* col0 = tile_ws + eq * 32 + lane;
+        float acc[kHalf];
+#pragma unroll
+        for (int c = 0; c < kHalf; ++c) acc[c] = __ldcg(col0 + (c_begin + c) * kBW);
+        for (int q = 1; q < nparts; ++q) {
+          const float* colq = col0 + q * BX * kBW;
+          float x[kHalf];
+#pragma unroll
+          for (int c = 0; c < kHalf; ++c) x[c] = __ldcg(colq + (c_begin + c) * kBW);
+#pragma unroll
+          for (int c = 0; c < kHalf; ++c) acc[c] = __fadd_rn(acc[c], x[c]);
+        }
+        if (ny < p.N) {
+#pragma unroll
+          for (int c = 0; c < kHalf; ++c)
+            if (m0 + c_begin + c < p.M) store_y(m0 + c_begin + c, ny, acc[c]);
+        }
+        if (tid == 0) p.ws_count[t] = 0;  // ready for the next call
       }
     }
   }
@@ -737,6 +882,44 @@ int pick_bx(int64_t M, int64_t N, int sms) {
   return best;
 }
 
+// How a problem runs: tile widths, whether CTAs split tiles, and the workspace that needs.
+struct LinPlan {
+  int bx = 16;
+  int64_t tiles_x = 0, tiles = 0;
+  int st_count = 0;
+  bool split = false;
+  int ctas = 0;
+  int max_parts = 1;
+  int64_t count_bytes = 0, ws_bytes = 0;
+};
+
+LinPlan plan_linear(int64_t M, int64_t N, int64_t K, int sms) {
+  LinPlan pl;
+  pl.bx = pick_bx(M, N, sms);
+  pl.tiles_x = (M + pl.bx - 1) / pl.bx;
+  pl.tiles = pl.tiles_x * ((N + kBW - 1) / kBW);
+  pl.st_count = int((K / kBK + kSub - 1) / kSub);
+  const int64_t units = pl.tiles * pl.st_count;
+  // fewer tiles than SMs: one CTA per SM, each an equal share of the units
+  if (kCanSplit(pl.bx) && pl.tiles < sms && units >= sms) {
+    pl.split = true;
+    pl.ctas = sms;
+    for (int64_t t = 0; t < pl.tiles; ++t) {
+      const int64_t parts = split_cta_of((t + 1) * pl.st_count - 1, units, sms) -
+                            split_cta_of(t * pl.st_count, units, sms) + 1;
+      if (parts > pl.max_parts) pl.max_parts = int(parts);
+    }
+    // the counters come first and sit at the same offsets for every problem on this
+    // device (one per SM bounds the tiles of a split problem), so a workspace reused
+    // across problems never reads another problem's partial tiles as counters
+    pl.count_bytes = (int64_t(sms) * 4 + 255) / 256 * 256;
+    pl.ws_bytes = pl.count_bytes + pl.tiles * pl.max_parts * pl.bx * kBW * 4;
+  } else {
+    pl.ctas = int(pl.tiles);
+  }
+  return pl;
+}
+
 template <bool kBF16>
 int launch_bx(int bx, const CUtensorMap& tx, const CUtensorMap& tw, const LinArgs& p,
               int64_t grid, cudaStream_t st, int dev) {
@@ -760,8 +943,8 @@ int dq4_nested_linear(const void* X, int32_t in_dtype, const uint8_t* packed,
                       const uint8_t* scale_codes, const float* nested_absmax,
                       const float* scale_codebook, const float* value_codebook, float offset,
                       int64_t M, int64_t N, int64_t K, int32_t blocksize,
-                      int32_t nested_blocksize, int32_t out_dtype, void* Y, int* bad,
-                      void* stream) {
+                      int32_t nested_blocksize, int32_t out_dtype, void* Y, void* workspace,
+                      int64_t workspace_bytes, int* bad, void* stream) {
   if (M < 0 || N < 0 || K < 0) return DQ4_ERR_N;
   if (in_dtype != DQ4_OUT_F16 && in_dtype != DQ4_OUT_BF16) return DQ4_ERR_DTYPE;
   if (N > 0 && K > INT64_MAX / N) return DQ4_ERR_N;
@@ -774,16 +957,21 @@ int dq4_nested_linear(const void* X, int32_t in_dtype, const uint8_t* packed,
     return DQ4_ERR_NULL;
   if (misaligned(X, 16) || misaligned(packed, 16) || misaligned(nested_absmax, 4) ||
       misaligned(scale_codebook, 4) || misaligned(value_codebook, 4) ||
-      misaligned(Y, out_itemsize(out_dtype)) || misaligned(bad, 4))
+      misaligned(Y, out_itemsize(out_dtype)) || misaligned(bad, 4) || misaligned(workspace, 256))
     return DQ4_ERR_ALIGN;
   int dev = 0, sms = 0;
   if (int st = current_device(&dev, &sms)) return st;
   EncodeTiled encode = tensor_map_encoder();
   if (!encode) return fail_cuda(DQ4_ERR_LAUNCH, cudaErrorNotSupported);
 
-  const int bx = pick_bx(M, N, sms);
-  const int64_t tiles_x = (M + bx - 1) / bx, tiles_w = (N + kBW - 1) / kBW;
-  if (tiles_x * tiles_w > INT32_MAX) return DQ4_ERR_N;
+  LinPlan pl = plan_linear(M, N, K, sms);
+  if (pl.tiles > INT32_MAX) return DQ4_ERR_N;
+  // without a large enough workspace, every CTA takes a whole tile
+  if (pl.split && (!workspace || workspace_bytes < pl.ws_bytes)) {
+    pl.split = false;
+    pl.ctas = int(pl.tiles);
+  }
+  const int bx = pl.bx;
   const cuuint32_t estride[2] = {1, 1};
   // X as a 2-D tensor (K fastest, M rows): 64 x bx boxes, 128-byte swizzle, rows past M
   // read as zero
@@ -817,7 +1005,14 @@ int dq4_nested_linear(const void* X, int32_t in_dtype, const uint8_t* packed,
   p.K = K;
   p.bad = bad;
   p.out_dtype = out_dtype;
-  p.tiles_x = static_cast<int>(tiles_x);
+  p.tiles_x = static_cast<int>(pl.tiles_x);
+  p.units = pl.tiles * pl.st_count;
+  p.ctas = pl.ctas;
+  p.split = pl.split ? 1 : 0;
+  p.max_parts = pl.max_parts;
+  p.ws_count = pl.split ? static_cast<int*>(workspace) : nullptr;
+  p.ws_part = pl.split ? reinterpret_cast<float*>(static_cast<char*>(workspace) + pl.count_bytes)
+                       : nullptr;
   {
     // a stage covers 64 kSub values of a row, starting at a multiple of that when K is
     // one; its codes are then blocks b00 .. b00 + window - 1 with b00 a multiple of the
@@ -831,9 +1026,19 @@ int dq4_nested_linear(const void* X, int32_t in_dtype, const uint8_t* packed,
                         : 0;
   }
   const auto st = static_cast<cudaStream_t>(stream);
-  const int64_t grid = tiles_x * tiles_w;
+  const int64_t grid = pl.ctas;
   return in_dtype == DQ4_OUT_BF16 ? launch_bx<true>(bx, tx, tw, p, grid, st, dev)
                                   : launch_bx<false>(bx, tx, tw, p, grid, st, dev);
+}
+
+int64_t dq4_nested_linear_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  if (M <= 0 || N <= 0 || K <= 0 || K % kBK != 0 || M > INT32_MAX || N > INT32_MAX ||
+      K > INT32_MAX)
+    return 0;
+  int dev = 0, sms = 0;
+  if (current_device(&dev, &sms) != DQ4_OK) return -DQ4_ERR_DEVICE;
+  const LinPlan pl = plan_linear(M, N, K, sms);
+  return pl.split ? pl.ws_bytes : 0;
 }
 
 }  // extern "C"

@@ -38,7 +38,7 @@ def test_header_declares_the_boundary():
                             "dq4_nested_unfused",
                             "dq4_nested_unfused_static", "dq4_status_string",
                             "dq4_int8_correction_prep", "dq4_nested_out_prod",
-                            "dq4_nested_linear",
+                            "dq4_nested_linear", "dq4_nested_linear_workspace_bytes",
                             "dq4_last_cuda_error"]), names
 
 
@@ -69,7 +69,7 @@ def test_status_strings(dq):
         s = dq.lib.dq4_status_string(code)
         assert s and s != b"unknown status", code
     assert dq.lib.dq4_status_string(1234) == b"unknown status"
-    assert dq.lib.dq4_abi_version() == 1
+    assert dq.lib.dq4_abi_version() == 2
 
 
 def test_host_validation_before_any_cuda_call(dq):
@@ -129,11 +129,16 @@ def test_host_validation_before_any_cuda_call(dq):
     assert O(nz, nz, nz, nz, nz, 0.0, 8, 8, 48, 256, nz, 4, nz, nz, 1 << 20, nz, None) == 3
     # fused dequant + GEMM: shapes, dtypes and alignment on the host
     Lr = L.dq4_nested_linear
-    assert Lr(nz, 1, nz, nz, nz, nz, nz, 0.0, 4, 8, 100, 64, 256, 1, nz, None, None) == 2
-    assert Lr(nz, 2, nz, nz, nz, nz, nz, 0.0, 4, 8, 64, 64, 256, 1, nz, None, None) == 5
-    assert Lr(nz, 1, nz, nz, nz, nz, nz, 0.0, 0, 8, 64, 64, 256, 1, nz, None, None) == 0
-    assert Lr(None, 1, nz, nz, nz, nz, nz, 0.0, 4, 8, 64, 64, 256, 1, nz, None, None) == 1
-    assert Lr(nz + 8, 1, nz, nz, nz, nz, nz, 0.0, 4, 8, 64, 64, 256, 1, nz, None, None) == 6
+    assert Lr(nz, 1, nz, nz, nz, nz, nz, 0.0, 4, 8, 100, 64, 256, 1, nz, None, 0, None, None) == 2
+    assert Lr(nz, 2, nz, nz, nz, nz, nz, 0.0, 4, 8, 64, 64, 256, 1, nz, None, 0, None, None) == 5
+    assert Lr(nz, 1, nz, nz, nz, nz, nz, 0.0, 0, 8, 64, 64, 256, 1, nz, None, 0, None, None) == 0
+    assert Lr(None, 1, nz, nz, nz, nz, nz, 0.0, 4, 8, 64, 64, 256, 1, nz, None, 0, None,
+              None) == 1
+    assert Lr(nz + 8, 1, nz, nz, nz, nz, nz, 0.0, 4, 8, 64, 64, 256, 1, nz, None, 0, None,
+              None) == 6
+    assert Lr(nz, 1, nz, nz, nz, nz, nz, 0.0, 4, 8, 64, 64, 256, 1, nz, nz + 16, 1 << 20, None,
+              None) == 6  # a workspace that is not 256-byte aligned
+    assert L.dq4_nested_linear_workspace_bytes(4, 8, 100) == 0  # K not a multiple of 64
     # allocation-free form: the static scratch limit is checked before anything else runs
     limit = _declared_constants()["DQ4_STATIC_SCRATCH_BLOCKS"]
     assert L.dq4_nested_unfused_static(nz, nz, nz, nz, nz, 0.0, 64 * limit + 1, 64, 256, 0, nz,

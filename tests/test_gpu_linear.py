@@ -146,3 +146,92 @@ def test_errors(dq):
     with pytest.raises(dq.Dq4Error, match="DQ4_ERR_ALIGN"):
         dq.linear(X, packed, t["scale_codes"], t["nested_absmax"], t["scale_codebook"],
                   t["value_codebook"], 0.0, 64, 64, 256)
+
+
+# Fewer output tiles than SMs: with a workspace the SMs share the tiles' K ranges and
+# partial FP32 tiles are summed in K order by the last CTA to finish each tile.
+# (units = tiles x 4-K-step stages must reach the SM count; K = 1216 ends in a partial stage)
+# BX = 16 for all but the last two (BX = 64 and 128 on a 152-SM GB300)
+SPLIT_SHAPES = [(16, 11008, 4096), (3, 2000, 4096), (100, 2000, 512), (128, 1024, 8192),
+                (16, 4860, 1216), (64, 9856, 1024), (128, 9856, 1024)]
+
+
+@pytest.mark.parametrize("M,N,K", SPLIT_SHAPES)
+def test_split_and_whole_tiles_are_exact(dq, M, N, K):
+    assert dq.lib.dq4_nested_linear_workspace_bytes(M, N, K) > 0  # the split path applies
+    p = gen.make_integer_problem(N, K, seed=M + N)
+    X = torch.from_numpy(gen.make_ternary_g(M, K, seed=K)).to(torch.bfloat16).to(DEV)
+    want = oracle.linear(p, x_bits(X), "bf16", N, K, threads=16)
+    t = {k: torch.from_numpy(np.ascontiguousarray(getattr(p, k))).to(DEV)
+         for k in ("packed", "scale_codes", "nested_absmax", "scale_codebook", "value_codebook")}
+    none = torch.empty(0, dtype=torch.uint8, device=DEV)
+    for ws in (None, none):  # cached workspace (split) / no workspace (whole tiles)
+        bad = torch.zeros(1, dtype=torch.int32, device=DEV)
+        got = dq.linear(X, t["packed"], t["scale_codes"], t["nested_absmax"], t["scale_codebook"],
+                        t["value_codebook"], 0.0, N, 64, 256, out_dtype=torch.float32, bad=bad,
+                        workspace=ws)
+        assert np.array_equal(got.double().cpu().numpy(), want), (M, N, K, ws is None)
+        assert int(bad.item()) == 0
+
+
+def test_split_workspace_is_left_zero_and_reusable(dq):
+    M, N, K = 16, 4096, 2048
+    need = int(dq.lib.dq4_nested_linear_workspace_bytes(M, N, K))
+    assert need > 0
+    ws = torch.zeros(need, dtype=torch.uint8, device=DEV)
+    p = gen.make_integer_problem(N, K, seed=77)
+    X = torch.from_numpy(gen.make_ternary_g(M, K, seed=78)).to(torch.bfloat16).to(DEV)
+    t = {k: torch.from_numpy(np.ascontiguousarray(getattr(p, k))).to(DEV)
+         for k in ("packed", "scale_codes", "nested_absmax", "scale_codebook", "value_codebook")}
+    want = oracle.linear(p, x_bits(X), "bf16", N, K, threads=16)
+    for _ in range(20):  # back to back on one stream, one workspace
+        got = dq.linear(X, t["packed"], t["scale_codes"], t["nested_absmax"], t["scale_codebook"],
+                        t["value_codebook"], 0.0, N, 64, 256, out_dtype=torch.float32,
+                        workspace=ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(got.double().cpu().numpy(), want)
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    counts = ws[:4 * sms].view(torch.int32)  # the counters: one per SM, first
+    assert int(counts.abs().sum().item()) == 0
+
+
+def test_split_realistic_matches_whole_tiles(dq):
+    """NF4 weights, normal activations: both paths within the FP32 bound, and the split
+    path is deterministic (its partial sums meet in a fixed order)."""
+    M, N, K = 16, 11008, 4096
+    p = gen.make_problem(N * K, 64, 256, "nf4", 1.0, 0.0371, seed=23)
+    X = torch.from_numpy(gen.make_normal_g(M, K, seed=24)).to(torch.bfloat16).to(DEV)
+    t = {k: torch.from_numpy(np.ascontiguousarray(getattr(p, k))).to(DEV)
+         for k in ("packed", "scale_codes", "nested_absmax", "scale_codebook", "value_codebook")}
+    args = (X, t["packed"], t["scale_codes"], t["nested_absmax"], t["scale_codebook"],
+            t["value_codebook"], float(p.offset), N, 64, 256)
+    split = [dq.linear(*args, out_dtype=torch.float32) for _ in range(3)]
+    whole = dq.linear(*args, out_dtype=torch.float32,
+                      workspace=torch.empty(0, dtype=torch.uint8, device=DEV))
+    torch.cuda.synchronize()
+    assert torch.equal(split[0], split[1]) and torch.equal(split[0], split[2])
+    xb = x_bits(X)
+    want = oracle.linear(p, xb, "bf16", N, K, threads=16)
+    w = oracle._bits16_to_f64(oracle.dq4_nested(p, "bf16", threads=16), "bf16").reshape(N, K)
+    x = oracle._bits16_to_f64(xb, "bf16")
+    tol = 16 * 2.0 ** -24 * K * np.sqrt((x * x) @ (w * w).T) + 1e-30
+    for got in (split[0], whole):
+        assert np.all(np.abs(got.double().cpu().numpy() - want) <= tol)
+
+
+def test_one_workspace_across_shapes(dq):
+    """A workspace first used by a problem with few tiles, then by ones with more."""
+    shapes = [(128, 256, 4096), (16, 11008, 1024), (100, 2000, 512), (3, 2000, 4096)]
+    need = max(int(dq.lib.dq4_nested_linear_workspace_bytes(*sh)) for sh in shapes)
+    ws = torch.zeros(need, dtype=torch.uint8, device=DEV)
+    for M, N, K in shapes + shapes[::-1]:
+        p = gen.make_integer_problem(N, K, seed=M * 7 + K)
+        X = torch.from_numpy(gen.make_ternary_g(M, K, seed=N)).to(torch.bfloat16).to(DEV)
+        t = {k: torch.from_numpy(np.ascontiguousarray(getattr(p, k))).to(DEV)
+             for k in ("packed", "scale_codes", "nested_absmax", "scale_codebook",
+                       "value_codebook")}
+        got = dq.linear(X, t["packed"], t["scale_codes"], t["nested_absmax"],
+                        t["scale_codebook"], t["value_codebook"], 0.0, N, 64, 256,
+                        out_dtype=torch.float32, workspace=ws)
+        want = oracle.linear(p, x_bits(X), "bf16", N, K, threads=16)
+        assert np.array_equal(got.double().cpu().numpy(), want), (M, N, K)
