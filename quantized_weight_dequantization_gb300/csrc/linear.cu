@@ -73,6 +73,10 @@ constexpr int kRawBytes = kBW * kBK / 2;  // one raw stage: 128 rows x 32 packed
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint32_t kWaitLimit = 1u << 24;
 constexpr uint32_t kSuspendNs = 1000;
+#ifndef DQ4_LIN_MMA_SUSPEND_NS
+#define DQ4_LIN_MMA_SUSPEND_NS 1000
+#endif
+constexpr uint32_t kMmaSuspendNs = DQ4_LIN_MMA_SUSPEND_NS;  // the MMA thread's polls
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -97,12 +101,13 @@ __device__ __forceinline__ uint32_t instr_desc(bool bf16) {
          (static_cast<uint32_t>(BX >> 3) << 17) | (static_cast<uint32_t>(kBW >> 4) << 24);
 }
 
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity,
+                                         uint32_t suspend_ns = kSuspendNs) {
   uint32_t done;
   asm volatile(
       "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
       "selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(done) : "r"(bar), "r"(parity), "r"(kSuspendNs) : "memory");
+      : "=r"(done) : "r"(bar), "r"(parity), "r"(suspend_ns) : "memory");
   return done != 0;
 }
 
@@ -127,11 +132,12 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  if (mbar_try(bar, parity)) return true;
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          uint32_t suspend_ns = kSuspendNs) {
+  if (mbar_try(bar, parity, suspend_ns)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t it = 0; it < kWaitLimit; ++it) {
-    if (mbar_try(bar, parity)) return true;
+    if (mbar_try(bar, parity, suspend_ns)) return true;
     if (global_ns() - t0 > kWaitNs) break;
   }
   return false;
@@ -271,11 +277,11 @@ __host__ __device__ __forceinline__ int64_t split_cta_of(int64_t u, int64_t unit
 #endif
 constexpr int kSub = DQ4_LIN_SUB;         // 64-value K steps per weight stage
 constexpr uint32_t kTmemCols = 512;       // the whole TMEM of the SM
-// The accumulators take columns 0 .. 2 BX - 1 (two of them when a CTA's units span two
-// tiles; one, 0 .. 255, at BX = 256), the weight ring the columns from kATmem(BX) on:
-// kAS(BX) stages of kSub K steps (32 columns each).
-__host__ __device__ constexpr uint32_t kATmem(int bx) { return bx <= 64 ? 128u : 256u; }
-__host__ __device__ constexpr bool kCanSplit(int bx) { return bx <= 128; }
+// The accumulators take columns 0 .. 2 BX - 1 (two of them when a CTA's units may span
+// two tiles, BX <= 64; one of BX columns otherwise), the weight ring the columns from
+// kATmem(BX) on: kAS(BX) stages of kSub K steps (32 columns each).
+__host__ __device__ constexpr uint32_t kATmem(int bx) { return bx <= 128 ? 128u : 256u; }
+__host__ __device__ constexpr bool kCanSplit(int bx) { return bx <= 64; }
 __host__ __device__ constexpr int kASOf(int bx) {
   return int((kTmemCols - kATmem(bx)) / 32) / kSub;
 }
@@ -361,8 +367,9 @@ __global__ void __launch_bounds__(kLinThreads, 1)
   const int st_count = (kt_count + kSub - 1) / kSub;      // weight stages per tile
   // this CTA's units u0 .. u1 - 1 (tile-major), in at most two tiles: segment 0 in tile
   // t0, segment 1 (if any) in tile t0 + 1 from its stage 0
+  constexpr bool kSplit = kCanSplit(BX);  // this width may share tiles between CTAs
   int64_t u0, u1;
-  if (kCanSplit(BX) && p.split) {
+  if (kSplit && p.split) {
     u0 = split_begin(blockIdx.x, p.units, p.ctas);
     u1 = split_begin(blockIdx.x + 1, p.units, p.ctas);
   } else {
@@ -370,24 +377,31 @@ __global__ void __launch_bounds__(kLinThreads, 1)
     u1 = u0 + st_count;
   }
   const int nl = int(u1 - u0);                            // local stages
-  const int64_t t0 = u0 / st_count;
-  const int nseg = (u1 - 1) / st_count != t0 ? 2 : 1;
+  const int64_t t0 = kSplit ? u0 / st_count : blockIdx.x;
+  const int nseg = kSplit && (u1 - 1) / st_count != t0 ? 2 : 1;
   const int l_split = nseg == 2 ? int((t0 + 1) * st_count - u0) : nl;  // segment 1's first
+  const int stage0 = kSplit ? int(u0 - t0 * st_count) : 0;  // segment 0's first stage
+  // first weight row and activation row of each segment's tile (t = tile_w tiles_x + x)
+  int64_t seg_n0[2], seg_m0[2];  // indexed by constants only (registers)
+#pragma unroll
+  for (int g = 0; g < 2; ++g) {
+    const int64_t t = t0 + g, tw = t / p.tiles_x;
+    seg_n0[g] = tw * kBW;
+    seg_m0[g] = (t - tw * p.tiles_x) * BX;
+  }
   struct StageRef {
     int64_t n0, m0;  // first weight row and activation row of the tile
     int stage;       // stage within the tile
     int seg;         // segment (accumulator) 0 or 1
     bool first;      // first stage of its segment
   };
-  auto stage_ref = [&](int l) {
+  auto stage_ref = [&](int l) {  // no division: a CTA's stages lie in at most two tiles
     StageRef r;
-    const int64_t u = u0 + l, t = u / st_count;
-    r.stage = int(u - t * st_count);
-    r.seg = l >= l_split ? 1 : 0;
+    r.seg = kSplit && l >= l_split ? 1 : 0;
+    r.stage = r.seg ? l - l_split : stage0 + l;
     r.first = l == 0 || l == l_split;
-    const int64_t tw = t / p.tiles_x;
-    r.n0 = tw * kBW;
-    r.m0 = (t - tw * p.tiles_x) * BX;
+    r.n0 = r.seg ? seg_n0[1] : seg_n0[0];
+    r.m0 = r.seg ? seg_m0[1] : seg_m0[0];
     return r;
   };
   auto fail = [&]() {
@@ -494,7 +508,7 @@ __global__ void __launch_bounds__(kLinThreads, 1)
       bool stop = false;
       int committed = 0;  // segments whose accumulator was committed
       for (int l = 0; l < nl && !stop; ++l, apos.next()) {
-        if (*abort_flag || !mbar_wait(full_w(apos.slot), apos.phase)) {
+        if (*abort_flag || !mbar_wait(full_w(apos.slot), apos.phase, kMmaSuspendNs)) {
           if (!*abort_flag) fail();
           break;
         }
@@ -502,7 +516,7 @@ __global__ void __launch_bounds__(kLinThreads, 1)
         const int ns = min(kSub, kt_count - sr.stage * kSub);
         const uint32_t d_tmem = tmem + sr.seg * BX;
         for (int sub = 0; sub < ns; ++sub, xpos.next()) {
-          if (!mbar_wait(full_x(xpos.slot), xpos.phase)) {
+          if (!mbar_wait(full_x(xpos.slot), xpos.phase, kMmaSuspendNs)) {
             fail();
             stop = true;
             break;
@@ -558,6 +572,10 @@ __global__ void __launch_bounds__(kLinThreads, 1)
     const float offset = p.w.offset;
     const uint32_t t_row = tmem + (static_cast<uint32_t>(quad * 32) << 16) + kATmemCol +
                            4 * kWords * h;  // this warp's lanes, its columns of a K step
+    // this thread's weight row in each segment's tile, and its first value's flat index
+    const int64_t row_n0 = seg_n0[0] + r, row_n1 = seg_n0[1] + r;
+    const int64_t row_idx0 = row_n0 * p.K + 8 * kWords * h;
+    const int64_t row_idx1 = row_n1 * p.K + 8 * kWords * h;
     // the scale codes / absmax of local stage l for this thread's row
     auto fetch = [&](int l, uint32_t (&c)[kSub][kHalves], float (&a)[kSub][kHalves]) {
 #pragma unroll
@@ -569,12 +587,12 @@ __global__ void __launch_bounds__(kLinThreads, 1)
         }
       if (l >= nl) return;
       const StageRef sr = stage_ref(l);
-      const int64_t n = sr.n0 + r;
-      if (n >= p.N) return;
+      if ((sr.seg ? row_n1 : row_n0) >= p.N) return;
       const int j0 = sr.stage * kSub;
+      const int64_t idx0 = sr.seg ? row_idx1 : row_idx0;  // this thread's first value
       if (p.code_window != 0) {
         // the stage's codes of this row in one aligned load, its absmax in another
-        const int64_t b00 = (n * p.K + int64_t(j0) * kBK) >> p.w.log2_bs;
+        const int64_t b00 = (idx0 - 8 * kWords * h + int64_t(j0) * kBK) >> p.w.log2_bs;
         const uint8_t* cp = p.w.codes + b00;
         uint64_t win;
         switch (p.code_window) {
@@ -594,7 +612,6 @@ __global__ void __launch_bounds__(kLinThreads, 1)
           }
         return;
       }
-      const int64_t idx0 = n * p.K + 8 * kWords * h;  // this thread's first value
 #pragma unroll
       for (int sub = 0; sub < kSub; ++sub)
 #pragma unroll
@@ -734,9 +751,12 @@ __global__ void __launch_bounds__(kLinThreads, 1)
         const int64_t s_lo = seg == 0 ? u0 : (t0 + 1) * st_count;
         const int64_t s_hi = seg == nseg - 1 ? u1 : (t0 + 1) * st_count;
         const bool whole = s_lo == t * st_count && s_hi == (t + 1) * st_count;
-        const bool ok = bar_and_256(!failed && !*abort_flag && mbar_wait(acc_full(seg), 0) &&
-                                    !*abort_flag);
-        if (!ok) break;  // the same decision in all 256 threads
+        const bool mine = !failed && !*abort_flag && mbar_wait(acc_full(seg), 0) &&
+                          !*abort_flag;
+        // the fixup's named barriers need all 256 threads to agree; whole tiles need only
+        // each warp to (its tcgen05.ld are warp-collective)
+        const bool ok = kSplit ? bar_and_256(mine) : __all_sync(kFull, mine);
+        if (!ok) break;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint32_t t_acc = tmem + (static_cast<uint32_t>(eq * 32) << 16) + seg * BX;
         if (whole) {
@@ -754,6 +774,7 @@ __global__ void __launch_bounds__(kLinThreads, 1)
           }
           continue;
         }
+        if constexpr (!kSplit) continue;
         // a shared tile: this CTA's FP32 partial into its slot (part = its rank among
         // the tile's CTAs, which is their K order), then the last to arrive sums them
         const int64_t c_first = split_cta_of(t * st_count, p.units, p.ctas);
@@ -769,12 +790,16 @@ __global__ void __launch_bounds__(kLinThreads, 1)
           for (int j = 0; j < 8; ++j)
             tile_ws[(part * BX + c + j) * kBW + eq * 32 + lane] = __uint_as_float(v[j]);
         }
-        __threadfence();
+        // the barrier orders every thread's partial before thread 0's fence (cumulative),
+        // whose release the counter carries; the last arriver's fence acquires the others'
         asm volatile("bar.sync 1, 256;" ::: "memory");
-        if (tid == 0) s_last = atomicAdd(p.ws_count + t, 1) == nparts - 1;
+        if (tid == 0) {
+          __threadfence();
+          s_last = atomicAdd(p.ws_count + t, 1) == nparts - 1;
+          __threadfence();
+        }
         asm volatile("bar.sync 1, 256;" ::: "memory");
         if (!s_last) continue;
-        __threadfence();
         // all of this thread's sums first (every load independent of every other), then
         // the stores: parts are added in K order, part 0 first
         const float* col0 = tile_ws + eq * 32 + lane;

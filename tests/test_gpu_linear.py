@@ -151,9 +151,9 @@ def test_errors(dq):
 # Fewer output tiles than SMs: with a workspace the SMs share the tiles' K ranges and
 # partial FP32 tiles are summed in K order by the last CTA to finish each tile.
 # (units = tiles x 4-K-step stages must reach the SM count; K = 1216 ends in a partial stage)
-# BX = 16 for all but the last two (BX = 64 and 128 on a 152-SM GB300)
+# BX = 16 for all but the last (BX = 64 on a 152-SM GB300; BX >= 128 never splits)
 SPLIT_SHAPES = [(16, 11008, 4096), (3, 2000, 4096), (100, 2000, 512), (128, 1024, 8192),
-                (16, 4860, 1216), (64, 9856, 1024), (128, 9856, 1024)]
+                (16, 4860, 1216), (64, 9856, 1024)]
 
 
 @pytest.mark.parametrize("M,N,K", SPLIT_SHAPES)
@@ -235,3 +235,7 @@ def test_one_workspace_across_shapes(dq):
                         out_dtype=torch.float32, workspace=ws)
         want = oracle.linear(p, x_bits(X), "bf16", N, K, threads=16)
         assert np.array_equal(got.double().cpu().numpy(), want), (M, N, K)
+
+
+def test_wide_tiles_never_split(dq):
+    assert dq.lib.dq4_nested_linear_workspace_bytes(128, 9856, 1024) == 0  # BX = 128
