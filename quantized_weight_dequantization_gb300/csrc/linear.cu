@@ -297,16 +297,20 @@ struct LinSmem {
   static_assert(kATmem(BX) + kAS * kSub * 32 <= kTmemCols, "weight ring fits TMEM");
   static constexpr int kRawSlot = kSub * kRawBytes;
   static constexpr int kB = BX * kBK * 2;           // one K step of activations
-  static constexpr int kXS = BX <= 32 ? 12 : BX == 64 ? 8 : BX == 128 ? 6 : 4;
+  // K steps per activation slot: a whole stage for narrow tiles (one wait and one
+  // release per stage for the MMA thread), one K step for wide ones
+  static constexpr int kXSub = BX <= 32 ? kSub : 1;
+  static constexpr int kXSlot = kXSub * kB;
+  static constexpr int kXS = BX <= 32 ? 3 : BX == 64 ? 8 : BX == 128 ? 6 : 4;  // slots
   // raw weight stages: what the activation ring leaves of a 220 KB budget, at most 16
-  static constexpr int kRawFit = (220 * 1024 - kXS * kB) / kRawSlot;
+  static constexpr int kRawFit = (220 * 1024 - kXS * kXSlot) / kRawSlot;
   // A group waits for the raw load of its stage i; the load into the same slot before it
   // (stage i - kRawS) must be known complete, which holds when that stage is the group's
   // own: kRawS a multiple of kGroups (TMA loads need not complete in issue order).
   static constexpr int kRawS = (kRawFit < 16 ? kRawFit : 16) / kGroups * kGroups;
   static_assert(kRawS >= 4, "raw ring too shallow");
   static constexpr int kXOff = 0;
-  static constexpr int kRawOff = kXOff + kXS * kB;
+  static constexpr int kRawOff = kXOff + kXS * kXSlot;
   static constexpr int kBarOff = kRawOff + kRawS * kRawSlot;
   // full_w, empty_a per weight stage; full_x, empty_x per activation stage;
   // raw_full, raw_empty per raw stage; acc_full for two segments; acc_done
@@ -472,15 +476,16 @@ __global__ void __launch_bounds__(kLinThreads, 1)
     }
   } else if (warp == kXWarp) {
     if (lane == 0) {
-      // ---- activation rows of each local stage's tile, one 64-value K step per slot
+      // ---- activation rows of each local stage's tile, kXSub 64-value K steps per slot
+      constexpr int kXSub = S::kXSub;
       const uint64_t tx = reinterpret_cast<uint64_t>(&tmap_x);
       RingPos<kXS> pos;
-      int q = 0;  // K steps requested
+      int q = 0;  // slots requested
       bool stop = false;
       for (int l = 0; l < nl && !stop; ++l) {
         const StageRef sr = stage_ref(l);
         const int ns = min(kSub, kt_count - sr.stage * kSub);
-        for (int sub = 0; sub < ns; ++sub, ++q, pos.next()) {
+        for (int sub = 0; sub < ns; sub += kXSub, ++q, pos.next()) {
           if (q >= kXS) {
             if (*abort_flag || !mbar_wait(empty_x(pos.slot), pos.phase ^ 1u)) {
               if (!*abort_flag) fail();
@@ -488,9 +493,11 @@ __global__ void __launch_bounds__(kLinThreads, 1)
               break;
             }
           }
-          mbar_expect(full_x(pos.slot), S::kB);
-          tma_load_2d(sbase + S::kXOff + pos.slot * S::kB, tx, (sr.stage * kSub + sub) * kBK,
-                      int(sr.m0), full_x(pos.slot));
+          const int cnt = min(kXSub, ns - sub);
+          mbar_expect(full_x(pos.slot), cnt * S::kB);
+          for (int i = 0; i < cnt; ++i)
+            tma_load_2d(sbase + S::kXOff + pos.slot * S::kXSlot + i * S::kB, tx,
+                        (sr.stage * kSub + sub + i) * kBK, int(sr.m0), full_x(pos.slot));
         }
       }
       if (*abort_flag)
@@ -499,24 +506,34 @@ __global__ void __launch_bounds__(kLinThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
-      // ---- the MMA issue: local stage l reads its weight slot (l % kAS) and one
-      // activation slot per K step, accumulating into its segment's accumulator
-      // (columns seg * BX ..); each slot is released when its MMAs complete
+      // ---- the MMA issue: local stage l reads its weight slot (l % kAS) and its
+      // activation slots (one per stage for narrow tiles, one per K step otherwise),
+      // accumulating into its segment's accumulator (columns seg * BX ..); each slot is
+      // released when its MMAs complete
       const uint32_t idesc = instr_desc<BX>(kBF16);
       RingPos<kAS> apos;
       RingPos<kXS> xpos;
       bool stop = false;
       int committed = 0;  // segments whose accumulator was committed
       for (int l = 0; l < nl && !stop; ++l, apos.next()) {
-        if (*abort_flag || !mbar_wait(full_w(apos.slot), apos.phase, kMmaSuspendNs)) {
+        // the weight stage and (with whole-stage activation slots) its activations, polled
+        // together first
+        const bool ready = !*abort_flag &&
+                           (S::kXSub == kSub
+                                ? mbar_try2(full_w(apos.slot), apos.phase, full_x(xpos.slot),
+                                            xpos.phase)
+                                : mbar_try(full_w(apos.slot), apos.phase));
+        if (!ready && (*abort_flag || !mbar_wait(full_w(apos.slot), apos.phase, kMmaSuspendNs))) {
           if (!*abort_flag) fail();
           break;
         }
         const StageRef sr = stage_ref(l);
         const int ns = min(kSub, kt_count - sr.stage * kSub);
         const uint32_t d_tmem = tmem + sr.seg * BX;
-        for (int sub = 0; sub < ns; ++sub, xpos.next()) {
-          if (!mbar_wait(full_x(xpos.slot), xpos.phase, kMmaSuspendNs)) {
+        for (int sub = 0; sub < ns; ++sub) {
+          const int xi = sub % S::kXSub;  // K step within the activation slot
+          if (xi == 0 && !(ready && sub == 0 && S::kXSub == kSub) &&
+              !mbar_wait(full_x(xpos.slot), xpos.phase, kMmaSuspendNs)) {
             fail();
             stop = true;
             break;
@@ -524,7 +541,7 @@ __global__ void __launch_bounds__(kLinThreads, 1)
           asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
           // weights (M side) from TMEM: 8 columns per 16-value K slice
           const uint32_t a_tmem = tmem + kATmemCol + (apos.slot * kSub + sub) * 32;
-          const uint32_t b_addr = sbase + S::kXOff + xpos.slot * S::kB;  // activations: N
+          const uint32_t b_addr = sbase + S::kXOff + xpos.slot * S::kXSlot + xi * S::kB;
 #pragma unroll
           for (int ks = 0; ks < kBK / 16; ++ks) {
             const uint64_t db = smem_desc(b_addr + ks * 32);
@@ -534,9 +551,12 @@ __global__ void __launch_bounds__(kLinThreads, 1)
                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}"
                 :: "r"(d_tmem), "r"(a_tmem + ks * 8), "l"(db), "r"(idesc), "r"(acc));
           }
-          asm volatile(
-              "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-              :: "r"(empty_x(xpos.slot)) : "memory");
+          if (xi == S::kXSub - 1 || sub == ns - 1) {  // the slot's last K step
+            asm volatile(
+                "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                :: "r"(empty_x(xpos.slot)) : "memory");
+            xpos.next();
+          }
         }
         if (stop) break;
         asm volatile(
