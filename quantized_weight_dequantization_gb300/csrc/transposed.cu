@@ -33,6 +33,22 @@ __device__ __forceinline__ uint32_t out_bits(float v) {
   }
 }
 
+// (a * sa, b * sb), each product rounded to nearest FP32 on its own (one packed f32x2
+// multiply; no contraction, so the bits equal two __fmul_rn).
+__device__ __forceinline__ void mul2_pair(float a, float b, uint64_t s2, float& x, float& y) {
+  uint64_t ab, r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(ab) : "f"(a), "f"(b));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(ab), "l"(s2));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(r));
+}
+
+// The FP32 word at shared-memory byte address `addr`.
+__device__ __forceinline__ float lds_f32_t(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
+}
+
 // Store the values of rows (r, r + 1) at column c of W into W^T.
 // `o` is the element index of (r, c) in W^T: c * rows + r.
 template <int OUT, bool kStoreVec>
@@ -137,16 +153,24 @@ __global__ void __launch_bounds__(kThreads, DQ4_T_MIN_CTAS)
     const uint4 s0 = *reinterpret_cast<const uint4*>(&s_pk[lr][16 * swz(lr, ch)]);
     const uint4 s1 = *reinterpret_cast<const uint4*>(&s_pk[lr + 1][16 * swz(lr + 1, ch)]);
     const float2 scp = *reinterpret_cast<const float2*>(&s_sc[ch][lr]);
-    const float sc0 = scp.x, sc1 = scp.y;
+    uint64_t sc2;  // (scale of row ra, scale of row ra + 1)
+    asm("mov.b64 %0, {%1, %2};" : "=l"(sc2) : "f"(scp.x), "f"(scp.y));
+    const uint32_t vcb = static_cast<uint32_t>(__cvta_generic_to_shared(s_vcb));
 #pragma unroll
     for (int k = 0; k < 4; ++k) {  // packed word k: 8 columns
       const uint32_t w0 = k == 0 ? s0.x : k == 1 ? s0.y : k == 2 ? s0.z : s0.w;
       const uint32_t w1 = k == 0 ? s1.x : k == 1 ? s1.y : k == 2 ? s1.z : s1.w;
+      // nibble * 4 (the byte offset of its codebook entry) in each byte: the high
+      // nibbles (values 0, 2, 4, 6 of the word) and the low ones (1, 3, 5, 7)
+      const uint32_t h0 = (w0 >> 2) & 0x3C3C3C3Cu, l0 = (w0 << 2) & 0x3C3C3C3Cu;
+      const uint32_t h1 = (w1 >> 2) & 0x3C3C3C3Cu, l1 = (w1 << 2) & 0x3C3C3C3Cu;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {  // value j of a word: byte j/2, high nibble first
-        const int sh = 8 * (j >> 1) + ((j & 1) ? 0 : 4);
-        const float v0 = __fmul_rn(s_vcb[(w0 >> sh) & 0xFu], sc0);
-        const float v1 = __fmul_rn(s_vcb[(w1 >> sh) & 0xFu], sc1);
+        const uint32_t sel = 0x4440u + (j >> 1);
+        const float a0 = lds_f32_t(vcb + __byte_perm((j & 1) ? l0 : h0, 0, sel));
+        const float a1 = lds_f32_t(vcb + __byte_perm((j & 1) ? l1 : h1, 0, sel));
+        float v0, v1;
+        mul2_pair(a0, a1, sc2, v0, v1);
         store_pair<OUT, kStoreVec>(a.out, o, v0, v1, has0, has1);
         o += rows;
       }
