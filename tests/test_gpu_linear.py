@@ -239,3 +239,42 @@ def test_one_workspace_across_shapes(dq):
 
 def test_wide_tiles_never_split(dq):
     assert dq.lib.dq4_nested_linear_workspace_bytes(128, 9856, 1024) == 0  # BX = 128
+
+
+@pytest.mark.parametrize("xin,out", [("f16", "f16"), ("f16", "f32"), ("bf16", "bf16")])
+def test_split_dtypes_exact(dq, xin, out):
+    """The split path with FP16 activations (the weight decoded to FP16) and 16-bit outputs."""
+    M, N, K = 16, 4860, 2048
+    assert dq.lib.dq4_nested_linear_workspace_bytes(M, N, K) > 0
+    p = gen.make_integer_problem(N, K, seed=31)
+    X = torch.from_numpy(gen.make_ternary_g(M, K, seed=32)).to(TDT[xin]).to(DEV)
+    want = oracle.linear(p, x_bits(X), xin, N, K, threads=16)
+    got = run(dq, p, X, N, K, out=TDT[out]).to(torch.float64).cpu().numpy()
+    assert np.array_equal(got, rounded(want, out))
+
+
+def test_graph_capture_and_replay(dq):
+    """dq.linear captured in a CUDA graph (split path, cached workspace) replays exactly."""
+    M, N, K = 16, 4096, 1024
+    p = gen.make_integer_problem(N, K, seed=41)
+    t = {k: torch.from_numpy(np.ascontiguousarray(getattr(p, k))).to(DEV)
+         for k in ("packed", "scale_codes", "nested_absmax", "scale_codebook", "value_codebook")}
+    X = torch.zeros((M, K), dtype=torch.bfloat16, device=DEV)
+    Y = torch.empty((M, N), dtype=torch.float32, device=DEV)
+    call = lambda: dq.linear(X, t["packed"], t["scale_codes"], t["nested_absmax"],
+                             t["scale_codebook"], t["value_codebook"], 0.0, N, 64, 256, Y=Y)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        call()  # the workspace for (device, stream) exists before capture
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            call()
+    for seed in (1, 2, 3):
+        G = gen.make_ternary_g(M, K, seed=seed)
+        X.copy_(torch.from_numpy(G).to(torch.bfloat16))
+        with torch.cuda.stream(s):
+            g.replay()
+        torch.cuda.synchronize()
+        want = oracle.linear(p, x_bits(X), "bf16", N, K, threads=16)
+        assert np.array_equal(Y.double().cpu().numpy(), want), seed
