@@ -32,7 +32,6 @@ constexpr int kThreads = DQ4_THREADS;
 constexpr int kWarpsPerCta = kThreads / 32;
 constexpr int kMaxDevices = 64;
 constexpr int64_t kMaxGrid = 2147483647;  // gridDim.x limit
-constexpr int kAbiVersion = 2;
 
 
 // ------------------------------------------------------------------ args

@@ -102,6 +102,8 @@ using namespace dq4d;
 
 extern "C" {
 
+// incremented on any change of a signature in dq4.h (2: dq4_nested_linear's workspace)
+constexpr int kAbiVersion = 2;
 int dq4_abi_version(void) { return kAbiVersion; }
 
 const char* dq4_status_string(int status) {
