@@ -272,6 +272,37 @@ int dq4_nested_linear(const void* X, int32_t in_dtype, const uint8_t* packed,
  */
 int64_t dq4_nested_linear_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
+/*
+ * The fused path (dq4_nested's values, bit for bit) from host arrays to a
+ * host array: the inputs go to the device, the output comes back, chunk by
+ * chunk, with the copies of one chunk overlapping the kernel and the copies
+ * of the others.  Source: "Fuse nested scale reconstruction into SM103 4-bit
+ * dequantization" (bitsandbytes issue #21), section "Proposed experiment".
+ *   packed .. value_codebook   HOST arrays laid out as for dq4_nested
+ *                              (page-locked, for the copies to overlap)
+ *   out                        HOST array of n elements of out_dtype
+ *   scratch                    DEVICE memory, 256-byte aligned, of
+ *                              scratch_bytes >= dq4_nested_host_scratch_bytes
+ *                              (a smaller scratch takes smaller chunks, down
+ *                              to one nested group; below that,
+ *                              DQ4_ERR_TOO_LARGE)
+ * The call is ordered in `stream`: it starts after the work already enqueued
+ * there and the work enqueued after it sees `out` complete.  The host arrays
+ * must stay valid until then.  Chunks start on nested-group boundaries, so a
+ * chunk's scale codes and absmax are its own.  Each copy is one
+ * cudaMemcpyAsync; two internal streams per device carry them.
+ */
+int dq4_nested_host(const uint8_t* packed, const uint8_t* scale_codes,
+                    const float* nested_absmax, const float* scale_codebook,
+                    const float* value_codebook, float offset, int64_t n, int32_t blocksize,
+                    int32_t nested_blocksize, int32_t out_dtype, void* out, void* scratch,
+                    int64_t scratch_bytes, void* stream);
+
+/* Device scratch bytes for dq4_nested_host's default chunk (at most 2^24
+ * values, whole nested groups); 0 for invalid arguments or n == 0. */
+int64_t dq4_nested_host_scratch_bytes(int64_t n, int32_t blocksize, int32_t nested_blocksize,
+                                      int32_t out_dtype);
+
 /* A static, human-readable string for a status code (never NULL). */
 const char* dq4_status_string(int status);
 

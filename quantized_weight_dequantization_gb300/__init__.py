@@ -13,6 +13,7 @@ from ._binding import (  # noqa: F401
     Dq4Error,
     dq4,
     dq4_nested,
+    dq4_nested_host,
     dq4_nested_transposed,
     dq4_nested_unfused,
     dq4_nested_unfused_static,
@@ -30,6 +31,6 @@ def __getattr__(name):
     raise AttributeError(name)
 
 
-__all__ = ["dq4_nested", "dq4_nested_transposed", "dq4", "dq4_nested_unfused", "dq4_nested_unfused_static", "Dq4Error",
-           "get_lib", "sizes", "int8_correction_prep", "out_prod", "linear",
-           "OUT_F16", "OUT_BF16", "OUT_F32"]
+__all__ = ["dq4_nested", "dq4_nested_host", "dq4_nested_transposed", "dq4",
+           "dq4_nested_unfused", "dq4_nested_unfused_static", "Dq4Error", "get_lib", "sizes",
+           "int8_correction_prep", "out_prod", "linear", "OUT_F16", "OUT_BF16", "OUT_F32"]

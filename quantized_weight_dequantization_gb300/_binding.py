@@ -70,6 +70,10 @@ def _load() -> ctypes.CDLL:
     L.dq4_nested_linear.restype = ctypes.c_int
     L.dq4_nested_linear_workspace_bytes.argtypes = [i64, i64, i64]
     L.dq4_nested_linear_workspace_bytes.restype = ctypes.c_int64
+    L.dq4_nested_host.argtypes = [p, p, p, p, p, f32, i64, i32, i32, i32, p, p, i64, p]
+    L.dq4_nested_host.restype = ctypes.c_int
+    L.dq4_nested_host_scratch_bytes.argtypes = [i64, i32, i32, i32]
+    L.dq4_nested_host_scratch_bytes.restype = ctypes.c_int64
     L.dq4_status_string.argtypes = [ctypes.c_int]
     L.dq4_status_string.restype = ctypes.c_char_p
     L.dq4_last_cuda_error.argtypes = []
@@ -181,6 +185,69 @@ def dq4_nested(packed: torch.Tensor, scale_codes: torch.Tensor, nested_absmax: t
     if st:
         raise Dq4Error(st, "dq4_nested")
     return res
+
+
+def _check_host(t: torch.Tensor, name: str, dtype: torch.dtype, numel: int) -> None:
+    if t.device.type != "cpu":
+        raise ValueError(f"{name}: must be a CPU tensor (this form copies host memory)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if t.numel() < numel:
+        raise ValueError(f"{name}: needs at least {numel} elements, has {t.numel()}")
+
+
+_SCRATCH = {}
+
+
+def dq4_nested_host(packed: torch.Tensor, scale_codes: torch.Tensor,
+                    nested_absmax: torch.Tensor, scale_codebook: torch.Tensor,
+                    value_codebook: torch.Tensor, offset: float, n: int, blocksize: int = 64,
+                    nested_blocksize: int = 256, out_dtype: torch.dtype = torch.float16,
+                    out: Optional[torch.Tensor] = None, device=None, stream=None,
+                    scratch: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """dq4_nested's values from host (CPU) tensors into a host tensor, pipelined.
+
+    Inputs and ``out`` are CPU tensors (page-locked for the copies to overlap;
+    ``out`` is allocated pinned if None).  The work runs chunk by chunk on
+    ``device``'s ``stream`` (default: the current ones); ``out`` is complete
+    once the stream reaches the point after this call.  ``scratch`` is device
+    memory; by default a cached buffer per (device, stream) is used.
+    """
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else \
+        torch.device(device)
+    npk, nb, ng = sizes(n, blocksize, nested_blocksize)
+    _check_host(packed, "packed", torch.uint8, npk)
+    _check_host(scale_codes, "scale_codes", torch.uint8, nb)
+    _check_host(nested_absmax, "nested_absmax", torch.float32, ng)
+    _check_host(scale_codebook, "scale_codebook", torch.float32, 256)
+    _check_host(value_codebook, "value_codebook", torch.float32, 16)
+    if out is not None:
+        out_dtype = out.dtype
+    if out_dtype not in _DTYPE_CODE:
+        raise TypeError(f"out_dtype: unsupported {out_dtype}")
+    if out is None:
+        out = torch.empty(n, dtype=out_dtype, pin_memory=True)
+    _check_host(out, "out", out_dtype, n)
+    handle = _stream_handle(stream, device)
+    if scratch is None:
+        need = int(get_lib().dq4_nested_host_scratch_bytes(n, blocksize, nested_blocksize,
+                                                          _DTYPE_CODE[out_dtype]))
+        key = (device.index, handle)
+        scratch = _SCRATCH.get(key)
+        if scratch is None or scratch.numel() < need:
+            scratch = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
+            _SCRATCH[key] = scratch
+    elif scratch.device != device or scratch.dtype != torch.uint8:
+        raise ValueError("scratch must be a uint8 tensor on the device")
+    st = get_lib().dq4_nested_host(_ptr(packed), _ptr(scale_codes), _ptr(nested_absmax),
+                                   _ptr(scale_codebook), _ptr(value_codebook), float(offset), n,
+                                   blocksize, nested_blocksize, _DTYPE_CODE[out_dtype],
+                                   _ptr(out), _ptr(scratch), scratch.numel(), handle)
+    if st:
+        raise Dq4Error(st, "dq4_nested_host")
+    return out
 
 
 def dq4_nested_transposed(packed: torch.Tensor, scale_codes: torch.Tensor,

@@ -39,6 +39,7 @@ def test_header_declares_the_boundary():
                             "dq4_nested_unfused_static", "dq4_status_string",
                             "dq4_int8_correction_prep", "dq4_nested_out_prod",
                             "dq4_nested_linear", "dq4_nested_linear_workspace_bytes",
+                            "dq4_nested_host", "dq4_nested_host_scratch_bytes",
                             "dq4_last_cuda_error"]), names
 
 
@@ -139,6 +140,16 @@ def test_host_validation_before_any_cuda_call(dq):
     assert Lr(nz, 1, nz, nz, nz, nz, nz, 0.0, 4, 8, 64, 64, 256, 1, nz, nz + 16, 1 << 20, None,
               None) == 6  # a workspace that is not 256-byte aligned
     assert L.dq4_nested_linear_workspace_bytes(4, 8, 100) == 0  # K not a multiple of 64
+    # host-to-host form: arguments and the scratch size on the host
+    H = L.dq4_nested_host
+    need = L.dq4_nested_host_scratch_bytes(1 << 20, 64, 256, 0)
+    assert need > 0 and L.dq4_nested_host_scratch_bytes(0, 64, 256, 0) == 0
+    assert L.dq4_nested_host_scratch_bytes(100, 48, 256, 0) == 0  # bad blocksize
+    assert H(nz, nz, nz, nz, nz, 0.0, -1, 64, 256, 0, nz, nz, need, None) == 2
+    assert H(nz, nz, nz, nz, nz, 0.0, 0, 64, 256, 0, nz, nz, need, None) == 0
+    assert H(nz, nz, nz, nz, nz, 0.0, 100, 64, 256, 0, nz, None, need, None) == 1
+    assert H(nz, nz, nz, nz, nz, 0.0, 100, 64, 256, 0, nz, nz + 16, need, None) == 6
+    assert H(nz, nz, nz, nz, nz, 0.0, 1 << 20, 64, 256, 0, nz, nz, 4096, None) == 10
     # allocation-free form: the static scratch limit is checked before anything else runs
     limit = _declared_constants()["DQ4_STATIC_SCRATCH_BLOCKS"]
     assert L.dq4_nested_unfused_static(nz, nz, nz, nz, nz, 0.0, 64 * limit + 1, 64, 256, 0, nz,
