@@ -11,12 +11,17 @@
 // and BX activation rows (TMEM columns, the MMA's N = 16 .. 256), so a decode
 // batch of a few tokens costs an N = 16 MMA instead of a 128-row activation
 // tile, and a large batch decodes each weight tile once per 256 activations.
+// With fewer output tiles than SMs (BX <= 64 and a caller workspace), one CTA
+// runs per SM on an equal share of the (tile, stage) units, at most two tiles;
+// a tile shared by several CTAs is summed from their FP32 partials, in K
+// order, by the last of them to finish (no CTA waits for another).
 // Eleven warps:
-//  * warp 9 (lane 0): streams the packed weight rows of the tile with TMA into
-//    a ring of raw stages (two 128-row x 64-value boxes, 4 KB each), as far
-//    ahead as the ring allows;
-//  * warp 10 (lane 0): streams the activation tiles (BX rows x 64 K, 128-byte
-//    swizzle, rows past M zero-filled) with TMA into their own ring;
+//  * warp 9 (lane 0): streams the packed weight rows of each stage's tile with
+//    TMA into a ring of raw stages (four 128-row x 64-value boxes, 4 KB each,
+//    32-byte swizzled), as far ahead as the ring allows;
+//  * warp 10 (lane 0): streams the activation tiles (BX rows x 64 K per K step,
+//    128-byte swizzle, rows past M zero-filled) into their own ring, a whole
+//    stage per slot for narrow tiles;
 //  * warps 0..7, two groups of four that take alternate weight stages (so one
 //    group's barrier polls overlap the other's arithmetic): warp w owns TMEM
 //    lanes 32 (w % 4) .. (the weight rows), a thread one row.  Per 64-value K
@@ -25,8 +30,8 @@
 //    one aligned load when the shape allows, held two own stages ahead in
 //    registers) and the 64 values (FP32 products, RN to BF16 / FP16), and
 //    writes them to the weight ring in TMEM with one tcgen05.st; afterwards
-//    warps 0..7 run the epilogue: tcgen05.ld of the accumulator, conversion,
-//    stores of Y;
+//    warps 0..7 run the epilogue: tcgen05.ld of each segment's accumulator,
+//    conversion, stores of Y (or of a partial tile, and the shared tiles' sums);
 //  * warp 8: allocates the TMEM; lane 0 issues tcgen05.mma (A = weights from
 //    TMEM, B = activations from shared memory, M = 128, N = BX, K = 16) for
 //    each K step and commits the weight and activation slots back to their
@@ -48,7 +53,7 @@ namespace {
 #define DQ4_LIN_PWARPS 8  // dequantizing warps per CTA: 8 or 16
 #endif
 #ifndef DQ4_LIN_GROUPS
-#define DQ4_LIN_GROUPS 2  // producer groups that take turns on weight stages: 1, 2 or 4
+#define DQ4_LIN_GROUPS 2  // producer groups taking turns on weight stages (<= the ring depth)
 #endif
 constexpr int kProducerWarps = DQ4_LIN_PWARPS;
 constexpr int kGroups = DQ4_LIN_GROUPS;
@@ -72,11 +77,7 @@ constexpr int kRawBytes = kBW * kBK / 2;  // one raw stage: 128 rows x 32 packed
 // issue slots the dequantizing warps need.
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint32_t kWaitLimit = 1u << 24;
-constexpr uint32_t kSuspendNs = 1000;
-#ifndef DQ4_LIN_MMA_SUSPEND_NS
-#define DQ4_LIN_MMA_SUSPEND_NS 1000
-#endif
-constexpr uint32_t kMmaSuspendNs = DQ4_LIN_MMA_SUSPEND_NS;  // the MMA thread's polls
+constexpr uint32_t kSuspendNs = 1000;  // (0 or 100 ns for the MMA thread measured alike)
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -523,7 +524,7 @@ __global__ void __launch_bounds__(kLinThreads, 1)
                                 ? mbar_try2(full_w(apos.slot), apos.phase, full_x(xpos.slot),
                                             xpos.phase)
                                 : mbar_try(full_w(apos.slot), apos.phase));
-        if (!ready && (*abort_flag || !mbar_wait(full_w(apos.slot), apos.phase, kMmaSuspendNs))) {
+        if (!ready && (*abort_flag || !mbar_wait(full_w(apos.slot), apos.phase))) {
           if (!*abort_flag) fail();
           break;
         }
@@ -533,7 +534,7 @@ __global__ void __launch_bounds__(kLinThreads, 1)
         for (int sub = 0; sub < ns; ++sub) {
           const int xi = sub % S::kXSub;  // K step within the activation slot
           if (xi == 0 && !(ready && sub == 0 && S::kXSub == kSub) &&
-              !mbar_wait(full_x(xpos.slot), xpos.phase, kMmaSuspendNs)) {
+              !mbar_wait(full_x(xpos.slot), xpos.phase)) {
             fail();
             stop = true;
             break;
