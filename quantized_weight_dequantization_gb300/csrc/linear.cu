@@ -11,10 +11,13 @@
 // and BX activation rows (TMEM columns, the MMA's N = 16 .. 256), so a decode
 // batch of a few tokens costs an N = 16 MMA instead of a 128-row activation
 // tile, and a large batch decodes each weight tile once per 256 activations.
-// With fewer output tiles than SMs (BX <= 64 and a caller workspace), one CTA
-// runs per SM on an equal share of the (tile, stage) units, at most two tiles;
-// a tile shared by several CTAs is summed from their FP32 partials, in K
-// order, by the last of them to finish (no CTA waits for another).
+// The work is the (tile, weight stage) units, tile-major; with a caller
+// workspace and tiles that would not fill the SMs in whole rounds, one CTA runs
+// per SM on an equal share of the units, a run that may cross tile boundaries.
+// Each tile piece (segment) accumulates on its own in TMEM; whole tiles are
+// stored at once, and a tile shared by several CTAs is summed from their FP32
+// partials, in K order, by the last of them to finish (no CTA waits for
+// another).
 // Eleven warps:
 //  * warp 9 (lane 0): streams the packed weight rows of each stage's tile with
 //    TMA into a ring of raw stages (four 128-row x 64-value boxes, 4 KB each,
@@ -167,14 +170,19 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, uint64_t tmap, int x, 
       :: "r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(bar) : "memory");
 }
 
-// 8 consecutive accumulator columns of this warp's 32 TMEM lanes.
+// 8 consecutive accumulator columns of this warp's 32 TMEM lanes.  The load carries no
+// memory clobber (it may be issued ahead of earlier stores); the wait names the loaded
+// registers, so no use of them precedes it.
 __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
         "=r"(r[7])
       : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7])
+               :: "memory");
 }
 
 // Named barrier 1 over the 256 epilogue threads, AND-reducing a predicate.
@@ -245,51 +253,52 @@ struct LinArgs {
   // codes form one aligned window with one absmax group (else 0: one load per K step)
   int code_window;
   // The work is units = tiles x stages, tile-major (tile t = tile_w * tiles_x + tile_x).
-  // Without split, CTA c takes tile c whole.  With split, CTA c takes units
-  // c units / ctas .. (c + 1) units / ctas - 1, which span at most two tiles (there are
-  // fewer tiles than CTAs); a tile that several CTAs share is summed from their FP32
-  // partial tiles in ws_part by the last of them to arrive (ws_count), in K order.
-  int64_t units;
+  // With whole != 0 there is one CTA per tile, CTA c taking tile c whole.  Otherwise
+  // CTA c takes units c units / ctas .. (c + 1) units / ctas - 1 (units < 2^32, ctas <
+  // 2^16), a run of stages that may cross tile boundaries: its first and last segments
+  // may be parts of tiles that other CTAs share; those go to ws_part as FP32 partial
+  // tiles, and the last CTA to arrive at such a tile (ws_count) sums its parts in K
+  // order.
+  int whole;
   int ctas;
-  int split;
-  int max_parts;   // most CTAs sharing one tile
-  float* ws_part;  // [tiles][max_parts][BX][128] partial accumulators
-  int* ws_count;   // [tiles] arrivals, zero before and after a completed call
+  uint32_t units;
+  uint32_t units_q, units_r;  // units / ctas, units % ctas
+  float* ws_part;  // [ctas][2][BX][128]: CTA c's partial first (0) and last (1) segments
+  int* ws_count;   // [ctas]: arrivals at the shared tile whose last part CTA c holds
 };
 
-// First unit of CTA c, and the CTA that holds unit u, under the split work division.
-__host__ __device__ __forceinline__ int64_t split_begin(int64_t c, int64_t units, int ctas) {
-  return c * units / ctas;
-}
-__host__ __device__ __forceinline__ int64_t split_cta_of(int64_t u, int64_t units, int ctas) {
-  return ((u + 1) * ctas - 1) / units;
+// First unit of CTA c under the split work division: c units / ctas, in 32-bit
+// arithmetic (c (units % ctas) < ctas^2 < 2^32).
+__host__ __device__ __forceinline__ uint32_t split_begin(uint32_t c, const LinArgs& p) {
+  return c * p.units_q + c * p.units_r / uint32_t(p.ctas);
 }
 
-// The dequantized weights (the MMA's A operand) live in TMEM: columns 0 ..
-// 255 hold the FP32 accumulator (BX of them used), columns 256 .. 511 a ring
-// of kAS weight stages of kSub 64-value K steps (32 columns each: 64 16-bit
-// values per lane = weight row).  Producers write them with tcgen05.st, so
-// shared memory only carries the activation ring (B operand, TMA) and the raw
-// packed weight ring (TMA), both as deep as the budget allows.  A weight stage
-// spans kSub K steps, so the per-stage barrier work of the producers is
-// shared by 32 * kSub values per thread.
+// The dequantized weights (the MMA's A operand) live in TMEM, after the FP32
+// accumulators: a ring of kAS weight stages of kSub 64-value K steps (32 columns each:
+// 64 16-bit values per lane = weight row).  Producers write them with tcgen05.st, so
+// shared memory only carries the activation ring (B operand, TMA) and the raw packed
+// weight ring (TMA), both as deep as the budget allows.  A weight stage spans kSub K
+// steps, so the per-stage barrier work of the producers is shared by 32 * kSub values
+// per thread.
 #ifndef DQ4_LIN_SUB
 #define DQ4_LIN_SUB 4
 #endif
 constexpr int kSub = DQ4_LIN_SUB;         // 64-value K steps per weight stage
 constexpr uint32_t kTmemCols = 512;       // the whole TMEM of the SM
-// The accumulators take columns 0 .. 2 BX - 1 (two of them when a CTA's units may span
-// two tiles, BX <= 64; one of BX columns otherwise), the weight ring the columns from
-// kATmem(BX) on: kAS(BX) stages of kSub K steps (32 columns each).
+// Accumulator buffers: two for narrow tiles (a segment accumulates while the previous
+// one is read out), one of BX columns otherwise.  They take columns 0 .. kATmem(BX) - 1,
+// the weight ring the rest: kAS(BX) stages.
+__host__ __device__ constexpr int kAccOf(int bx) { return bx <= 64 ? 2 : 1; }
 __host__ __device__ constexpr uint32_t kATmem(int bx) { return bx <= 128 ? 128u : 256u; }
-__host__ __device__ constexpr bool kCanSplit(int bx) { return bx <= 64; }
 __host__ __device__ constexpr int kASOf(int bx) {
   return int((kTmemCols - kATmem(bx)) / 32) / kSub;
 }
 template <int BX>
 struct LinSmem {
   static constexpr int kAS = kASOf(BX);              // weight stages in TMEM
+  static constexpr int kAcc = kAccOf(BX);            // accumulator buffers
   static_assert(kAS >= 2, "double-buffered weight ring");
+  static_assert(kAcc * BX <= int(kATmem(BX)), "accumulators fit before the weight ring");
   // mbarrier waits test a phase's parity, so a waiter must never be two phases ahead
   // of the barrier.  A group at stage i waits for the MMAs of stage i - kAS and knows,
   // from its previous wait, that those of stage i - kGroups - kAS completed (MMAs
@@ -314,8 +323,8 @@ struct LinSmem {
   static constexpr int kRawOff = kXOff + kXS * kXSlot;
   static constexpr int kBarOff = kRawOff + kRawS * kRawSlot;
   // full_w, empty_a per weight stage; full_x, empty_x per activation stage;
-  // raw_full, raw_empty per raw stage; acc_full for two segments; acc_done
-  static constexpr int kBars = 2 * kAS + 2 * kXS + 2 * kRawS + 3;
+  // raw_full, raw_empty per raw stage; acc_full, acc_empty per accumulator; acc_done
+  static constexpr int kBars = 2 * kAS + 2 * kXS + 2 * kRawS + 2 * kAcc + 1;
   static constexpr int kBytes = kBarOff + 8 * kBars + 1024;  // + alignment slack
   static_assert(kBytes <= 227 * 1024, "shared memory budget");
   // more than half an SM's shared memory: one CTA per SM, so the 512-column TMEM
@@ -342,7 +351,7 @@ __global__ void __launch_bounds__(kLinThreads, 1)
     dq4_linear_kernel(const __grid_constant__ CUtensorMap tmap_x,
                       const __grid_constant__ CUtensorMap tmap_w, const LinArgs p) {
   using S = LinSmem<BX>;
-  constexpr int kAS = S::kAS, kXS = S::kXS, kRawS = S::kRawS;
+  constexpr int kAS = S::kAS, kXS = S::kXS, kRawS = S::kRawS, kAcc = S::kAcc;
   constexpr uint32_t kATmemCol = kATmem(BX);
   constexpr int kOut = kBF16 ? DQ4_OUT_BF16 : DQ4_OUT_F16;
   constexpr unsigned kFull = 0xFFFFFFFFu;
@@ -362,52 +371,64 @@ __global__ void __launch_bounds__(kLinThreads, 1)
   auto empty_x = [&](int s) { return bar0 + 8 * (2 * kAS + kXS + s); };
   auto raw_full = [&](int s) { return bar0 + 8 * (2 * kAS + 2 * kXS + s); };
   auto raw_empty = [&](int s) { return bar0 + 8 * (2 * kAS + 2 * kXS + kRawS + s); };
-  // acc_full(0), acc_full(1): a segment's accumulator is final; acc_done: every MMA done
-  auto acc_full = [&](int g) { return bar0 + 8 * (2 * kAS + 2 * kXS + 2 * kRawS + g); };
-  const uint32_t acc_done = acc_full(2);
+  // acc_full(b): the segment in accumulator b is final; acc_empty(b): read out; acc_done:
+  // every MMA done
+  auto acc_full = [&](int b) { return bar0 + 8 * (2 * kAS + 2 * kXS + 2 * kRawS + b); };
+  auto acc_empty = [&](int b) { return acc_full(kAcc + b); };
+  const uint32_t acc_done = acc_full(2 * kAcc);
   volatile int* abort_flag = &s_abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int kt_count = int(p.K / kBK);                    // 64-value K steps
   const int st_count = (kt_count + kSub - 1) / kSub;      // weight stages per tile
-  // this CTA's units u0 .. u1 - 1 (tile-major), in at most two tiles: segment 0 in tile
-  // t0, segment 1 (if any) in tile t0 + 1 from its stage 0
-  constexpr bool kSplit = kCanSplit(BX);  // this width may share tiles between CTAs
-  int64_t u0, u1;
-  if (kSplit && p.split) {
-    u0 = split_begin(blockIdx.x, p.units, p.ctas);
-    u1 = split_begin(blockIdx.x + 1, p.units, p.ctas);
-  } else {
-    u0 = int64_t(blockIdx.x) * st_count;
+  // this CTA's units u0 .. u1 - 1 (tile-major), local stages l = 0 .. nl - 1: segment s
+  // is the part in tile t0 + s, from local stage seg_start(s) on (no 64-bit division)
+  int64_t u0, u1, t0;
+  int stage0, nseg;
+  if (p.whole) {
+    t0 = blockIdx.x;
+    u0 = t0 * st_count;
     u1 = u0 + st_count;
+    stage0 = 0;
+    nseg = 1;
+  } else {
+    const uint32_t a = split_begin(blockIdx.x, p), b = split_begin(blockIdx.x + 1, p);
+    const uint32_t ta = a / uint32_t(st_count);
+    u0 = a;
+    u1 = b;
+    t0 = ta;
+    stage0 = int(a - ta * uint32_t(st_count));
+    nseg = int((b - 1) / uint32_t(st_count) - ta) + 1;
   }
-  const int nl = int(u1 - u0);                            // local stages
-  const int64_t t0 = kSplit ? u0 / st_count : blockIdx.x;
-  const int nseg = kSplit && (u1 - 1) / st_count != t0 ? 2 : 1;
-  const int l_split = nseg == 2 ? int((t0 + 1) * st_count - u0) : nl;  // segment 1's first
-  const int stage0 = kSplit ? int(u0 - t0 * st_count) : 0;  // segment 0's first stage
-  // first weight row and activation row of each segment's tile (t = tile_w tiles_x + x)
-  int64_t seg_n0[2], seg_m0[2];  // indexed by constants only (registers)
-#pragma unroll
-  for (int g = 0; g < 2; ++g) {
-    const int64_t t = t0 + g, tw = t / p.tiles_x;
-    seg_n0[g] = tw * kBW;
-    seg_m0[g] = (t - tw * p.tiles_x) * BX;
-  }
-  struct StageRef {
-    int64_t n0, m0;  // first weight row and activation row of the tile
-    int stage;       // stage within the tile
-    int seg;         // segment (accumulator) 0 or 1
-    bool first;      // first stage of its segment
+  const int nl = int(u1 - u0);
+  auto seg_start = [&](int sg) { return sg == 0 ? 0 : sg * st_count - stage0; };
+  // where a local stage sits: its segment, its stage within the tile, and the tile's first
+  // weight row and activation row (advanced without division but at tile boundaries)
+  struct Cursor {
+    int seg, stage;
+    int64_t n0, m0;
   };
-  auto stage_ref = [&](int l) {  // no division: a CTA's stages lie in at most two tiles
-    StageRef r;
-    r.seg = kSplit && l >= l_split ? 1 : 0;
-    r.stage = r.seg ? l - l_split : stage0 + l;
-    r.first = l == 0 || l == l_split;
-    r.n0 = r.seg ? seg_n0[1] : seg_n0[0];
-    r.m0 = r.seg ? seg_m0[1] : seg_m0[0];
-    return r;
+  auto set_origin = [&](Cursor& c) {
+    const uint32_t t = uint32_t(t0 + c.seg), tw = t / uint32_t(p.tiles_x);
+    c.n0 = int64_t(tw) * kBW;
+    c.m0 = int64_t(t - tw * uint32_t(p.tiles_x)) * BX;
+  };
+  auto cursor_at = [&](int l) {
+    Cursor c;
+    c.seg = (stage0 + l) / st_count;
+    c.stage = stage0 + l - c.seg * st_count;
+    set_origin(c);
+    return c;
+  };
+  auto advance = [&](Cursor& c, int k) {
+    c.stage += k;
+    if (c.stage >= st_count) {
+      do {
+        c.stage -= st_count;
+        ++c.seg;
+      } while (c.stage >= st_count);
+      set_origin(c);
+    }
   };
   auto fail = [&]() {
     *abort_flag = 1;
@@ -437,7 +458,11 @@ __global__ void __launch_bounds__(kLinThreads, 1)
         mbar_init(raw_full(s), 1);
         mbar_init(raw_empty(s), kGroupWarps);
       }
-      for (int g = 0; g < 3; ++g) mbar_init(acc_full(g), 1);
+      for (int g = 0; g < kAcc; ++g) {
+        mbar_init(acc_full(g), 1);
+        mbar_init(acc_empty(g), 8);  // the 8 epilogue warps
+      }
+      mbar_init(acc_done, 1);
       *abort_flag = 0;
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
       asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmap_x)));
@@ -455,8 +480,9 @@ __global__ void __launch_bounds__(kLinThreads, 1)
       // bytes (64 values) per stage, 32-byte swizzled, each in its own 4 KB
       const uint64_t tw = reinterpret_cast<uint64_t>(&tmap_w);
       RingPos<kRawS> pos;
+      Cursor cs = cursor_at(0);
       int l = 0;
-      for (; l < nl; ++l, pos.next()) {
+      for (; l < nl; ++l, pos.next(), advance(cs, 1)) {
         if (l >= kRawS) {
           if (*abort_flag) break;
           if (!mbar_wait(raw_empty(pos.slot), pos.phase ^ 1u)) {
@@ -464,12 +490,11 @@ __global__ void __launch_bounds__(kLinThreads, 1)
             break;
           }
         }
-        const StageRef sr = stage_ref(l);
-        const int ns = min(kSub, kt_count - sr.stage * kSub);
+        const int ns = min(kSub, kt_count - cs.stage * kSub);
         mbar_expect(raw_full(pos.slot), ns * kRawBytes);
         for (int sub = 0; sub < ns; ++sub)
           tma_load_2d(sbase + S::kRawOff + pos.slot * S::kRawSlot + sub * kRawBytes, tw,
-                      (sr.stage * kSub + sub) * (kBK / 2), int(sr.n0), raw_full(pos.slot));
+                      (cs.stage * kSub + sub) * (kBK / 2), int(cs.n0), raw_full(pos.slot));
       }
       if (*abort_flag)  // copies still in flight land before the CTA leaves
         for (int j = l - 1; j >= 0 && j >= l - kRawS; --j)
@@ -483,9 +508,9 @@ __global__ void __launch_bounds__(kLinThreads, 1)
       RingPos<kXS> pos;
       int q = 0;  // slots requested
       bool stop = false;
-      for (int l = 0; l < nl && !stop; ++l) {
-        const StageRef sr = stage_ref(l);
-        const int ns = min(kSub, kt_count - sr.stage * kSub);
+      Cursor cs = cursor_at(0);
+      for (int l = 0; l < nl && !stop; ++l, advance(cs, 1)) {
+        const int ns = min(kSub, kt_count - cs.stage * kSub);
         for (int sub = 0; sub < ns; sub += kXSub, ++q, pos.next()) {
           if (q >= kXS) {
             if (*abort_flag || !mbar_wait(empty_x(pos.slot), pos.phase ^ 1u)) {
@@ -498,7 +523,7 @@ __global__ void __launch_bounds__(kLinThreads, 1)
           mbar_expect(full_x(pos.slot), cnt * S::kB);
           for (int i = 0; i < cnt; ++i)
             tma_load_2d(sbase + S::kXOff + pos.slot * S::kXSlot + i * S::kB, tx,
-                        (sr.stage * kSub + sub + i) * kBK, int(sr.m0), full_x(pos.slot));
+                        (cs.stage * kSub + sub + i) * kBK, int(cs.m0), full_x(pos.slot));
         }
       }
       if (*abort_flag)
@@ -509,14 +534,15 @@ __global__ void __launch_bounds__(kLinThreads, 1)
     if (lane == 0) {
       // ---- the MMA issue: local stage l reads its weight slot (l % kAS) and its
       // activation slots (one per stage for narrow tiles, one per K step otherwise),
-      // accumulating into its segment's accumulator (columns seg * BX ..); each slot is
-      // released when its MMAs complete
+      // accumulating into its segment's accumulator (columns buf * BX ..), which the
+      // segment kAcc back must have left; each slot is released when its MMAs complete
       const uint32_t idesc = instr_desc<BX>(kBF16);
       RingPos<kAS> apos;
       RingPos<kXS> xpos;
-      bool stop = false;
+      Cursor cs = cursor_at(0);
+      bool stop = false, first = true;  // first: the stage opens its segment
       int committed = 0;  // segments whose accumulator was committed
-      for (int l = 0; l < nl && !stop; ++l, apos.next()) {
+      for (int l = 0; l < nl && !stop; ++l, apos.next(), advance(cs, 1)) {
         // the weight stage and (with whole-stage activation slots) its activations, polled
         // together first
         const bool ready = !*abort_flag &&
@@ -528,9 +554,15 @@ __global__ void __launch_bounds__(kLinThreads, 1)
           if (!*abort_flag) fail();
           break;
         }
-        const StageRef sr = stage_ref(l);
-        const int ns = min(kSub, kt_count - sr.stage * kSub);
-        const uint32_t d_tmem = tmem + sr.seg * BX;
+        const int buf = kAcc == 1 ? 0 : (cs.seg & 1);
+        if (first && cs.seg >= kAcc &&
+            (*abort_flag ||
+             !mbar_wait(acc_empty(buf), uint32_t(cs.seg / kAcc - 1) & 1u))) {
+          if (!*abort_flag) fail();
+          break;
+        }
+        const int ns = min(kSub, kt_count - cs.stage * kSub);
+        const uint32_t d_tmem = tmem + buf * BX;
         for (int sub = 0; sub < ns; ++sub) {
           const int xi = sub % S::kXSub;  // K step within the activation slot
           if (xi == 0 && !(ready && sub == 0 && S::kXSub == kSub) &&
@@ -546,7 +578,7 @@ __global__ void __launch_bounds__(kLinThreads, 1)
 #pragma unroll
           for (int ks = 0; ks < kBK / 16; ++ks) {
             const uint64_t db = smem_desc(b_addr + ks * 32);
-            const uint32_t acc = (sr.first && sub == 0 && ks == 0) ? 0u : 1u;
+            const uint32_t acc = (first && sub == 0 && ks == 0) ? 0u : 1u;
             asm volatile(
                 "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}"
@@ -563,18 +595,19 @@ __global__ void __launch_bounds__(kLinThreads, 1)
         asm volatile(
             "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
             :: "r"(empty_a(apos.slot)) : "memory");
-        if (l == nl - 1 || l + 1 == l_split) {  // the segment's last stage
+        first = cs.stage == st_count - 1 || l == nl - 1;  // the segment's last stage
+        if (first) {
           asm volatile(
               "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-              :: "r"(acc_full(sr.seg)) : "memory");
+              :: "r"(acc_full(buf)) : "memory");
           ++committed;
         }
       }
-      // after a failure, release the epilogue's waits (each barrier gets one arrival)
-      for (; committed < nseg; ++committed)
+      // after a failure, release the epilogue's next wait on each accumulator
+      for (int k = 0; k < kAcc && committed < nseg; ++k, ++committed)
         asm volatile(
             "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-            :: "r"(acc_full(committed)) : "memory");
+            :: "r"(acc_full(kAcc == 1 ? 0 : (committed & 1))) : "memory");
       // tracks every MMA issued above: no MMA still writes TMEM when it is freed below
       asm volatile(
           "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
@@ -593,12 +626,10 @@ __global__ void __launch_bounds__(kLinThreads, 1)
     const float offset = p.w.offset;
     const uint32_t t_row = tmem + (static_cast<uint32_t>(quad * 32) << 16) + kATmemCol +
                            4 * kWords * h;  // this warp's lanes, its columns of a K step
-    // this thread's weight row in each segment's tile, and its first value's flat index
-    const int64_t row_n0 = seg_n0[0] + r, row_n1 = seg_n0[1] + r;
-    const int64_t row_idx0 = row_n0 * p.K + 8 * kWords * h;
-    const int64_t row_idx1 = row_n1 * p.K + 8 * kWords * h;
-    // the scale codes / absmax of local stage l for this thread's row
-    auto fetch = [&](int l, uint32_t (&c)[kSub][kHalves], float (&a)[kSub][kHalves]) {
+    // the scale codes / absmax of the stage at cursor cs (local stage l) for this
+    // thread's row
+    auto fetch = [&](int l, const Cursor& cs, uint32_t (&c)[kSub][kHalves],
+                     float (&a)[kSub][kHalves]) {
 #pragma unroll
       for (int sub = 0; sub < kSub; ++sub)
 #pragma unroll
@@ -606,11 +637,9 @@ __global__ void __launch_bounds__(kLinThreads, 1)
           c[sub][hh] = 0;
           a[sub][hh] = 0.f;
         }
-      if (l >= nl) return;
-      const StageRef sr = stage_ref(l);
-      if ((sr.seg ? row_n1 : row_n0) >= p.N) return;
-      const int j0 = sr.stage * kSub;
-      const int64_t idx0 = sr.seg ? row_idx1 : row_idx0;  // this thread's first value
+      if (l >= nl || cs.n0 + r >= p.N) return;
+      const int j0 = cs.stage * kSub;
+      const int64_t idx0 = (cs.n0 + r) * p.K + 8 * kWords * h;  // this thread's first value
       if (p.code_window != 0) {
         // the stage's codes of this row in one aligned load, its absmax in another
         const int64_t b00 = (idx0 - 8 * kWords * h + int64_t(j0) * kBK) >> p.w.log2_bs;
@@ -645,203 +674,253 @@ __global__ void __launch_bounds__(kLinThreads, 1)
           }
         }
     };
+    // ---- read-out of segment ds (warps 0..7; named barrier 1 over their 256 threads):
+    // warps w and w + 4 read TMEM lanes 32 (w % 4) .. (weight rows = columns of Y), each
+    // half of the BX accumulator columns (activation rows).  A whole tile goes to Y; a
+    // shared one to this CTA's partial slot, and the last CTA to arrive at the tile sums
+    // its parts into Y.
+    constexpr int kHalf = BX / 2;
+    constexpr int kChunk = kHalf < 32 ? kHalf : 32;  // columns per step of the parts' sum
+    const int eq = warp & 3, c_begin = ((warp >> 2) & 1) * kHalf;
+    auto store_y = [&](int64_t m, int64_t ny, float f) {
+      const int64_t o = m * p.N + ny;  // a warp writes 32 consecutive columns of row m
+      if (p.out_dtype == DQ4_OUT_F32) {
+        static_cast<float*>(p.Y)[o] = f;
+      } else if (p.out_dtype == DQ4_OUT_BF16) {
+        static_cast<__nv_bfloat16*>(p.Y)[o] = __float2bfloat16_rn(f);
+      } else {
+        static_cast<__half*>(p.Y)[o] = __float2half_rn(f);
+      }
+    };
+    bool failed = false;
+    auto drain = [&](int ds) {
+      if (warp >= 8) return;
+      const int buf = kAcc == 1 ? 0 : (ds & 1);
+      const bool mine = !failed && !*abort_flag &&
+                        mbar_wait(acc_full(buf), uint32_t(ds / kAcc) & 1u) && !*abort_flag;
+      if (!bar_and_256(mine)) {  // the same verdict in all 256 threads
+        failed = true;
+        return;
+      }
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const int64_t t = t0 + ds;
+      const uint32_t tw = uint32_t(t) / uint32_t(p.tiles_x);
+      const int64_t m0 = int64_t(uint32_t(t) - tw * uint32_t(p.tiles_x)) * BX + c_begin;
+      const int64_t ny = int64_t(tw) * kBW + eq * 32 + lane;  // this lane's column of Y
+      const bool whole =
+          (ds > 0 || stage0 == 0) && (ds < nseg - 1 || u1 == (t + 1) * st_count);
+      const uint32_t t_acc = tmem + (static_cast<uint32_t>(eq * 32) << 16) + buf * BX +
+                             c_begin;
+      // after its TMEM loads of the segment the warp hands the accumulator back
+      auto release = [&]() {
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acc_empty(buf));
+      };
+      if (whole) {
+#pragma unroll 1
+        for (int c = 0; c < kHalf; c += 8) {
+          if (m0 + c >= p.M) break;  // warp-uniform
+          uint32_t v[8];
+          tmem_ld8(t_acc + c, v);
+          if (ny >= p.N) continue;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (m0 + c + j >= p.M) break;
+            store_y(m0 + c + j, ny, __uint_as_float(v[j]));
+          }
+        }
+        release();
+        return;
+      }
+      // a shared tile: this CTA's FP32 partial into its slot (0 for its first segment, 1
+      // for its last), then the last of the tile's CTAs to arrive sums them
+      float* part = p.ws_part +
+                    ((int64_t(blockIdx.x) * 2 + (ds == 0 ? 0 : 1)) * BX + c_begin) * kBW +
+                    eq * 32 + lane;
+#pragma unroll 1
+      for (int c = 0; c < kHalf; c += 8) {
+        uint32_t v[8];
+        tmem_ld8(t_acc + c, v);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) part[(c + j) * kBW] = __uint_as_float(v[j]);
+      }
+      release();
+      // the tile's parts are those of CTAs c_first .. c_last, in K order (found by
+      // stepping from this CTA: a tile has few parts); c_last holds the tile's last part,
+      // which no other shared tile ends in
+      const uint32_t t_lo = uint32_t(t) * uint32_t(st_count), t_hi = t_lo + st_count;
+      uint32_t c_first = blockIdx.x, c_last = blockIdx.x;
+      while (split_begin(c_first, p) > t_lo) --c_first;
+      while (split_begin(c_last + 1, p) < t_hi) ++c_last;
+      // the barrier orders every thread's partial before thread 0's fence (cumulative),
+      // whose release the counter carries; the last arriver's fence acquires the others'
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      if (tid == 0) {
+        __threadfence();
+        s_last = atomicAdd(p.ws_count + c_last, 1) == int(c_last - c_first);
+        __threadfence();
+      }
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      if (!s_last) return;
+      // part q is CTA c_first + q's first segment (slot 0), except that the tile may be
+      // the last segment (slot 1) of CTA c_first, when that CTA began in an earlier tile
+      const int slot0 = split_begin(c_first, p) < t_lo ? 1 : 0;
+      const int nparts = int(c_last - c_first + 1);
+      auto part_of = [&](int q) {
+        return p.ws_part +
+               ((int64_t(c_first + q) * 2 + (q == 0 ? slot0 : 0)) * BX + c_begin) * kBW +
+               eq * 32 + lane;
+      };
+#pragma unroll 1
+      for (int c = 0; c < kHalf; c += kChunk) {
+        // all loads of a part before its sums (independent loads overlap), parts added in
+        // K order, part 0 first
+        float acc[kChunk];
+        const float* src0 = part_of(0) + c * kBW;
+#pragma unroll
+        for (int j = 0; j < kChunk; ++j) acc[j] = __ldcg(src0 + j * kBW);
+        for (int q = 1; q < nparts; ++q) {
+          const float* src = part_of(q) + c * kBW;
+          float x[kChunk];
+#pragma unroll
+          for (int j = 0; j < kChunk; ++j) x[j] = __ldcg(src + j * kBW);
+#pragma unroll
+          for (int j = 0; j < kChunk; ++j) acc[j] = __fadd_rn(acc[j], x[j]);
+        }
+        if (ny < p.N) {
+#pragma unroll
+          for (int j = 0; j < kChunk; ++j) {
+            if (m0 + c + j >= p.M) break;
+            store_y(m0 + c + j, ny, acc[j]);
+          }
+        }
+      }
+      if (tid == 0) p.ws_count[c_last] = 0;  // ready for the next call
+    };
+
     // the codes / absmax of this group's next two stages, rotated every stage (no
     // unrolling over stages: the loop body stays small enough for the instruction cache)
     uint32_t cA[kSub][kHalves], cB[kSub][kHalves];
     float aA[kSub][kHalves], aB[kSub][kHalves];
-    fetch(group, cA, aA);
-    fetch(group + kGroups, cB, aB);
+    Cursor cur = cursor_at(group);            // stage l
+    Cursor pf = cursor_at(group + kGroups);   // stage l + 2 kGroups, once advanced below
+    fetch(group, cur, cA, aA);
+    fetch(group + kGroups, pf, cB, aB);
+    advance(pf, kGroups);
     RingPos<kAS> apos;
     RingPos<kRawS> rpos;
     for (int g = 0; g < group; ++g) {  // this group's first stage
       apos.next();
       rpos.next();
     }
-    bool failed = false;
+    bool timed_out = false;
+    int next_drain = 0;  // the next segment to read out
     const uint32_t vcb = smem_u32(s_vcb);  // codebook entries at vcb + 4 * nibble
     const int flip = (r >> 2) & 1;  // the raw boxes' 32-byte swizzle for this row
-    for (int l = group; l < nl; l += kGroups) {  // local stage l
-      float sc[kSub][kHalves];
-#pragma unroll
-      for (int sub = 0; sub < kSub; ++sub)
-#pragma unroll
-        for (int hh = 0; hh < kHalves; ++hh) {  // two roundings, never an FMA
-          sc[sub][hh] = __fadd_rn(__fmul_rn(s_scb[cA[sub][hh]], aA[sub][hh]), offset);
-          cA[sub][hh] = cB[sub][hh];
-          aA[sub][hh] = aB[sub][hh];
-        }
-      fetch(l + 2 * kGroups, cB, aB);
-      // the raw stage has landed and the MMAs that read this weight slot last completed
-      // (the first kAS stages have nothing to wait for: their empty phase reads as done)
-      bool ok = !*abort_flag &&
-                (mbar_try2(raw_full(rpos.slot), rpos.phase, empty_a(apos.slot),
-                           l >= kAS ? apos.phase ^ 1u : 1u) ||
-                 (mbar_wait(raw_full(rpos.slot), rpos.phase) &&
-                  (l < kAS || mbar_wait(empty_a(apos.slot), apos.phase ^ 1u))));
-      if (!__all_sync(kFull, ok)) {  // warp-uniform, so the warp stays converged
-        failed = true;
-        break;
-      }
-      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const int ns = min(kSub, kt_count - stage_ref(l).stage * kSub);
-      // rows are 32 bytes apart in each raw box, whose 32-byte swizzle stores the 16-byte
-      // chunk c of row r at chunk c ^ ((r >> 2) & 1): the 8 rows a quarter warp reads then
-      // fill all 32 banks
-      const uint8_t* raw_row = base + S::kRawOff + rpos.slot * S::kRawSlot + r * 32;
-      const uint32_t t_stage = t_row + apos.slot * kSub * 32;
-#pragma unroll 1
-      for (int sub = 0; sub < ns; ++sub) {
-        // this K step's scales, picked by selects rather than a register-array index
-        uint64_t sc2[kHalves];
-#pragma unroll
-        for (int hh = 0; hh < kHalves; ++hh) {
-          float v = sc[0][hh];
-#pragma unroll
-          for (int k = 1; k < kSub; ++k) v = sub == k ? sc[k][hh] : v;
-          asm("mov.b64 %0, {%1, %1};" : "=l"(sc2[hh]) : "f"(v));
-        }
-        uint32_t wd[kWords];
-        const uint8_t* row = raw_row + sub * kRawBytes;
-#pragma unroll
-        for (int v = 0; v < (kWords + 3) / 4; ++v) {
-          const int chunk = (kWords * h) / 4 + v;  // logical 16-byte chunk of the row
-          const uint8_t* src = row + (((chunk ^ flip) & 1) << 4) + ((kWords * h) % 4) * 4;
-          if constexpr (kWords >= 4) {
-            const uint4 w4 = *reinterpret_cast<const uint4*>(src);
-            wd[4 * v] = w4.x, wd[4 * v + 1] = w4.y, wd[4 * v + 2] = w4.z, wd[4 * v + 3] = w4.w;
-          } else {
-            const uint2 w2 = *reinterpret_cast<const uint2*>(src);
-            wd[0] = w2.x, wd[1] = w2.y;
+    // Segment d is read out before the first stage whose weight slot waits for MMAs that
+    // need its accumulator back (kAS stages into segment d + 1; the MMA then has those
+    // kAS stages queued when it gets the accumulator), the rest after the last stage.
+    // The stage loop runs up to the next read-out, so the read-out code stays out of it.
+    int l = group;  // this group's next local stage
+    for (;;) {
+      const int lim = next_drain < nseg - 1 ? min(nl, seg_start(next_drain + 1) + kAS) : nl;
+      for (; l < lim; l += kGroups) {  // local stage l
+        float sc[kSub][kHalves];
+  #pragma unroll
+        for (int sub = 0; sub < kSub; ++sub)
+  #pragma unroll
+          for (int hh = 0; hh < kHalves; ++hh) {  // two roundings, never an FMA
+            sc[sub][hh] = __fadd_rn(__fmul_rn(s_scb[cA[sub][hh]], aA[sub][hh]), offset);
+            cA[sub][hh] = cB[sub][hh];
+            aA[sub][hh] = aB[sub][hh];
           }
+        fetch(l + 2 * kGroups, pf, cB, aB);
+        advance(pf, kGroups);
+        // the raw stage has landed and the MMAs that read this weight slot last completed
+        // (the first kAS stages have nothing to wait for: their empty phase reads as done)
+        bool ok = !*abort_flag &&
+                  (mbar_try2(raw_full(rpos.slot), rpos.phase, empty_a(apos.slot),
+                             l >= kAS ? apos.phase ^ 1u : 1u) ||
+                   (mbar_wait(raw_full(rpos.slot), rpos.phase) &&
+                    (l < kAS || mbar_wait(empty_a(apos.slot), apos.phase ^ 1u))));
+        if (!__all_sync(kFull, ok)) {  // warp-uniform, so the warp stays converged
+          timed_out = failed = true;
+          break;
         }
-        uint32_t o[4 * kWords];  // 8 values per word, two per 32-bit TMEM column
-#pragma unroll
-        for (int e = 0; e < kWords; ++e) {
-          // nibble * 4 (the byte offset of its codebook entry) in each byte
-          const uint32_t hi4 = (wd[e] >> 2) & 0x3C3C3C3Cu;  // earlier value of each byte
-          const uint32_t lo4 = (wd[e] << 2) & 0x3C3C3C3Cu;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float a = lds_f32(vcb + __byte_perm(hi4, 0, 0x4440 + j));
-            const float b = lds_f32(vcb + __byte_perm(lo4, 0, 0x4440 + j));
-            float v0, v1;
-            mul2_rn(a, b, sc2[e / 4 < kHalves ? e / 4 : 0], v0, v1);
-            o[4 * e + j] = pack2<kOut>(v0, v1);
-          }
-        }
-        // rows past N hold finite values (zero codes, zero-filled nibbles) and only feed
-        // accumulator lanes that are never stored
-        tmem_st<4 * kWords>(t_stage + sub * 32, o);
-      }
-      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(full_w(apos.slot));
-        mbar_arrive(raw_empty(rpos.slot));
-      }
-#pragma unroll
-      for (int g = 0; g < kGroups; ++g) {
-        apos.next();
-        rpos.next();
-      }
-    }
-    if (failed && lane == 0) fail();
-    // ---- epilogue on warps 0..7 (named barrier 1, 256 threads): per segment, warps w
-    // and w + 4 read TMEM lanes 32 (w % 4) .. (weight rows), each half of the segment's BX
-    // accumulator columns (activation rows)
-    if (warp < 8) {
-      const int eq = warp & 3;
-      constexpr int kHalf = BX / 2;
-      const int c_begin = (warp >> 2) * kHalf;
-      auto store_y = [&](int64_t m, int64_t ny, float f) {
-        const int64_t o = m * p.N + ny;  // a warp writes 32 consecutive columns of row m
-        if (p.out_dtype == DQ4_OUT_F32) {
-          static_cast<float*>(p.Y)[o] = f;
-        } else if (p.out_dtype == DQ4_OUT_BF16) {
-          static_cast<__nv_bfloat16*>(p.Y)[o] = __float2bfloat16_rn(f);
-        } else {
-          static_cast<__half*>(p.Y)[o] = __float2half_rn(f);
-        }
-      };
-      for (int seg = 0; seg < nseg; ++seg) {
-        const int64_t t = t0 + seg;
-        const int64_t tw = t / p.tiles_x;
-        const int64_t m0 = (t - tw * p.tiles_x) * BX;
-        const int64_t ny = tw * kBW + eq * 32 + lane;  // this lane's column of Y
-        const int64_t s_lo = seg == 0 ? u0 : (t0 + 1) * st_count;
-        const int64_t s_hi = seg == nseg - 1 ? u1 : (t0 + 1) * st_count;
-        const bool whole = s_lo == t * st_count && s_hi == (t + 1) * st_count;
-        const bool mine = !failed && !*abort_flag && mbar_wait(acc_full(seg), 0) &&
-                          !*abort_flag;
-        // the fixup's named barriers need all 256 threads to agree; whole tiles need only
-        // each warp to (its tcgen05.ld are warp-collective)
-        const bool ok = kSplit ? bar_and_256(mine) : __all_sync(kFull, mine);
-        if (!ok) break;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const uint32_t t_acc = tmem + (static_cast<uint32_t>(eq * 32) << 16) + seg * BX;
-        if (whole) {
-#pragma unroll 1
-          for (int c = c_begin; c < c_begin + kHalf; c += 8) {
-            if (m0 + c >= p.M) break;  // warp-uniform
-            uint32_t v[8];
-            tmem_ld8(t_acc + c, v);
-            if (ny >= p.N) continue;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              if (m0 + c + j >= p.M) break;
-              store_y(m0 + c + j, ny, __uint_as_float(v[j]));
+        const int ns = min(kSub, kt_count - cur.stage * kSub);
+        // rows are 32 bytes apart in each raw box, whose 32-byte swizzle stores the 16-byte
+        // chunk c of row r at chunk c ^ ((r >> 2) & 1): the 8 rows a quarter warp reads then
+        // fill all 32 banks
+        const uint8_t* raw_row = base + S::kRawOff + rpos.slot * S::kRawSlot + r * 32;
+        const uint32_t t_stage = t_row + apos.slot * kSub * 32;
+  #pragma unroll 1
+        for (int sub = 0; sub < ns; ++sub) {
+          // this K step's scales, picked by selects rather than a register-array index
+          uint64_t sc2[kHalves];
+  #pragma unroll
+          for (int hh = 0; hh < kHalves; ++hh) {
+            float v = sc[0][hh];
+  #pragma unroll
+            for (int k = 1; k < kSub; ++k) v = sub == k ? sc[k][hh] : v;
+            asm("mov.b64 %0, {%1, %1};" : "=l"(sc2[hh]) : "f"(v));
+          }
+          uint32_t wd[kWords];
+          const uint8_t* row = raw_row + sub * kRawBytes;
+  #pragma unroll
+          for (int v = 0; v < (kWords + 3) / 4; ++v) {
+            const int chunk = (kWords * h) / 4 + v;  // logical 16-byte chunk of the row
+            const uint8_t* src = row + (((chunk ^ flip) & 1) << 4) + ((kWords * h) % 4) * 4;
+            if constexpr (kWords >= 4) {
+              const uint4 w4 = *reinterpret_cast<const uint4*>(src);
+              wd[4 * v] = w4.x, wd[4 * v + 1] = w4.y, wd[4 * v + 2] = w4.z, wd[4 * v + 3] = w4.w;
+            } else {
+              const uint2 w2 = *reinterpret_cast<const uint2*>(src);
+              wd[0] = w2.x, wd[1] = w2.y;
             }
           }
-          continue;
+          uint32_t o[4 * kWords];  // 8 values per word, two per 32-bit TMEM column
+  #pragma unroll
+          for (int e = 0; e < kWords; ++e) {
+            // nibble * 4 (the byte offset of its codebook entry) in each byte
+            const uint32_t hi4 = (wd[e] >> 2) & 0x3C3C3C3Cu;  // earlier value of each byte
+            const uint32_t lo4 = (wd[e] << 2) & 0x3C3C3C3Cu;
+  #pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float a = lds_f32(vcb + __byte_perm(hi4, 0, 0x4440 + j));
+              const float b = lds_f32(vcb + __byte_perm(lo4, 0, 0x4440 + j));
+              float v0, v1;
+              mul2_rn(a, b, sc2[e / 4 < kHalves ? e / 4 : 0], v0, v1);
+              o[4 * e + j] = pack2<kOut>(v0, v1);
+            }
+          }
+          // rows past N hold finite values (zero codes, zero-filled nibbles) and only feed
+          // accumulator lanes that are never stored
+          tmem_st<4 * kWords>(t_stage + sub * 32, o);
         }
-        if constexpr (!kSplit) continue;
-        // a shared tile: this CTA's FP32 partial into its slot (part = its rank among
-        // the tile's CTAs, which is their K order), then the last to arrive sums them
-        const int64_t c_first = split_cta_of(t * st_count, p.units, p.ctas);
-        const int part = int(blockIdx.x - c_first);
-        const int nparts =
-            int(split_cta_of((t + 1) * st_count - 1, p.units, p.ctas) - c_first + 1);
-        float* tile_ws = p.ws_part + t * p.max_parts * BX * kBW;  // [part][column][row]
-#pragma unroll 1
-        for (int c = c_begin; c < c_begin + kHalf; c += 8) {
-          uint32_t v[8];
-          tmem_ld8(t_acc + c, v);
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            tile_ws[(part * BX + c + j) * kBW + eq * 32 + lane] = __uint_as_float(v[j]);
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(full_w(apos.slot));
+          mbar_arrive(raw_empty(rpos.slot));
         }
-        // the barrier orders every thread's partial before thread 0's fence (cumulative),
-        // whose release the counter carries; the last arriver's fence acquires the others'
-        asm volatile("bar.sync 1, 256;" ::: "memory");
-        if (tid == 0) {
-          __threadfence();
-          s_last = atomicAdd(p.ws_count + t, 1) == nparts - 1;
-          __threadfence();
+  #pragma unroll
+        for (int g = 0; g < kGroups; ++g) {
+          apos.next();
+          rpos.next();
         }
-        asm volatile("bar.sync 1, 256;" ::: "memory");
-        if (!s_last) continue;
-        // all of this thread's sums first (every load independent of every other), then
-        // the stores: parts are added in K order, part 0 first
-        const float* col0 = tile_ws + eq * 32 + lane;
-        float acc[kHalf];
-#pragma unroll
-        for (int c = 0; c < kHalf; ++c) acc[c] = __ldcg(col0 + (c_begin + c) * kBW);
-        for (int q = 1; q < nparts; ++q) {
-          const float* colq = col0 + q * BX * kBW;
-          float x[kHalf];
-#pragma unroll
-          for (int c = 0; c < kHalf; ++c) x[c] = __ldcg(colq + (c_begin + c) * kBW);
-#pragma unroll
-          for (int c = 0; c < kHalf; ++c) acc[c] = __fadd_rn(acc[c], x[c]);
-        }
-        if (ny < p.N) {
-#pragma unroll
-          for (int c = 0; c < kHalf; ++c)
-            if (m0 + c_begin + c < p.M) store_y(m0 + c_begin + c, ny, acc[c]);
-        }
-        if (tid == 0) p.ws_count[t] = 0;  // ready for the next call
+        advance(cur, kGroups);
       }
+      if (timed_out) {
+        if (lane == 0) fail();
+        timed_out = false;
+      }
+      // every segment is read out, failed or not (each read-out takes all epilogue threads)
+      if (next_drain >= nseg) break;
+      drain(next_drain++);
+      if (failed) l = nl;  // no more stages
     }
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -908,62 +987,61 @@ int launch_linear(const CUtensorMap& tx, const CUtensorMap& tw, const LinArgs& p
 #endif
 }
 
-// Activation rows per CTA.  A CTA spends max(MMA time ~ BX, decode time of its 128 x K
-// weight tile ~ 160 in the same units) per round of the grid, so pick the BX with the
-// fewest rounds x that, among the powers of two from 16 up to the first one >= M.
-int pick_bx(int64_t M, int64_t N, int sms) {
-  const int64_t tiles_w = (N + kBW - 1) / kBW;
-  int best = 16;
-  int64_t best_cost = INT64_MAX;
-  for (int bx = 16; bx <= 256; bx *= 2) {
-    const int64_t tiles = tiles_w * ((M + bx - 1) / bx);
-    const int64_t rounds = (tiles + sms - 1) / sms;
-    const int64_t cost = rounds * (bx > 160 ? bx : 160);
-    if (cost < best_cost) {
-      best_cost = cost;
-      best = bx;
-    }
-    if (bx >= M) break;
-  }
-  return best;
-}
-
-// How a problem runs: tile widths, whether CTAs split tiles, and the workspace that needs.
+// How a problem runs: the activation-tile width BX, the CTAs and the workspace.
 struct LinPlan {
   int bx = 16;
   int64_t tiles_x = 0, tiles = 0;
   int st_count = 0;
-  bool split = false;
-  int ctas = 0;
-  int max_parts = 1;
-  int64_t count_bytes = 0, ws_bytes = 0;
+  int ctas = 0;                          // == tiles: one CTA per tile, each whole
+  int64_t count_bytes = 0, ws_bytes = 0;  // a split's counters and whole workspace
 };
 
-LinPlan plan_linear(int64_t M, int64_t N, int64_t K, int sms) {
-  LinPlan pl;
-  pl.bx = pick_bx(M, N, sms);
-  pl.tiles_x = (M + pl.bx - 1) / pl.bx;
-  pl.tiles = pl.tiles_x * ((N + kBW - 1) / kBW);
-  pl.st_count = int((K / kBK + kSub - 1) / kSub);
-  const int64_t units = pl.tiles * pl.st_count;
-  // fewer tiles than SMs: one CTA per SM, each an equal share of the units
-  if (kCanSplit(pl.bx) && pl.tiles < sms && units >= sms) {
-    pl.split = true;
-    pl.ctas = sms;
-    for (int64_t t = 0; t < pl.tiles; ++t) {
-      const int64_t parts = split_cta_of((t + 1) * pl.st_count - 1, units, sms) -
-                            split_cta_of(t * pl.st_count, units, sms) + 1;
-      if (parts > pl.max_parts) pl.max_parts = int(parts);
+// Plans by estimated time, in units of 1/800 of a weight stage: a stage of BX columns
+// costs 640 + BX (dequantization with the shared-memory reads it contends for, and the
+// MMAs), a CTA about 2400 more (pipeline fill, drain and read-out), and a split CTA the
+// partial tiles' stores and sums, about 1600, and a read-out per tile boundary it crosses
+// (about 400 with one accumulator, hidden with two).  The widths tried are the powers of
+// two from 16 up to the first one >= M.  With split false only whole-tile plans count.
+LinPlan plan_linear(int64_t M, int64_t N, int64_t K, int sms, bool split) {
+  LinPlan best;
+  int64_t best_cost = INT64_MAX;
+  const int st_count = int((K / kBK + kSub - 1) / kSub);
+  for (int bx = 16; bx <= 256; bx *= 2) {
+    LinPlan pl;
+    pl.bx = bx;
+    pl.st_count = st_count;
+    pl.tiles_x = (M + bx - 1) / bx;
+    pl.tiles = pl.tiles_x * ((N + kBW - 1) / kBW);
+    const int64_t units = pl.tiles * st_count;
+    const int64_t stage_cost = 640 + bx;
+    // one CTA per tile, rounds of sms at a time
+    const int64_t rounds = (pl.tiles + sms - 1) / sms;
+    int64_t cost = rounds * (st_count * stage_cost + 2400);
+    pl.ctas = int(pl.tiles < INT32_MAX ? pl.tiles : INT32_MAX);
+    // one CTA per SM, an equal share of the units each (the kernel's unit arithmetic is
+    // 32-bit: units < 2^32, sms < 2^16)
+    if (split && units >= sms && units <= int64_t(UINT32_MAX) && sms < 65536) {
+      const int64_t per_cta = (units + sms - 1) / sms;
+      const int64_t crossings = (per_cta + st_count - 1) / st_count;
+      const int64_t split_cost =
+          per_cta * stage_cost + 2400 + 1600 + (kAccOf(bx) == 1 ? 400 * crossings : 0);
+      if (split_cost < cost) {
+        cost = split_cost;
+        pl.ctas = sms;
+        // the counters come first and sit at the same offsets for every problem on this
+        // device (one per CTA, at most one per SM), so a workspace reused across problems
+        // never reads another problem's partial tiles as counters
+        pl.count_bytes = (int64_t(sms) * 4 + 255) / 256 * 256;
+        pl.ws_bytes = pl.count_bytes + int64_t(sms) * 2 * bx * kBW * 4;
+      }
     }
-    // the counters come first and sit at the same offsets for every problem on this
-    // device (one per SM bounds the tiles of a split problem), so a workspace reused
-    // across problems never reads another problem's partial tiles as counters
-    pl.count_bytes = (int64_t(sms) * 4 + 255) / 256 * 256;
-    pl.ws_bytes = pl.count_bytes + pl.tiles * pl.max_parts * pl.bx * kBW * 4;
-  } else {
-    pl.ctas = int(pl.tiles);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = pl;
+    }
+    if (bx >= M) break;
   }
-  return pl;
+  return best;
 }
 
 template <bool kBF16>
@@ -1010,13 +1088,11 @@ int dq4_nested_linear(const void* X, int32_t in_dtype, const uint8_t* packed,
   EncodeTiled encode = tensor_map_encoder();
   if (!encode) return fail_cuda(DQ4_ERR_LAUNCH, cudaErrorNotSupported);
 
-  LinPlan pl = plan_linear(M, N, K, sms);
+  // a split needs the workspace; without one large enough, every CTA takes a whole tile
+  LinPlan pl = plan_linear(M, N, K, sms, true);
+  if (pl.ws_bytes > 0 && (!workspace || workspace_bytes < pl.ws_bytes))
+    pl = plan_linear(M, N, K, sms, false);
   if (pl.tiles > INT32_MAX) return DQ4_ERR_N;
-  // without a large enough workspace, every CTA takes a whole tile
-  if (pl.split && (!workspace || workspace_bytes < pl.ws_bytes)) {
-    pl.split = false;
-    pl.ctas = int(pl.tiles);
-  }
   const int bx = pl.bx;
   const cuuint32_t estride[2] = {1, 1};
   // X as a 2-D tensor (K fastest, M rows): 64 x bx boxes, 128-byte swizzle, rows past M
@@ -1052,13 +1128,15 @@ int dq4_nested_linear(const void* X, int32_t in_dtype, const uint8_t* packed,
   p.bad = bad;
   p.out_dtype = out_dtype;
   p.tiles_x = static_cast<int>(pl.tiles_x);
-  p.units = pl.tiles * pl.st_count;
+  const bool split = pl.ws_bytes > 0;
+  p.whole = split ? 0 : 1;
   p.ctas = pl.ctas;
-  p.split = pl.split ? 1 : 0;
-  p.max_parts = pl.max_parts;
-  p.ws_count = pl.split ? static_cast<int*>(workspace) : nullptr;
-  p.ws_part = pl.split ? reinterpret_cast<float*>(static_cast<char*>(workspace) + pl.count_bytes)
-                       : nullptr;
+  p.units = split ? uint32_t(pl.tiles * pl.st_count) : 0;
+  p.units_q = split ? p.units / uint32_t(pl.ctas) : 0;
+  p.units_r = split ? p.units % uint32_t(pl.ctas) : 0;
+  p.ws_count = split ? static_cast<int*>(workspace) : nullptr;
+  p.ws_part = split ? reinterpret_cast<float*>(static_cast<char*>(workspace) + pl.count_bytes)
+                    : nullptr;
   {
     // a stage covers 64 kSub values of a row, starting at a multiple of that when K is
     // one; its codes are then blocks b00 .. b00 + window - 1 with b00 a multiple of the
@@ -1083,8 +1161,7 @@ int64_t dq4_nested_linear_workspace_bytes(int64_t M, int64_t N, int64_t K) {
     return 0;
   int dev = 0, sms = 0;
   if (current_device(&dev, &sms) != DQ4_OK) return -DQ4_ERR_DEVICE;
-  const LinPlan pl = plan_linear(M, N, K, sms);
-  return pl.split ? pl.ws_bytes : 0;
+  return plan_linear(M, N, K, sms, true).ws_bytes;
 }
 
 }  // extern "C"

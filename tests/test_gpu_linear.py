@@ -50,10 +50,11 @@ def rounded(y64, out):
         t.to(torch.float32).to(torch.float64).numpy()
 
 
-# The kernel picks its activation-tile width BX from M, N and the SM count; on a
+# The kernel picks its activation-tile width BX from M, N, K and the SM count; on a
 # 152-SM GB300 the shapes with N = 4860 take BX = 32, 64, 128 and 256 (38 weight tiles,
 # the last one ragged), the others BX = 16 or 128; N = 4700 gives an odd count of
-# weight tiles (37) at BX = 128 and 256.
+# weight tiles (37) at BX = 128 and 256.  Most run one CTA per tile; (128, 256, 4096)
+# splits its units over the SMs.
 SHAPES = [(1, 128, 64), (5, 200, 128), (127, 130, 192), (128, 256, 4096), (300, 1000, 512),
           (129, 384, 1024), (2048, 768, 256), (128, 4860, 192), (256, 4860, 128),
           (512, 4860, 64), (1024, 4860, 256), (512, 4700, 128), (2048, 4700, 64)]
@@ -102,7 +103,7 @@ def test_unaligned_scale_codes(dq):
     assert np.array_equal(got.double().cpu().numpy(), want)
 
 
-@pytest.mark.parametrize("M", [16, 512])
+@pytest.mark.parametrize("M", [16, 128, 512, 2048])
 def test_realistic_llm_shape(dq, M):
     """An 11008 x 4096 NF4-style nested weight (blocksize 64, nested 256)."""
     N, K = 11008, 4096
@@ -148,12 +149,16 @@ def test_errors(dq):
                   t["value_codebook"], 0.0, 64, 64, 256)
 
 
-# Fewer output tiles than SMs: with a workspace the SMs share the tiles' K ranges and
-# partial FP32 tiles are summed in K order by the last CTA to finish each tile.
-# (units = tiles x 4-K-step stages must reach the SM count; K = 1216 ends in a partial stage)
-# BX = 16 for all but the last (BX = 64 on a 152-SM GB300; BX >= 128 never splits)
-SPLIT_SHAPES = [(16, 11008, 4096), (3, 2000, 4096), (100, 2000, 512), (128, 1024, 8192),
-                (16, 4860, 1216), (64, 9856, 1024)]
+# Tiles that would not fill the SMs in whole rounds: with a workspace one CTA per SM
+# takes an equal share of the (tile, stage) units, a run that may cross tile boundaries;
+# partial FP32 tiles are summed in K order by the last CTA to finish each tile.  On a
+# 152-SM GB300 these take (BX, most tiles one CTA touches): (16, 2), (16, 1), (128, 1),
+# (16, 1) with a partial last stage (K = 1216), (64, 2), (256, 2), (256, 2) ragged,
+# (256, 3) ragged, (256, 3) with one-stage tiles, (64, 3) one-stage, (16, 3), (256, 5).
+# BX <= 64 alternates two accumulators, wider tiles reuse one.
+SPLIT_SHAPES = [(16, 11008, 4096), (3, 2000, 4096), (128, 1024, 8192), (16, 4860, 1216),
+                (128, 2000, 2048), (300, 2000, 2048), (640, 2000, 1216), (2048, 4096, 1216),
+                (1024, 9856, 128), (300, 9856, 192), (16, 49152, 512), (2048, 9856, 512)]
 
 
 @pytest.mark.parametrize("M,N,K", SPLIT_SHAPES)
@@ -221,7 +226,8 @@ def test_split_realistic_matches_whole_tiles(dq):
 
 def test_one_workspace_across_shapes(dq):
     """A workspace first used by a problem with few tiles, then by ones with more."""
-    shapes = [(128, 256, 4096), (16, 11008, 1024), (100, 2000, 512), (3, 2000, 4096)]
+    shapes = [(128, 256, 4096), (16, 11008, 1024), (300, 2000, 2048), (100, 2000, 512),
+              (3, 2000, 4096), (2048, 9856, 512)]
     need = max(int(dq.lib.dq4_nested_linear_workspace_bytes(*sh)) for sh in shapes)
     ws = torch.zeros(need, dtype=torch.uint8, device=DEV)
     for M, N, K in shapes + shapes[::-1]:
@@ -237,8 +243,13 @@ def test_one_workspace_across_shapes(dq):
         assert np.array_equal(got.double().cpu().numpy(), want), (M, N, K)
 
 
-def test_wide_tiles_never_split(dq):
-    assert dq.lib.dq4_nested_linear_workspace_bytes(128, 9856, 1024) == 0  # BX = 128
+def test_workspace_is_bounded_by_the_sm_count(dq):
+    """Partial tiles are kept per CTA (two each, one CTA per SM), not per tile."""
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    bound = (4 * sms + 255) // 256 * 256 + sms * 2 * 256 * 128 * 4
+    for M, N, K in [(16, 11008, 4096), (512, 11008, 4096), (4096, 11008, 4096),
+                    (4096, 28672, 8192), (65536, 4096, 4096)]:
+        assert 0 <= int(dq.lib.dq4_nested_linear_workspace_bytes(M, N, K)) <= bound
 
 
 @pytest.mark.parametrize("xin,out", [("f16", "f16"), ("f16", "f32"), ("bf16", "bf16")])
@@ -255,7 +266,8 @@ def test_split_dtypes_exact(dq, xin, out):
 
 def test_graph_capture_and_replay(dq):
     """dq.linear captured in a CUDA graph (split path, cached workspace) replays exactly."""
-    M, N, K = 16, 4096, 1024
+    M, N, K = 16, 4096, 2048
+    assert dq.lib.dq4_nested_linear_workspace_bytes(M, N, K) > 0
     p = gen.make_integer_problem(N, K, seed=41)
     t = {k: torch.from_numpy(np.ascontiguousarray(getattr(p, k))).to(DEV)
          for k in ("packed", "scale_codes", "nested_absmax", "scale_codebook", "value_codebook")}
