@@ -999,9 +999,11 @@ struct LinPlan {
 // Plans by estimated time, in units of 1/800 of a weight stage: a stage of BX columns
 // costs 640 + BX (dequantization with the shared-memory reads it contends for, and the
 // MMAs), a CTA about 2400 more (pipeline fill, drain and read-out), and a split CTA the
-// partial tiles' stores and sums, about 1600, and a read-out per tile boundary it crosses
-// (about 400 with one accumulator, hidden with two).  The widths tried are the powers of
-// two from 16 up to the first one >= M.  With split false only whole-tile plans count.
+// partial tiles' stores and sums, about 1600 + 15 BX (two FP32 partials of 128 x BX each
+// go out and come back, at the end of the run when every SM does the same), and a
+// read-out per tile boundary it crosses (about 400 with one accumulator, hidden with
+// two).  The widths tried are the powers of two from 16 up to the first one >= M.  With
+// split false only whole-tile plans count.
 LinPlan plan_linear(int64_t M, int64_t N, int64_t K, int sms, bool split) {
   LinPlan best;
   int64_t best_cost = INT64_MAX;
@@ -1024,7 +1026,8 @@ LinPlan plan_linear(int64_t M, int64_t N, int64_t K, int sms, bool split) {
       const int64_t per_cta = (units + sms - 1) / sms;
       const int64_t crossings = (per_cta + st_count - 1) / st_count;
       const int64_t split_cost =
-          per_cta * stage_cost + 2400 + 1600 + (kAccOf(bx) == 1 ? 400 * crossings : 0);
+          per_cta * stage_cost + 2400 + 1600 + 15 * bx +
+          (kAccOf(bx) == 1 ? 400 * crossings : 0);
       if (split_cost < cost) {
         cost = split_cost;
         pl.ctas = sms;

@@ -152,13 +152,15 @@ def test_errors(dq):
 # Tiles that would not fill the SMs in whole rounds: with a workspace one CTA per SM
 # takes an equal share of the (tile, stage) units, a run that may cross tile boundaries;
 # partial FP32 tiles are summed in K order by the last CTA to finish each tile.  On a
-# 152-SM GB300 these take (BX, most tiles one CTA touches): (16, 2), (16, 1), (128, 1),
-# (16, 1) with a partial last stage (K = 1216), (64, 2), (256, 2), (256, 2) ragged,
-# (256, 3) ragged, (256, 3) with one-stage tiles, (64, 3) one-stage, (16, 3), (256, 5).
+# 152-SM GB300 these take (BX, most tiles one CTA touches): (16, 2), (16, 1), (64, 2),
+# (16, 1) with a partial last stage (K = 1216), (64, 2), (128, 2) ragged, (128, 3)
+# ragged, (256, 2) ragged, (256, 3) with a partial last stage, (256, 4) ragged with
+# one-stage tiles of one K step, (256, 5) one-stage, (16, 3), (256, 5).
 # BX <= 64 alternates two accumulators, wider tiles reuse one.
 SPLIT_SHAPES = [(16, 11008, 4096), (3, 2000, 4096), (128, 1024, 8192), (16, 4860, 1216),
-                (128, 2000, 2048), (300, 2000, 2048), (640, 2000, 1216), (2048, 4096, 1216),
-                (1024, 9856, 128), (300, 9856, 192), (16, 49152, 512), (2048, 9856, 512)]
+                (128, 2000, 2048), (384, 1000, 4096), (300, 9856, 2048), (300, 4096, 4096),
+                (1024, 9856, 1216), (1500, 9856, 64), (2048, 9856, 256), (16, 49152, 512),
+                (2048, 9856, 512)]
 
 
 @pytest.mark.parametrize("M,N,K", SPLIT_SHAPES)
@@ -226,7 +228,7 @@ def test_split_realistic_matches_whole_tiles(dq):
 
 def test_one_workspace_across_shapes(dq):
     """A workspace first used by a problem with few tiles, then by ones with more."""
-    shapes = [(128, 256, 4096), (16, 11008, 1024), (300, 2000, 2048), (100, 2000, 512),
+    shapes = [(128, 256, 4096), (16, 11008, 1024), (300, 4096, 4096), (100, 2000, 512),
               (3, 2000, 4096), (2048, 9856, 512)]
     need = max(int(dq.lib.dq4_nested_linear_workspace_bytes(*sh)) for sh in shapes)
     ws = torch.zeros(need, dtype=torch.uint8, device=DEV)
