@@ -195,19 +195,17 @@ __device__ __forceinline__ bool bar_and_256(bool v) {
   return r != 0;
 }
 
-// The FP32 word at shared-memory byte address `addr` (a 32-bit shared address, so the
-// load is a shared-memory load whatever the compiler infers about the pointer).
-__device__ __forceinline__ float lds_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+// The 8-byte word at shared-memory byte address `addr` (8-byte aligned).
+__device__ __forceinline__ uint64_t lds_b64(uint32_t addr) {
+  uint64_t v;
+  asm volatile("ld.shared.b64 %0, [%1];" : "=l"(v) : "r"(addr));
   return v;
 }
 
-// (a * s, b * s), each product rounded to nearest FP32 on its own (one packed
-// f32x2 multiply; no contraction, so the bits equal two __fmul_rn).
-__device__ __forceinline__ void mul2_rn(float a, float b, uint64_t s2, float& x, float& y) {
-  uint64_t ab, r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(ab) : "f"(a), "f"(b));
+// (a * s, b * s) for the FP32 pair ab = {a, b} (a in the low word), each product
+// rounded to nearest FP32 on its own: one packed f32x2 multiply, never contracted.
+__device__ __forceinline__ void mul2_rn64(uint64_t ab, uint64_t s2, float& x, float& y) {
+  uint64_t r;
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(ab), "l"(s2));
   asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(r));
 }
@@ -312,8 +310,14 @@ struct LinSmem {
   static constexpr int kXSub = BX <= 32 ? kSub : 1;
   static constexpr int kXSlot = kXSub * kB;
   static constexpr int kXS = BX <= 32 ? 3 : BX == 64 ? 8 : BX == 128 ? 6 : 4;  // slots
-  // raw weight stages: what the activation ring leaves of a 220 KB budget, at most 16
-  static constexpr int kRawFit = (220 * 1024 - kXS * kXSlot) / kRawSlot;
+  // The codebook as a byte-indexed pair table: entry b holds (vcb[b >> 4], vcb[b & 15]),
+  // the two values of a packed byte, as 8 bytes, replicated 16 times so that lane l reads
+  // copy l % 16: each half warp's 8-byte loads then fall in 16 distinct bank pairs
+  // whatever bytes its lanes decode.  Entry b copy g sits at (16 b + g) * 8.
+  static constexpr int kTabBytes = 256 * 16 * 8;
+  // raw weight stages: what the activation ring and the table leave of a 224 KB budget,
+  // at most 16
+  static constexpr int kRawFit = (224 * 1024 - kTabBytes - kXS * kXSlot) / kRawSlot;
   // A group waits for the raw load of its stage i; the load into the same slot before it
   // (stage i - kRawS) must be known complete, which holds when that stage is the group's
   // own: kRawS a multiple of kGroups (TMA loads need not complete in issue order).
@@ -321,12 +325,14 @@ struct LinSmem {
   static_assert(kRawS >= 4, "raw ring too shallow");
   static constexpr int kXOff = 0;
   static constexpr int kRawOff = kXOff + kXS * kXSlot;
-  static constexpr int kBarOff = kRawOff + kRawS * kRawSlot;
+  static constexpr int kTabOff = kRawOff + kRawS * kRawSlot;
+  static constexpr int kBarOff = kTabOff + kTabBytes;
   // full_w, empty_a per weight stage; full_x, empty_x per activation stage;
   // raw_full, raw_empty per raw stage; acc_full, acc_empty per accumulator; acc_done
   static constexpr int kBars = 2 * kAS + 2 * kXS + 2 * kRawS + 2 * kAcc + 1;
   static constexpr int kBytes = kBarOff + 8 * kBars + 1024;  // + alignment slack
-  static_assert(kBytes <= 227 * 1024, "shared memory budget");
+  // with the kernel's static shared memory (the scale codebook and a few words)
+  static_assert(kBytes + 1280 <= 227 * 1024, "shared memory budget");
   // more than half an SM's shared memory: one CTA per SM, so the 512-column TMEM
   // allocation never waits for another CTA
   static_assert(kBytes > 116 * 1024, "one CTA per SM");
@@ -356,7 +362,6 @@ __global__ void __launch_bounds__(kLinThreads, 1)
   constexpr int kOut = kBF16 ? DQ4_OUT_BF16 : DQ4_OUT_F16;
   constexpr unsigned kFull = 0xFFFFFFFFu;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ float s_vcb[16];
   __shared__ float s_scb[256];
   __shared__ uint32_t s_tmem;          // TMEM base address from tcgen05.alloc
   __shared__ volatile int s_abort;     // set when any wait of the CTA ran out
@@ -439,7 +444,11 @@ __global__ void __launch_bounds__(kLinThreads, 1)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
 #endif
-  if (tid < 16) s_vcb[tid] = __ldg(p.w.vcb + tid);
+  for (int i = tid; i < 256 * 16; i += kLinThreads) {  // the pair table, entry i / 16
+    const int b = i >> 4;
+    *reinterpret_cast<float2*>(base + S::kTabOff + 8 * i) =
+        make_float2(__ldg(p.w.vcb + (b >> 4)), __ldg(p.w.vcb + (b & 15)));
+  }
   for (int k = tid; k < 256; k += kLinThreads) s_scb[k] = __ldg(p.w.scb + k);
   if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
@@ -816,7 +825,8 @@ __global__ void __launch_bounds__(kLinThreads, 1)
     }
     bool timed_out = false;
     int next_drain = 0;  // the next segment to read out
-    const uint32_t vcb = smem_u32(s_vcb);  // codebook entries at vcb + 4 * nibble
+    // this lane's copy of the pair table: entry b at tab + 128 b
+    const uint32_t tab = sbase + S::kTabOff + (lane & 15) * 8;
     const int flip = (r >> 2) & 1;  // the raw boxes' 32-byte swizzle for this row
     // Segment d is read out before the first stage whose weight slot waits for MMAs that
     // need its accumulator back (kAS stages into segment d + 1; the MMA then has those
@@ -883,15 +893,12 @@ __global__ void __launch_bounds__(kLinThreads, 1)
           uint32_t o[4 * kWords];  // 8 values per word, two per 32-bit TMEM column
   #pragma unroll
           for (int e = 0; e < kWords; ++e) {
-            // nibble * 4 (the byte offset of its codebook entry) in each byte
-            const uint32_t hi4 = (wd[e] >> 2) & 0x3C3C3C3Cu;  // earlier value of each byte
-            const uint32_t lo4 = (wd[e] << 2) & 0x3C3C3C3Cu;
   #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              const float a = lds_f32(vcb + __byte_perm(hi4, 0, 0x4440 + j));
-              const float b = lds_f32(vcb + __byte_perm(lo4, 0, 0x4440 + j));
+              // byte j's pair (earlier value = high nibble, later = low nibble)
+              const uint32_t byte = __byte_perm(wd[e], 0, 0x4440 + j);
               float v0, v1;
-              mul2_rn(a, b, sc2[e / 4 < kHalves ? e / 4 : 0], v0, v1);
+              mul2_rn64(lds_b64(tab + (byte << 7)), sc2[e / 4 < kHalves ? e / 4 : 0], v0, v1);
               o[4 * e + j] = pack2<kOut>(v0, v1);
             }
           }
