@@ -185,6 +185,35 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
                :: "memory");
 }
 
+// 32 consecutive accumulator columns: four loads, one wait.  The wait names half the
+// registers (an asm statement takes at most 30 operands); the empty statement after it
+// (volatile, so it stays after the wait) names the rest, so no use of any of them
+// moves above the wait.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+        : "=r"(r[8 * q]), "=r"(r[8 * q + 1]), "=r"(r[8 * q + 2]), "=r"(r[8 * q + 3]),
+          "=r"(r[8 * q + 4]), "=r"(r[8 * q + 5]), "=r"(r[8 * q + 6]), "=r"(r[8 * q + 7])
+        : "r"(taddr + 8 * q));
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+               :: "memory");
+  asm volatile(""
+               : "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                 "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]),
+                 "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
+}
+
+template <int N>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[N]) {
+  static_assert(N == 8 || N == 32, "8 or 32 columns");
+  if constexpr (N == 8) tmem_ld8(taddr, r); else tmem_ld32(taddr, r);
+}
+
 // Named barrier 1 over the 256 epilogue threads, AND-reducing a predicate.
 __device__ __forceinline__ bool bar_and_256(bool v) {
   uint32_t r;
@@ -193,6 +222,20 @@ __device__ __forceinline__ bool bar_and_256(bool v) {
       "selp.u32 %0, 1, 0, q;\n}"
       : "=r"(r) : "r"(static_cast<uint32_t>(v)) : "memory");
   return r != 0;
+}
+
+// 16 and 8 bytes at shared-memory byte address `addr` (aligned to their size): shared
+// loads named as such, so they need no generic-address resolution.
+__device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint2 lds_v2(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
 }
 
 // The 8-byte word at shared-memory byte address `addr` (8-byte aligned).
@@ -444,11 +487,6 @@ __global__ void __launch_bounds__(kLinThreads, 1)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
 #endif
-  for (int i = tid; i < 256 * 16; i += kLinThreads) {  // the pair table, entry i / 16
-    const int b = i >> 4;
-    *reinterpret_cast<float2*>(base + S::kTabOff + 8 * i) =
-        make_float2(__ldg(p.w.vcb + (b >> 4)), __ldg(p.w.vcb + (b & 15)));
-  }
   for (int k = tid; k < 256; k += kLinThreads) s_scb[k] = __ldg(p.w.scb + k);
   if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
@@ -624,6 +662,21 @@ __global__ void __launch_bounds__(kLinThreads, 1)
       mbar_wait(acc_done, 0);
     }
   } else {
+    // The pair table, built by the producer warps alone while the TMA warps start their
+    // copies: one codebook load per thread, the entries' values by shuffle (entry b copy
+    // g = word 16 b + g holds vcb[b >> 4], vcb[b & 15]); named barrier 2 over the producer
+    // threads orders it before their first lookup.
+    {
+      const float v = __ldg(p.w.vcb + (lane & 15));
+      for (int i = tid; i < 256 * 16; i += kProducerWarps * 32) {
+        const int b = i >> 4;
+        float2 e;
+        e.x = __shfl_sync(kFull, v, b >> 4);
+        e.y = __shfl_sync(kFull, v, b & 15);
+        *reinterpret_cast<float2*>(base + S::kTabOff + 8 * i) = e;
+      }
+      asm volatile("bar.sync 2, %0;" :: "n"(kProducerWarps * 32) : "memory");
+    }
     // ---- dequantize.  Producer group `group` (kGroupWarps warps) takes local stages
     // group, group + kGroups, ...; within it, warp w writes TMEM lanes 32 (w % 4) ..
     // (weight row r = 32 (w % 4) + lane of the stage's tile) and values 8 kWords h ..
@@ -635,10 +688,15 @@ __global__ void __launch_bounds__(kLinThreads, 1)
     const float offset = p.w.offset;
     const uint32_t t_row = tmem + (static_cast<uint32_t>(quad * 32) << 16) + kATmemCol +
                            4 * kWords * h;  // this warp's lanes, its columns of a K step
-    // the scale codes / absmax of the stage at cursor cs (local stage l) for this
-    // thread's row
+    // The scale codes / absmax of the stage at cursor cs (local stage l) for this thread's
+    // row.  With an aligned code window the stage's codes arrive in one load (w) and its
+    // absmax in another (m), unpacked into c / a only when the stage is decoded: nothing
+    // consumes a load in the iteration that issues it, so no warp waits on one.  Otherwise
+    // the codes and absmax are loaded per K step straight into c / a.
     auto fetch = [&](int l, const Cursor& cs, uint32_t (&c)[kSub][kHalves],
-                     float (&a)[kSub][kHalves]) {
+                     float (&a)[kSub][kHalves], uint64_t& w, float& m) {
+      w = 0;
+      m = 0.f;
 #pragma unroll
       for (int sub = 0; sub < kSub; ++sub)
 #pragma unroll
@@ -650,25 +708,15 @@ __global__ void __launch_bounds__(kLinThreads, 1)
       const int j0 = cs.stage * kSub;
       const int64_t idx0 = (cs.n0 + r) * p.K + 8 * kWords * h;  // this thread's first value
       if (p.code_window != 0) {
-        // the stage's codes of this row in one aligned load, its absmax in another
         const int64_t b00 = (idx0 - 8 * kWords * h + int64_t(j0) * kBK) >> p.w.log2_bs;
         const uint8_t* cp = p.w.codes + b00;
-        uint64_t win;
         switch (p.code_window) {
-          case 8: win = __ldg(reinterpret_cast<const unsigned long long*>(cp)); break;
-          case 4: win = __ldg(reinterpret_cast<const unsigned int*>(cp)); break;
-          case 2: win = __ldg(reinterpret_cast<const unsigned short*>(cp)); break;
-          default: win = __ldg(cp); break;
+          case 8: w = __ldg(reinterpret_cast<const unsigned long long*>(cp)); break;
+          case 4: w = __ldg(reinterpret_cast<const unsigned int*>(cp)); break;
+          case 2: w = __ldg(reinterpret_cast<const unsigned short*>(cp)); break;
+          default: w = __ldg(cp); break;
         }
-        const float am = __ldg(p.w.absmax + (b00 >> p.w.log2_nbs));
-#pragma unroll
-        for (int sub = 0; sub < kSub; ++sub)
-#pragma unroll
-          for (int hh = 0; hh < kHalves; ++hh) {
-            const int off = (kBK * sub + 32 * hh + 8 * kWords * h) >> p.w.log2_bs;
-            c[sub][hh] = static_cast<uint32_t>(win >> (8 * off)) & 0xFFu;  // off < window
-            a[sub][hh] = am;
-          }
+        m = __ldg(p.w.absmax + (b00 >> p.w.log2_nbs));
         return;
       }
 #pragma unroll
@@ -683,6 +731,19 @@ __global__ void __launch_bounds__(kLinThreads, 1)
           }
         }
     };
+    // a window-loaded stage's codes and absmax, per K step and 32-value half
+    auto unpack = [&](uint64_t w, float m, uint32_t (&c)[kSub][kHalves],
+                      float (&a)[kSub][kHalves]) {
+      if (p.code_window == 0) return;
+#pragma unroll
+      for (int sub = 0; sub < kSub; ++sub)
+#pragma unroll
+        for (int hh = 0; hh < kHalves; ++hh) {
+          const int off = (kBK * sub + 32 * hh + 8 * kWords * h) >> p.w.log2_bs;
+          c[sub][hh] = static_cast<uint32_t>(w >> (8 * off)) & 0xFFu;  // off < window
+          a[sub][hh] = m;
+        }
+    };
     // ---- read-out of segment ds (warps 0..7; named barrier 1 over their 256 threads):
     // warps w and w + 4 read TMEM lanes 32 (w % 4) .. (weight rows = columns of Y), each
     // half of the BX accumulator columns (activation rows).  A whole tile goes to Y; a
@@ -690,6 +751,7 @@ __global__ void __launch_bounds__(kLinThreads, 1)
     // its parts into Y.
     constexpr int kHalf = BX / 2;
     constexpr int kChunk = kHalf < 32 ? kHalf : 32;  // columns per step of the parts' sum
+    constexpr int kLd = kHalf < 32 ? 8 : 32;  // accumulator columns per TMEM read (one wait)
     const int eq = warp & 3, c_begin = ((warp >> 2) & 1) * kHalf;
     auto store_y = [&](int64_t m, int64_t ny, float f) {
       const int64_t o = m * p.N + ny;  // a warp writes 32 consecutive columns of row m
@@ -728,13 +790,13 @@ __global__ void __launch_bounds__(kLinThreads, 1)
       };
       if (whole) {
 #pragma unroll 1
-        for (int c = 0; c < kHalf; c += 8) {
+        for (int c = 0; c < kHalf; c += kLd) {
           if (m0 + c >= p.M) break;  // warp-uniform
-          uint32_t v[8];
-          tmem_ld8(t_acc + c, v);
+          uint32_t v[kLd];
+          tmem_ld(t_acc + c, v);
           if (ny >= p.N) continue;
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
+          for (int j = 0; j < kLd; ++j) {
             if (m0 + c + j >= p.M) break;
             store_y(m0 + c + j, ny, __uint_as_float(v[j]));
           }
@@ -748,11 +810,11 @@ __global__ void __launch_bounds__(kLinThreads, 1)
                     ((int64_t(blockIdx.x) * 2 + (ds == 0 ? 0 : 1)) * BX + c_begin) * kBW +
                     eq * 32 + lane;
 #pragma unroll 1
-      for (int c = 0; c < kHalf; c += 8) {
-        uint32_t v[8];
-        tmem_ld8(t_acc + c, v);
+      for (int c = 0; c < kHalf; c += kLd) {
+        uint32_t v[kLd];
+        tmem_ld(t_acc + c, v);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) part[(c + j) * kBW] = __uint_as_float(v[j]);
+        for (int j = 0; j < kLd; ++j) part[(c + j) * kBW] = __uint_as_float(v[j]);
       }
       release();
       // the tile's parts are those of CTAs c_first .. c_last, in K order (found by
@@ -812,10 +874,12 @@ __global__ void __launch_bounds__(kLinThreads, 1)
     // unrolling over stages: the loop body stays small enough for the instruction cache)
     uint32_t cA[kSub][kHalves], cB[kSub][kHalves];
     float aA[kSub][kHalves], aB[kSub][kHalves];
+    uint64_t wA, wB;
+    float mA, mB;
     Cursor cur = cursor_at(group);            // stage l
     Cursor pf = cursor_at(group + kGroups);   // stage l + 2 kGroups, once advanced below
-    fetch(group, cur, cA, aA);
-    fetch(group + kGroups, pf, cB, aB);
+    fetch(group, cur, cA, aA, wA, mA);
+    fetch(group + kGroups, pf, cB, aB, wB, mB);
     advance(pf, kGroups);
     RingPos<kAS> apos;
     RingPos<kRawS> rpos;
@@ -836,6 +900,7 @@ __global__ void __launch_bounds__(kLinThreads, 1)
     for (;;) {
       const int lim = next_drain < nseg - 1 ? min(nl, seg_start(next_drain + 1) + kAS) : nl;
       for (; l < lim; l += kGroups) {  // local stage l
+        unpack(wA, mA, cA, aA);  // loaded an iteration ago
         float sc[kSub][kHalves];
   #pragma unroll
         for (int sub = 0; sub < kSub; ++sub)
@@ -845,7 +910,9 @@ __global__ void __launch_bounds__(kLinThreads, 1)
             cA[sub][hh] = cB[sub][hh];
             aA[sub][hh] = aB[sub][hh];
           }
-        fetch(l + 2 * kGroups, pf, cB, aB);
+        wA = wB;
+        mA = mB;
+        fetch(l + 2 * kGroups, pf, cB, aB, wB, mB);
         advance(pf, kGroups);
         // the raw stage has landed and the MMAs that read this weight slot last completed
         // (the first kAS stages have nothing to wait for: their empty phase reads as done)
@@ -863,7 +930,7 @@ __global__ void __launch_bounds__(kLinThreads, 1)
         // rows are 32 bytes apart in each raw box, whose 32-byte swizzle stores the 16-byte
         // chunk c of row r at chunk c ^ ((r >> 2) & 1): the 8 rows a quarter warp reads then
         // fill all 32 banks
-        const uint8_t* raw_row = base + S::kRawOff + rpos.slot * S::kRawSlot + r * 32;
+        const uint32_t raw_row = sbase + S::kRawOff + rpos.slot * S::kRawSlot + r * 32;
         const uint32_t t_stage = t_row + apos.slot * kSub * 32;
   #pragma unroll 1
         for (int sub = 0; sub < ns; ++sub) {
@@ -877,16 +944,16 @@ __global__ void __launch_bounds__(kLinThreads, 1)
             asm("mov.b64 %0, {%1, %1};" : "=l"(sc2[hh]) : "f"(v));
           }
           uint32_t wd[kWords];
-          const uint8_t* row = raw_row + sub * kRawBytes;
+          const uint32_t row = raw_row + sub * kRawBytes;
   #pragma unroll
           for (int v = 0; v < (kWords + 3) / 4; ++v) {
             const int chunk = (kWords * h) / 4 + v;  // logical 16-byte chunk of the row
-            const uint8_t* src = row + (((chunk ^ flip) & 1) << 4) + ((kWords * h) % 4) * 4;
+            const uint32_t src = row + (((chunk ^ flip) & 1) << 4) + ((kWords * h) % 4) * 4;
             if constexpr (kWords >= 4) {
-              const uint4 w4 = *reinterpret_cast<const uint4*>(src);
+              const uint4 w4 = lds_v4(src);
               wd[4 * v] = w4.x, wd[4 * v + 1] = w4.y, wd[4 * v + 2] = w4.z, wd[4 * v + 3] = w4.w;
             } else {
-              const uint2 w2 = *reinterpret_cast<const uint2*>(src);
+              const uint2 w2 = lds_v2(src);
               wd[0] = w2.x, wd[1] = w2.y;
             }
           }
