@@ -99,6 +99,46 @@ def dist_env():
     return rank, world, local
 
 
+class Ranks:
+    """The ranks of a run: one process per GPU under torchrun, each a replica of the
+    workload (no data-path collective).  The only cross-rank traffic is the barrier that
+    brackets the timed region and the max of the ranks' times.  `backend` is "nccl" on
+    the GPUs; the multi-rank CPU tests run the same code over "gloo"."""
+
+    def __init__(self, backend: str = "nccl", device=None):
+        self.rank, self.world, self.local = dist_env()
+        self.device = device
+        self._dist = None
+        if self.world > 1:
+            import torch.distributed as dist
+            kw = {"device_id": device} if backend == "nccl" else {}
+            dist.init_process_group(backend, **kw)
+            self._dist = dist
+
+    def barrier(self):
+        if self._dist is not None:
+            self._dist.barrier()
+
+    def max_over_ranks(self, x: float) -> float:
+        if self._dist is None:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64, device=self.device)
+        self._dist.all_reduce(t, op=self._dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self._dist is not None:
+            self._dist.destroy_process_group()
+            self._dist = None
+
+
+def whole_job_rate(world: int, units_per_rank: float, elapsed_ms: float) -> float:
+    """Units all ranks processed per second of the slowest rank's time (weak scaling:
+    every rank processes the same units)."""
+    return world * units_per_rank / (elapsed_ms / 1e3)
+
+
 def read_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -200,26 +240,15 @@ class ClockSampler:
 # -------------------------------------------------------------- our arm
 def run_ours(args):
     import torch
-    import torch.distributed as dist
 
     import quantized_weight_dequantization_gb300 as dq
 
-    rank, world, local = dist_env()
+    _, _, local = dist_env()
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
-    if world > 1:
-        dist.init_process_group("nccl", device_id=dev)
-
-    def barrier():
-        if world > 1:
-            dist.barrier()
-
-    def max_over_ranks(x: float) -> float:
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    ranks = Ranks("nccl", dev)
+    rank, world = ranks.rank, ranks.world
+    barrier, max_over_ranks = ranks.barrier, ranks.max_over_ranks
 
     cell = gen.CELLS[args.cell]
     p = cell.problem()
@@ -414,7 +443,7 @@ def run_ours(args):
 
     peak, peak_kind = read_peaks()
     ms_per_step = elapsed_ms / K
-    value = world * K * n / (elapsed_ms / 1e3)
+    value = whole_job_rate(world, K * n, elapsed_ms)
     achieved_gbs = alg_bytes / (avg_launch_ms / 1e3) / 1e9
     rec = traffic_record(args.cell)
     out = {
@@ -472,7 +501,7 @@ def run_ours(args):
             "launches": {"fused": 1, "unfused": 3},
         },
         "e2e": None if e2e_ms is None else {
-            "value": world * E * n / (e2e_ms / 1e3), "unit": UNIT,
+            "value": whole_job_rate(world, E * n, e2e_ms), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": E,
             "ms_per_step": e2e_ms / E},
         "gpu_launches": K,
@@ -482,8 +511,7 @@ def run_ours(args):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(p, cell, transposed)
-    if world > 1:
-        dist.destroy_process_group()
+    ranks.close()
     if rank == 0:
         print(json.dumps(out), flush=True)
 
