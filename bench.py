@@ -70,6 +70,9 @@ def parse_args():
     ap.add_argument("--m", type=int, default=2048, help="int8prep: activation rows M")
     ap.add_argument("--kn", type=int, default=14336, help="int8prep: K = N")
     ap.add_argument("--l", type=int, default=64, help="int8prep: outlier columns L")
+    ap.add_argument("--int8-grid", action="store_true",
+                    help="int8prep: the page's preparation grid, one launch against the eager "
+                         "gather/multiply/cast/transpose sequence")
     ap.add_argument("--rows", type=int, default=600000, help="outprod: rows of W (summed over)")
     ap.add_argument("--cols", type=int, default=256, help="outprod: columns of W")
     ap.add_argument("--ncols", type=int, default=256, help="outprod: columns of G")
@@ -597,8 +600,125 @@ def run_reference(args):
     }), flush=True)
 
 
+def run_int8_grid(args):
+    """dq4_int8_correction_prep against the eager torch sequence it replaces, over the
+    preparation grid of "Fuse LLM.int8 correction operand preparation into one CUDA kernel"
+    (section "B300 benchmark plan": M in {1, 8, 64, 512, 2048}, K = N in {3584, 4096, 8192,
+    14336}, L in {1, 5, 16, 64}).  Eager: gather A's columns; gather CB's columns, FP32
+    multiply by SCB, FP32 multiply by RN32(1/127), FP16, transpose (section "Exact
+    correctness oracle" fixes that order).  Both produce the same bits, checked per cell.
+    Inputs are drawn on the device from a seeded generator (CB is up to 205 MB per cell).
+    Times: CUDA events around `reps` back-to-back calls, interleaved over `samples` rounds,
+    median per cell, twice: called from Python (host dispatch included: five torch ops
+    against one ctypes call) and replayed from a CUDA graph (device time alone)."""
+    import torch
+
+    import quantized_weight_dequantization_gb300 as dq
+
+    dev = torch.device("cuda:0")
+    L_ = dq.get_lib()
+    r127 = torch.tensor(1.0 / 127.0, dtype=torch.float32, device=dev)
+    g = torch.Generator(device=dev)
+    samples, reps = 30, 10
+    cells = []
+    for KN in (3584, 4096, 8192, 14336):
+        g.manual_seed(KN)
+        CB = torch.randint(-127, 128, (KN, KN), dtype=torch.int8, device=dev, generator=g)
+        SCB = torch.rand(KN, dtype=torch.float32, device=dev, generator=g) * 8.0
+        for M in (1, 8, 64, 512, 2048):
+            A = torch.randn(M, KN, dtype=torch.float16, device=dev, generator=g)
+            for L in (1, 5, 16, 64):
+                cols = torch.sort(torch.randperm(KN, device=dev, generator=g)[:L]).values
+                subA = torch.empty((M, L), dtype=torch.float16, device=dev)
+                subB = torch.empty((L, KN), dtype=torch.float16, device=dev)
+
+                def ours():
+                    return L_.dq4_int8_correction_prep(
+                        A.data_ptr(), CB.data_ptr(), SCB.data_ptr(), cols.data_ptr(), M, KN, KN,
+                        L, subA.data_ptr(), subB.data_ptr(), None,
+                        torch.cuda.current_stream(dev).cuda_stream)
+
+                def eager():
+                    ea = A.index_select(1, cols)
+                    eb = ((CB.index_select(1, cols).float() * SCB.view(-1, 1)) * r127)
+                    return ea, eb.half().t().contiguous()
+
+                if ours() != 0:
+                    raise SystemExit(f"status error at M={M} K=N={KN} L={L}")
+                ea, eb = eager()
+                torch.cuda.synchronize(dev)
+                if not (torch.equal(ea.view(torch.int16), subA.view(torch.int16)) and
+                        torch.equal(eb.view(torch.int16), subB.view(torch.int16))):
+                    raise SystemExit(f"eager and fused differ at M={M} K=N={KN} L={L}")
+                for _ in range(max(3, args.warmup)):
+                    ours()
+                    eager()
+                t_o, t_e = [], []
+                for _ in range(samples):
+                    for fn, acc in ((ours, t_o), (eager, t_e)):
+                        e0 = torch.cuda.Event(enable_timing=True)
+                        e1 = torch.cuda.Event(enable_timing=True)
+                        e0.record()
+                        for _ in range(reps):
+                            fn()
+                        e1.record()
+                        torch.cuda.synchronize(dev)
+                        acc.append(e0.elapsed_time(e1) / reps * 1e3)
+                # device time alone: each arm's `reps` calls captured in a CUDA graph
+                graphs = []
+                for fn in (ours, eager):
+                    s_ = torch.cuda.Stream(dev)
+                    s_.wait_stream(torch.cuda.current_stream(dev))
+                    with torch.cuda.stream(s_):
+                        fn()
+                    torch.cuda.current_stream(dev).wait_stream(s_)
+                    gr = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(gr):
+                        for _ in range(reps):
+                            fn()
+                    graphs.append(gr)
+                d_o, d_e = [], []
+                for _ in range(samples):
+                    for gr, acc in zip(graphs, (d_o, d_e)):
+                        e0 = torch.cuda.Event(enable_timing=True)
+                        e1 = torch.cuda.Event(enable_timing=True)
+                        e0.record()
+                        gr.replay()
+                        e1.record()
+                        torch.cuda.synchronize(dev)
+                        acc.append(e0.elapsed_time(e1) / reps * 1e3)
+                del graphs
+                cells.append({"M": M, "KN": KN, "L": L,
+                              "fused_us": pct(t_o, 50), "eager_us": pct(t_e, 50),
+                              "speedup": pct(t_e, 50) / pct(t_o, 50),
+                              "fused_device_us": pct(d_o, 50), "eager_device_us": pct(d_e, 50),
+                              "speedup_device": pct(d_e, 50) / pct(d_o, 50)})
+            del A
+        del CB, SCB
+    sp = [c["speedup"] for c in cells]
+    spd = [c["speedup_device"] for c in cells]
+    print(json.dumps({
+        "metric": "LLM.int8 correction-operand preparation: eager torch time / fused time",
+        "value": pct(spd, 50), "unit": "x (median over cells, device time)",
+        "higher_is_better": True,
+        "n_gpus": 1, "dtype": "f32", "data": "synthetic (seeded device generator)",
+        "config": {"workload": "int8 correction prep grid M {1,8,64,512,2048} x K=N "
+                               "{3584,4096,8192,14336} x L {1,5,16,64}",
+                   "timing": f"CUDA events, {samples} interleaved samples of {reps} calls, "
+                             "median per cell; inputs resident; device time from CUDA-graph "
+                             "replay, host-driven time from Python calls"},
+        "speedup_device_min": min(spd), "speedup_device_median": pct(spd, 50),
+        "speedup_device_max": max(spd),
+        "speedup_host_min": min(sp), "speedup_host_median": pct(sp, 50),
+        "speedup_host_max": max(sp),
+        "cells": cells,
+    }), flush=True)
+
+
 def run_int8prep(args):
     """Time dq4_int8_correction_prep on one (M, K = N, L) cell of the preparation grid."""
+    if args.int8_grid:
+        return run_int8_grid(args)
     import torch
 
     import quantized_weight_dequantization_gb300 as dq

@@ -9,8 +9,11 @@ namespace dq4d {
 // correctness oracle", in one launch over two output regions:
 //   subA[m][l] = A[m][cols[l]]                                   (16-bit copy)
 //   subB[l][n] = RN16(RN32(RN32(CB[n][cols[l]] * SCB[n]) * RN32(1/127)))
-// CTAs [0, ctas_a) fill subA: each covers kAElems consecutive elements of
-// the row-major M x L array, lanes walking l, so stores are contiguous.  CTAs
+// CTAs [0, ctas_a) fill subA: each covers a_per * kThreads consecutive elements
+// of the row-major M x L array, lanes walking l, so stores are contiguous.  A
+// thread's elements are a chain of dependent loads (index, then A), so a_per
+// is as small as filling the SMs once allows (1 .. 8): small M x L spreads over
+// many CTAs, large M x L keeps its gathers paced against the subB ones.  CTAs
 // [ctas_a, ...) fill subB: each covers kBN consecutive n (two per thread:
 // both SCB values in one 8-byte load, both results in one 4-byte store) and
 // kBL consecutive l; per l a warp stores 128 contiguous bytes of subB.  The
@@ -18,7 +21,7 @@ namespace dq4d {
 // thread issues all kBL * 2 of them before using any.  Column indices are
 // bounds-checked: an index outside [0, K) reads nothing, yields 0 and is
 // counted once into *bad (if given).
-constexpr int kAElems = 2048;  // subA elements per CTA
+constexpr int kAMaxPer = 8;  // most subA elements per thread
 constexpr int kBN = 2 * kThreads;  // subB: n per CTA
 constexpr int kBL = 4;             // subB: l per CTA
 
@@ -32,6 +35,7 @@ struct PrepArgs {
   int* bad;
   int64_t M, N, K, L;
   int64_t ctas_a;
+  int a_per;  // subA elements per thread
   int64_t l_chunks;
   bool count_in_a;  // bad indices are counted once: in the subA region if M > 0
 };
@@ -47,9 +51,9 @@ __global__ void __launch_bounds__(kThreads) int8_prep_kernel(const PrepArgs p) {
   const int64_t bid = blockIdx.x;
   if (bid < p.ctas_a) {
     // ---- subA: a contiguous run of the row-major M x L array
-    const int64_t e0 = bid * kAElems;
+    const int64_t e0 = bid * p.a_per * kThreads;
     const int64_t total = p.M * p.L;
-    for (int k = 0; k < kAElems / kThreads; ++k) {
+    for (int k = 0; k < p.a_per; ++k) {
       const int64_t e = e0 + k * kThreads + threadIdx.x;
       if (e >= total) break;
       const int64_t m = e / p.L, l = e - m * p.L;
@@ -151,7 +155,11 @@ int dq4_int8_correction_prep(const uint16_t* A, const int8_t* CB, const float* S
   p.N = N;
   p.K = K;
   p.L = L;
-  p.ctas_a = (M * L + kAElems - 1) / kAElems;
+  {
+    const int64_t per = (M * L + int64_t(kThreads) * sms - 1) / (int64_t(kThreads) * sms);
+    p.a_per = int(per < 1 ? 1 : per > kAMaxPer ? kAMaxPer : per);
+  }
+  p.ctas_a = (M * L + int64_t(p.a_per) * kThreads - 1) / (int64_t(p.a_per) * kThreads);
   p.l_chunks = (L + kBL - 1) / kBL;
   p.count_in_a = M > 0;
   const int64_t ctas_b = N > 0 ? ((N + kBN - 1) / kBN) * p.l_chunks : 0;
