@@ -30,9 +30,12 @@
 //    lanes 32 (w % 4) .. (the weight rows), a thread one row.  Per 64-value K
 //    step it computes the nested scales of its row's two 32-value halves
 //    (separately rounded FP32 multiply and add; a stage's scale codes come in
-//    one aligned load when the shape allows, held two own stages ahead in
-//    registers) and the 64 values (FP32 products, RN to BF16 / FP16), and
-//    writes them to the weight ring in TMEM with one tcgen05.st; afterwards
+//    one aligned load when the shape allows, loaded two own stages ahead and
+//    unpacked only when their stage is decoded) and the 64 values (both values
+//    of a packed byte from one 8-byte load of a byte-indexed codebook pair
+//    table in shared memory, which these warps build at the start; FP32
+//    products, RN to BF16 / FP16), and writes them to the weight ring in TMEM
+//    with one tcgen05.st; afterwards
 //    warps 0..7 run the epilogue: tcgen05.ld of each segment's accumulator,
 //    conversion, stores of Y (or of a partial tile, and the shared tiles' sums);
 //  * warp 8: allocates the TMEM; lane 0 issues tcgen05.mma (A = weights from
