@@ -109,3 +109,27 @@ def test_unaligned_subB_and_repeated_calls(dq):
         subA, out = dq.int8_correction_prep(A, CB, SCB, cols, subB=subB)
     wa, wb = oracle.int8_correction_prep(p.A_bits, p.CB, p.SCB, p.cols)
     assert np.array_equal(bits16(out), wb) and np.array_equal(bits16(subA), wa)
+
+
+def test_subA_several_elements_per_thread_ragged(dq):
+    # M x L = 128961: more than three fills of the SMs, so each subA thread takes several
+    # elements, and not a multiple of a CTA's share, so the last subA CTA is partial
+    check(dq, gen.make_int8_problem(2047, 512, 4096, 63, seed=13, cols_mode="unsorted"))
+
+
+def test_out_of_range_columns_counted_once_at_large_M(dq):
+    p = gen.make_int8_problem(2047, 64, 4096, 63, seed=14, cols_mode="unsorted")
+    good = p.cols.copy()
+    cols = good.copy()
+    cols[5], cols[40] = -1, 4096  # two invalid entries
+    A, CB, SCB, _ = dev_inputs(p)
+    bad = torch.zeros(1, dtype=torch.int32, device=DEV)
+    subA, subB = dq.int8_correction_prep(A, CB, SCB, torch.from_numpy(cols).to(DEV),
+                                         bad_cols=bad)
+    torch.cuda.synchronize()
+    assert int(bad.item()) == 2
+    wa, wb = oracle.int8_correction_prep(p.A_bits, p.CB, p.SCB, good)
+    ga, gb = bits16(subA), bits16(subB)
+    keep = [l for l in range(63) if l not in (5, 40)]
+    assert np.array_equal(ga[:, keep], wa[:, keep]) and np.all(ga[:, [5, 40]] == 0)
+    assert np.array_equal(gb[keep], wb[keep]) and np.all(gb[[5, 40]] == 0)
