@@ -62,7 +62,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cell", default=DEFAULT_CELL, choices=sorted(gen.CELLS))
-    ap.add_argument("--op", choices=["nested", "transposed", "int8prep", "outprod", "linear"],
+    ap.add_argument("--op", choices=["nested", "transposed", "int8prep", "outprod", "linear",
+                                     "grad_a"],
                     default="nested",
                     help="nested: dq4_nested (flat output); transposed: dq4_nested_transposed "
                          "(W^T output of the rows x cols weight); int8prep: LLM.int8 "
@@ -77,6 +78,8 @@ def parse_args():
     ap.add_argument("--cols", type=int, default=256, help="outprod: columns of W")
     ap.add_argument("--ncols", type=int, default=256, help="outprod: columns of G")
     ap.add_argument("--transient-mib", type=int, default=256, help="outprod: transient bound")
+    ap.add_argument("--grad-m", default="2048,8192",
+                    help="grad_a: rows M of dY (tokens) for the grad_A = dY W shapes")
     ap.add_argument("--lin-m", default="16,128,512,2048,4096",
                     help="linear: comma-separated M values (activation rows)")
     ap.add_argument("--lin-n", type=int, default=11008, help="linear: N (weight rows)")
@@ -971,6 +974,122 @@ def run_linear(args):
         "cells": cells}), flush=True)
 
 
+def graph_time_us(fn, dev, warmup: int, steps: int, calls: int) -> float:
+    """Time per call of `fn`: `calls` back-to-back calls captured in a CUDA graph, replayed
+    until about `steps` calls ran (host overhead excluded)."""
+    import torch
+
+    stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, warmup)):
+            fn()
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for _ in range(calls):
+                fn()
+        for _ in range(2):
+            graph.replay()
+        torch.cuda.synchronize(dev)
+        reps = max(1, steps // calls + 1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            graph.replay()
+        e1.record()
+        torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) / (reps * calls) * 1e3
+
+
+def run_grad_a(args):
+    """grad_A = dY W for a nested 4-bit weight W (N x K): the weight dequantized to BF16 and a
+    cuBLAS GEMM, with the fused dequantization (dq4_nested, one launch) against the unfused
+    three-launch sequence (dq4_nested_unfused, caller-owned FP32 scratch, so no allocator work
+    is timed).  "Fuse nested scale reconstruction into SM103 4-bit dequantization", section
+    "Problem", names this path (the backward of the 4-bit matmul takes grad_A through the
+    dequantization), and section "B300 evidence plan" lists it as a public-path control for
+    training shapes.  At those M the weight is dequantized once per call and the GEMM
+    dominates; the line reports both the whole step and the dequantization alone.  The two
+    arms' dequantized weights and grad_A are checked equal bit for bit first."""
+    import torch
+
+    import quantized_weight_dequantization_gb300 as dq
+
+    dev = torch.device("cuda:0")
+    cells = []
+    for N, K in ((11008, 4096), (4096, 11008)):
+        wbytes = (N * K) // 2 + N * K // 64 + 4 * -(-(N * K // 64) // 256)
+        nsets = max(2, -(-(160 << 20) // wbytes) + 1)
+        p0 = gen.make_problem(N * K, 64, 256, "nf4", 1.0, 0.0371, seed=61)
+        sets = []
+        for i in range(nsets):
+            sets.append({k: torch.from_numpy(np.ascontiguousarray(getattr(p0, k))).to(dev)
+                         for k in ("packed", "scale_codes", "nested_absmax", "scale_codebook",
+                                   "value_codebook")})
+        nb = N * K // 64
+        scratch = torch.empty(nb, dtype=torch.float32, device=dev)
+        Wd = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
+        state = {"i": 0}
+
+        def nxt():
+            state["i"] = (state["i"] + 1) % nsets
+            return sets[state["i"]]
+
+        def deq_fused():
+            t = nxt()
+            dq.dq4_nested(t["packed"], t["scale_codes"], t["nested_absmax"], t["scale_codebook"],
+                          t["value_codebook"], float(p0.offset), N * K, 64, 256,
+                          torch.bfloat16, out=Wd.view(-1))
+
+        def deq_unfused():
+            t = nxt()
+            dq.dq4_nested_unfused(t["packed"], t["scale_codes"], t["nested_absmax"],
+                                  t["scale_codebook"], t["value_codebook"], float(p0.offset),
+                                  N * K, 64, 256, torch.bfloat16, out=Wd.view(-1),
+                                  scale_scratch=scratch)
+
+        for M in [int(x) for x in args.grad_m.split(",")]:
+            dY = torch.from_numpy(gen.make_normal_g(M, N, seed=62)).to(torch.bfloat16).to(dev)
+            GA = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+
+            def fused():
+                deq_fused()
+                torch.matmul(dY, Wd, out=GA)
+
+            def unfused():
+                deq_unfused()
+                torch.matmul(dY, Wd, out=GA)
+
+            fused()
+            torch.cuda.synchronize(dev)
+            w_f, g_f = Wd.clone(), GA.clone()
+            unfused()
+            torch.cuda.synchronize(dev)
+            if not (torch.equal(w_f.view(torch.int16), Wd.view(torch.int16)) and
+                    torch.equal(g_f.view(torch.int16), GA.view(torch.int16))):
+                raise SystemExit(f"fused and unfused grad_A differ at M={M} N={N} K={K}")
+            calls = 2 * nsets
+            t = {name: graph_time_us(fn, dev, args.warmup, args.steps, calls)
+                 for name, fn in (("fused", fused), ("unfused", unfused),
+                                  ("dequant_fused", deq_fused), ("dequant_unfused", deq_unfused))}
+            cells.append({"M": M, "N": N, "K": K, "fused_us": t["fused"],
+                          "unfused_us": t["unfused"], "speedup": t["unfused"] / t["fused"],
+                          "dequant_fused_us": t["dequant_fused"],
+                          "dequant_unfused_us": t["dequant_unfused"],
+                          "dequant_speedup": t["dequant_unfused"] / t["dequant_fused"]})
+        del sets, Wd, scratch
+    print(json.dumps({
+        "metric": "grad_A = dY W time: fused nested dequant + cuBLAS GEMM", "unit": "us",
+        "higher_is_better": False, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "grad_A = dY W, W = N x K NF4-style nested (bs 64, nested 256), "
+                               "BF16 dY and grad_A",
+                   "l2": "rotating weight sets of more bytes than L2",
+                   "timing": "CUDA-graph replay of back-to-back calls (host overhead "
+                             "excluded)"},
+        "cells": cells}), flush=True)
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
@@ -981,6 +1100,8 @@ def main():
         run_outprod(args)
     elif args.op == "linear":
         run_linear(args)
+    elif args.op == "grad_a":
+        run_grad_a(args)
     else:
         run_ours(args)
 
