@@ -94,7 +94,10 @@ __device__ __forceinline__ int swz(int rr, int ch) { return ch ^ ((rr >> 1) & 7)
 #define DQ4_T_MIN_CTAS 8
 #endif
 
-template <int OUT, bool kStoreVec>
+// kQuad (16-bit output, rows % 4 == 0, out 8-byte aligned): lanes 2q and 2q + 1 hold rows
+// 4q .. 4q + 3 of the tile between them; per two columns they swap one packed pair, so each
+// writes 8 bytes (4 rows) of one column: half the store instructions of pair stores.
+template <int OUT, bool kStoreVec, bool kQuad = false>
 __global__ void __launch_bounds__(kThreads, DQ4_T_MIN_CTAS)
     dq4_transposed_kernel(const Args a, int64_t rows, int64_t cols, uint32_t tiles_r) {
   __shared__ float s_vcb[16];
@@ -140,7 +143,8 @@ __global__ void __launch_bounds__(kThreads, DQ4_T_MIN_CTAS)
   const int wc = 64 * (w & 3);
   const int64_t ra = r0 + wr + 2 * lane;  // this lane's rows: ra, ra + 1
   const bool has0 = ra < rows, has1 = ra + 1 < rows;
-  if (!has0) return;
+  // (the quad path keeps every lane for its shuffles: a pair's rows are valid together)
+  if (!kQuad && !has0) return;
   const int64_t cbase = c0 + wc;
   const int ncol = int(cols - cbase < 64 ? cols - cbase : 64);
   if (ncol <= 0) return;
@@ -164,6 +168,25 @@ __global__ void __launch_bounds__(kThreads, DQ4_T_MIN_CTAS)
       // nibbles (values 0, 2, 4, 6 of the word) and the low ones (1, 3, 5, 7)
       const uint32_t h0 = (w0 >> 2) & 0x3C3C3C3Cu, l0 = (w0 << 2) & 0x3C3C3C3Cu;
       const uint32_t h1 = (w1 >> 2) & 0x3C3C3C3Cu, l1 = (w1 << 2) & 0x3C3C3C3Cu;
+      if constexpr (kQuad) {
+        const bool odd = lane & 1;
+#pragma unroll
+        for (int j = 0; j < 8; j += 2) {  // columns j (high nibbles) and j + 1 (low)
+          const uint32_t sel = 0x4440u + (j >> 1);
+          float v0, v1, u0, u1;
+          mul2_pair(lds_f32_t(vcb + __byte_perm(h0, 0, sel)),
+                    lds_f32_t(vcb + __byte_perm(h1, 0, sel)), sc2, v0, v1);
+          mul2_pair(lds_f32_t(vcb + __byte_perm(l0, 0, sel)),
+                    lds_f32_t(vcb + __byte_perm(l1, 0, sel)), sc2, u0, u1);
+          const uint32_t pj = pack2<OUT>(v0, v1), pj1 = pack2<OUT>(u0, u1);
+          const uint32_t got = __shfl_xor_sync(0xffffffffu, odd ? pj : pj1, 1);
+          // even lane: column j, rows ra .. ra + 3; odd lane: column j + 1, rows ra - 2 .. ra + 1
+          const uint2 val = odd ? make_uint2(got, pj1) : make_uint2(pj, got);
+          const int64_t at = odd ? o + rows - 2 : o;
+          if (has0) __stcs(reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + at), val);
+          o += 2 * rows;
+        }
+      } else {
 #pragma unroll
       for (int j = 0; j < 8; ++j) {  // value j of a word: byte j/2, high nibble first
         const uint32_t sel = 0x4440u + (j >> 1);
@@ -173,6 +196,7 @@ __global__ void __launch_bounds__(kThreads, DQ4_T_MIN_CTAS)
         mul2_pair(a0, a1, sc2, v0, v1);
         store_pair<OUT, kStoreVec>(a.out, o, v0, v1, has0, has1);
         o += rows;
+      }
       }
     }
   }
@@ -232,6 +256,10 @@ int launch_transposed(const Args& a, int64_t rows, int64_t cols, cudaStream_t st
     const int64_t grid = tiles_r * ((cols + kSC - 1) / kSC);
     if (grid > int64_t(UINT32_MAX)) return DQ4_ERR_N;  // 32-bit tile ids
     const uint32_t tr = uint32_t(tiles_r);
+    const bool quad = OUT != DQ4_OUT_F32 && rows % 4 == 0 &&
+                      reinterpret_cast<uintptr_t>(a.out) % 8 == 0;
+    if (quad)
+      return launch_kernel(dq4_transposed_kernel<OUT, true, true>, grid, stream, a, rows, cols, tr);
     if (sv) return launch_kernel(dq4_transposed_kernel<OUT, true>, grid, stream, a, rows, cols, tr);
     return launch_kernel(dq4_transposed_kernel<OUT, false>, grid, stream, a, rows, cols, tr);
   }

@@ -63,6 +63,9 @@ SHAPES = [
     (1, 1), (1, 8), (8, 1), (3, 5), (63, 65), (64, 64), (65, 64), (64, 72), (127, 129),
     (96, 40), (200, 8), (8, 200), (1, 4096), (4096, 1), (130, 1000), (1000, 130),
     (257, 264), (512, 4095), (4095, 512), (333, 777),
+    # rows % 4 == 0 and cols % 32 == 0 with partial row tiles: 16-bit outputs take the
+    # 8-byte (four-row) stores there
+    (100, 96), (260, 320), (4, 32), (132, 4096),
 ]
 
 
