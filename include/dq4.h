@@ -243,14 +243,17 @@ int dq4_nested_out_prod(const uint8_t* packed, const uint8_t* scale_codes,
  *   X, packed  16-byte aligned (both are read by TMA)
  *   workspace  optional device memory (NULL to skip), 256-byte aligned, of
  *              workspace_bytes bytes, zero-filled before its first use.  When
- *              there are fewer output tiles than SMs and workspace_bytes is at
- *              least dq4_nested_linear_workspace_bytes(M, N, K), the SMs share
- *              the tiles' K ranges: partial FP32 tiles meet in the workspace
- *              and are summed in K order (deterministic).  A completed call
- *              leaves its counters zero again, so it can be reused by later
- *              calls of any shape in the same stream (not by concurrent calls).  Without it each tile
- *              runs on one CTA; the result is the same up to FP32 summation
- *              order.
+ *              dq4_nested_linear_workspace_bytes(M, N, K) is nonzero (the tiles
+ *              would not fill the SMs in whole rounds and sharing them is
+ *              expected to be faster) and workspace_bytes is at least that,
+ *              one CTA runs per SM on an equal share of the (tile, K stage)
+ *              units: partial FP32 tiles meet in the workspace and are summed
+ *              in K order (deterministic).  Its size is bounded by the SM
+ *              count, not the problem.  A completed call leaves its counters
+ *              zero again, so it can be reused by later calls of any shape in
+ *              the same stream (not by concurrent calls).  Without it each
+ *              tile runs on one CTA; the result is the same up to FP32
+ *              summation order.
  *   bad        optional device int (NULL to skip): incremented by each part
  *              of a CTA that stopped because a bounded wait ran out (never
  *              expected; nonzero means Y is incomplete and the workspace must
