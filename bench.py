@@ -538,10 +538,33 @@ def cpu_baseline(p, cell, transposed: bool = False, repeats: int = 3):
             oracle.dq4_nested(p, cell.out, threads=threads)
         times.append(time.perf_counter() - t0)
     t = statistics.median(times)
-    return {"value": p.n / t, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"the whole {cell.name} workload ({p.n} values), median of {repeats} runs, "
-                      f"{threads} threads over nested-group-aligned chunks",
-            "gbs": cell.algorithmic_bytes() / t / 1e9}
+    out = {"value": p.n / t, "unit": UNIT, "cores": threads, "kind": "oracle",
+           "sample": f"the whole {cell.name} workload ({p.n} values), median of {repeats} runs, "
+                     f"{threads} threads over nested-group-aligned chunks",
+           "gbs": cell.algorithmic_bytes() / t / 1e9}
+    if not transposed:
+        # one thread, on a prefix of whole nested groups (bounded: 2^24 values)
+        unit = p.blocksize * p.nested_blocksize
+        n1 = max(unit, min(p.n, 1 << 24) // unit * unit) if p.n >= unit else p.n
+        p1 = gen.Problem(p.packed[:(n1 + 1) // 2], p.scale_codes[:-(-n1 // p.blocksize)],
+                         p.nested_absmax[:-(-n1 // unit)], p.scale_codebook, p.value_codebook,
+                         p.offset, n1, p.blocksize, p.nested_blocksize)
+        t1 = []
+        for _ in range(repeats):
+            t0 = time.perf_counter()
+            oracle.dq4_nested(p1, cell.out, threads=1)
+            t1.append(time.perf_counter() - t0)
+        out["single_thread"] = {"value": n1 / statistics.median(t1), "unit": UNIT,
+                                "sample": f"the first {n1} values of {cell.name}, median of "
+                                          f"{repeats} runs, one thread"}
+    try:
+        info = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        model = next((ln.split(":", 1)[1].strip() for ln in info.splitlines()
+                      if ln.startswith("Model name")), None)
+    except (OSError, subprocess.SubprocessError):
+        model = None
+    out["cpu_model"] = model
+    return out
 
 
 # ------------------------------------------------------- reference arm
