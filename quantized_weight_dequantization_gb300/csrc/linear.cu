@@ -486,11 +486,10 @@ __global__ void __launch_bounds__(kLinThreads, 1)
     if (p.bad) atomicAdd(p.bad, 1);
   };
 
-#if DQ4_PDL
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;");
-#endif
-  for (int k = tid; k < 256; k += kLinThreads) s_scb[k] = __ldg(p.w.scb + k);
+  // The setup below touches no global memory (the tensor maps are kernel parameters), so
+  // under programmatic dependent launch it overlaps the previous kernel in the stream;
+  // every global read comes after griddepcontrol.wait.  (Two CTAs of this kernel never
+  // share an SM: each takes more than half its shared memory, so the TMEM is free.)
   if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                  :: "r"(smem_u32(&s_tmem)), "r"(kTmemCols));
@@ -523,6 +522,10 @@ __global__ void __launch_bounds__(kLinThreads, 1)
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = s_tmem;
+#if DQ4_PDL
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+#endif
 
   if (warp == kRawWarp) {
     if (lane == 0) {
@@ -670,6 +673,8 @@ __global__ void __launch_bounds__(kLinThreads, 1)
     // g = word 16 b + g holds vcb[b >> 4], vcb[b & 15]); named barrier 2 over the producer
     // threads orders it before their first lookup.
     {
+      static_assert(kProducerWarps * 32 >= 256, "the producers load the scale codebook");
+      if (tid < 256) s_scb[tid] = __ldg(p.w.scb + tid);
       const float v = __ldg(p.w.vcb + (lane & 15));
       for (int i = tid; i < 256 * 16; i += kProducerWarps * 32) {
         const int b = i >> 4;
