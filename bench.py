@@ -47,6 +47,14 @@ import dq4_inputs as gen  # noqa: E402
 METRIC = "dequantized elements/s and effective HBM GB/s vs GB300 peak (1 GPU)"
 UNIT = "elements/s"
 DEFAULT_CELL = "C4a"
+# Every cell of the >= 80 % bar (the >= 4096x11008 weights: C3, C4, and C5 at each block size,
+# whose four offsets change arithmetic, not traffic, so each block size is timed at one of
+# them) and the smaller C1 / C2 cells, timed one by one for the `cells` record.
+DEFAULT_CELLS = (["C1", "C2a", "C2b", "C3a", "C3b", "C3c", "C3d", "C4b", "C4c", "C4d"]
+                 + [f"C5-bs{bs}-off{off:+g}" for bs, off in
+                    zip((32, 64, 128, 256, 512, 1024, 2048, 4096),
+                        (-1.0, -1e-3, 1e-3, 1.0, -1.0, -1e-3, 1e-3, 1.0))])
+BAR_CELL_PREFIXES = ("C3", "C4", "C5")
 N_SETS = 3
 FALLBACK_HBM_GBS = 6800.0
 # the sources of the flat dequantization kernels (the ncu traffic record is tied to them)
@@ -63,7 +71,7 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cell", default=DEFAULT_CELL, choices=sorted(gen.CELLS))
     ap.add_argument("--op", choices=["nested", "transposed", "int8prep", "outprod", "linear",
-                                     "grad_a"],
+                                     "grad_a", "pair"],
                     default="nested",
                     help="nested: dq4_nested (flat output); transposed: dq4_nested_transposed "
                          "(W^T output of the rows x cols weight); int8prep: LLM.int8 "
@@ -90,6 +98,8 @@ def parse_args():
                     help="rotating device buffer sets (each larger than L2)")
     ap.add_argument("--isolated-launches", type=int, default=100,
                     help="launches timed one by one (own event pair) after the timed region")
+    ap.add_argument("--cells", default=",".join(DEFAULT_CELLS),
+                    help="cells timed one by one into the `cells` record (empty: none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-compare", action="store_true")
@@ -243,6 +253,26 @@ class ClockSampler:
                 "power_w_max": max(power) if power else None}
 
 
+def cell_config(cell, op: str, world: int, n_sets: int) -> dict:
+    """The workload description both arms print (same dict, so the two lines compare)."""
+    transposed = op == "transposed"
+    alg_bytes = cell.algorithmic_bytes()
+    return {
+        "workload": f"{cell.rows}x{cell.cols} {cell.fmt.upper()}-style nested 4-bit dequant, "
+                    f"blocksize {cell.blocksize}, nested blocksize {cell.nested_blocksize}, "
+                    f"{cell.out.upper()} out ({cell.name})"
+                    + (", transposed output" if transposed else ""),
+        "op": op,
+        "n_values": cell.n, "blocksize": cell.blocksize,
+        "nested_blocksize": cell.nested_blocksize, "format": cell.fmt,
+        "out_dtype": cell.out, "offset": cell.offset,
+        "algorithmic_bytes_per_step": alg_bytes,
+        "l2": f"inputs larger than L2: {alg_bytes / 1e6:.1f} MB per step, {n_sets} rotating "
+              "buffer sets",
+        "parallelism": f"replicas x{world}",
+    }
+
+
 # -------------------------------------------------------------- our arm
 def run_ours(args):
     import torch
@@ -327,15 +357,10 @@ def run_ours(args):
                                             else torch.int32))):
         raise SystemExit("fused and unfused outputs differ; refusing to time")
 
-    # ---- warm-up, then exactly K timed steps
+    # ---- warm-up, then exactly K timed steps.  The clock sampler starts first (it takes
+    # half a second to come up), so the warm-up launches run right before the timed region
+    # and the GPU does not idle in between.
     K, W = args.steps, args.warmup
-    for i in range(W):
-        if fused(i):
-            raise SystemExit("dq4_nested failed in warm-up")
-    # batch boundaries (>= 7 batches); the launches run back to back
-    nb = max(1, min(K, max(7, min(20, K // 50))))
-    edges = sorted(set(np.linspace(0, K, nb + 1).astype(int).tolist()))
-    ev_b = {e: torch.cuda.Event(enable_timing=True) for e in edges}
     gpu_uuid = None
     try:
         u = str(torch.cuda.get_device_properties(dev).uuid)
@@ -345,6 +370,13 @@ def run_ours(args):
     clocks = None if args.no_clocks else ClockSampler(gpu_uuid)
     if clocks:
         clocks.start()
+    for i in range(W):
+        if fused(i):
+            raise SystemExit("dq4_nested failed in warm-up")
+    # batch boundaries (>= 7 batches); the launches run back to back
+    nb = max(1, min(K, max(7, min(20, K // 50))))
+    edges = sorted(set(np.linspace(0, K, nb + 1).astype(int).tolist()))
+    ev_b = {e: torch.cuda.Event(enable_timing=True) for e in edges}
     torch.cuda.synchronize(dev)
     barrier()
     torch.cuda.synchronize(dev)
@@ -448,6 +480,10 @@ def run_ours(args):
             raise SystemExit("e2e output mismatch")
 
     peak, peak_kind = read_peaks()
+    # the host link alone for the e2e step's bytes, and every listed cell timed on its own
+    link = link_bound(h2d, d2h, dev) if e2e_ms is not None else None
+    names = [c for c in args.cells.split(",") if c]
+    cells_rec = time_cells(names, dev, stream, transposed, peak) if names else None
     ms_per_step = elapsed_ms / K
     value = whole_job_rate(world, K * n, elapsed_ms)
     achieved_gbs = alg_bytes / (avg_launch_ms / 1e3) / 1e9
@@ -463,22 +499,9 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f32",
+        "dtype": cell.out,
         "data": "synthetic (seeded splitmix64 codes, lognormal nested absmax)",
-        "config": {
-            "workload": f"{cell.rows}x{cell.cols} {cell.fmt.upper()}-style nested 4-bit dequant, "
-                        f"blocksize {cell.blocksize}, nested blocksize {cell.nested_blocksize}, "
-                        f"{cell.out.upper()} out ({cell.name})"
-                        + (", transposed output" if transposed else ""),
-            "op": args.op,
-            "n_values": n, "blocksize": cell.blocksize,
-            "nested_blocksize": cell.nested_blocksize, "format": cell.fmt,
-            "out_dtype": cell.out, "offset": cell.offset,
-            "algorithmic_bytes_per_step": alg_bytes,
-            "l2": f"inputs larger than L2: {alg_bytes / 1e6:.1f} MB per step, {n_sets} rotating "
-                  "buffer sets",
-            "parallelism": f"replicas x{world}",
-        },
+        "config": cell_config(cell, args.op, world, n_sets),
         "effective_gbs": alg_bytes / (ms_per_step / 1e3) / 1e9,
         "roofline": {
             "bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
@@ -509,7 +532,12 @@ def run_ours(args):
         "e2e": None if e2e_ms is None else {
             "value": whole_job_rate(world, E * n, e2e_ms), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": E,
-            "ms_per_step": e2e_ms / E},
+            "ms_per_step": e2e_ms / E,
+            # the roofline of this leg is the host link: the step's copies alone, both
+            # directions at once, against the whole step
+            "link_gbs": link, "link_bound_ms": link["both_directions_ms"],
+            "frac": link["both_directions_ms"] / (e2e_ms / E)},
+        "cells": cells_rec,
         "gpu_launches": K,
         "clocks": clk,
         "wall_s_timed": wall,
@@ -520,6 +548,137 @@ def run_ours(args):
     ranks.close()
     if rank == 0:
         print(json.dumps(out), flush=True)
+
+
+def time_cells(names, dev, stream, transposed: bool, peak: float, batches: int = 7):
+    """Each named cell timed like the main step: back-to-back launches on `stream` over
+    rotating buffer sets (together more than twice the L2, so no launch finds its inputs
+    there), >= 20 warm-up launches, then `batches` batches of >= 2 ms each; per call the
+    median, p10 and p90 over the batches, the effective GB/s and its fraction of `peak`."""
+    import torch
+
+    import quantized_weight_dequantization_gb300 as dq
+
+    L = dq.lib
+    sh = stream.cuda_stream
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 << 20))
+    codes = {"f16": dq.OUT_F16, "bf16": dq.OUT_BF16, "f32": dq.OUT_F32}
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+    rec = {}
+    for name in names:
+        cell = gen.CELLS[name]
+        p = cell.problem()
+        alg = cell.algorithmic_bytes()
+        n_sets = max(3, -(-2 * l2 // alg) + 1)
+        first = {k: torch.from_numpy(np.ascontiguousarray(getattr(p, k))).to(dev)
+                 for k in ("packed", "scale_codes", "nested_absmax")}
+        scb = torch.from_numpy(p.scale_codebook).to(dev)
+        vcb = torch.from_numpy(p.value_codebook).to(dev)
+        sets = [{k: (v if i == 0 else v.clone()) for k, v in first.items()}
+                for i in range(n_sets)]
+        for s in sets:
+            s["out"] = torch.empty(p.n, dtype=tdt[cell.out], device=dev)
+        ptrs = [(s["packed"].data_ptr(), s["scale_codes"].data_ptr(),
+                 s["nested_absmax"].data_ptr(), s["out"].data_ptr()) for s in sets]
+        off, bs, nbs, code = float(p.offset), p.blocksize, p.nested_blocksize, codes[cell.out]
+
+        def call(i):
+            pk, cd, am, o = ptrs[i % n_sets]
+            if transposed:
+                return L.dq4_nested_transposed(pk, cd, am, scb.data_ptr(), vcb.data_ptr(), off,
+                                               cell.rows, cell.cols, bs, nbs, code, o, sh)
+            return L.dq4_nested(pk, cd, am, scb.data_ptr(), vcb.data_ptr(), off, p.n, bs, nbs,
+                                code, o, sh)
+
+        est_us = alg / (peak * 1e3)
+        iters = max(20, int(2000.0 / est_us) + 1)
+        for i in range(max(20, n_sets)):
+            if call(i):
+                raise SystemExit(f"{name}: launch failed")
+        torch.cuda.synchronize(dev)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(batches + 1)]
+        j = 0
+        for b in range(batches):
+            ev[b].record(stream)
+            for _ in range(iters):
+                call(j)
+                j += 1
+        ev[batches].record(stream)
+        torch.cuda.synchronize(dev)
+        us = [ev[b].elapsed_time(ev[b + 1]) / iters * 1e3 for b in range(batches)]
+        med = pct(us, 50)
+        gbs = alg / (med * 1e-6) / 1e9
+        rec[name] = {"us": round(med, 3), "p10_us": round(pct(us, 10), 3),
+                     "p90_us": round(pct(us, 90), 3), "gbs": round(gbs, 1),
+                     "frac": round(gbs / peak, 4), "in_bar": name.startswith(BAR_CELL_PREFIXES),
+                     "algorithmic_bytes": alg, "sets": n_sets, "calls_per_batch": iters,
+                     "batches": batches}
+        del sets, first
+    bar = [v["frac"] for v in rec.values() if v["in_bar"]]
+    return {"cells": rec, "bar_min_frac": min(bar) if bar else None,
+            "protocol": f"per cell: rotating buffer sets (> 2x L2 in all), >= 20 warm-up "
+                        f"launches, {batches} batches of >= 2 ms of back-to-back launches, "
+                        f"median / p10 / p90 per call over the batches"}
+
+
+def link_bound(h2d_bytes: int, d2h_bytes: int, dev, reps: int = 5):
+    """The host link alone for one e2e step's byte counts: one pinned H2D and one pinned
+    D2H cudaMemcpyAsync timed apart (GB/s) and at once on two streams (ms, the e2e step's
+    floor: its pipeline overlaps the two directions)."""
+    import torch
+
+    hin = torch.empty(h2d_bytes, dtype=torch.uint8).pin_memory()
+    din = torch.empty(h2d_bytes, dtype=torch.uint8, device=dev)
+    dout = torch.empty(d2h_bytes, dtype=torch.uint8, device=dev)
+    hout = torch.empty(d2h_bytes, dtype=torch.uint8).pin_memory()
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def timed(h2d: bool, d2h: bool) -> float:
+        ts = []
+        for _ in range(reps + 1):
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
+            if h2d:
+                with torch.cuda.stream(s1):
+                    din.copy_(hin, non_blocking=True)
+            if d2h:
+                with torch.cuda.stream(s2):
+                    hout.copy_(dout, non_blocking=True)
+            torch.cuda.synchronize(dev)
+            ts.append(time.perf_counter() - t0)
+        return statistics.median(ts[1:]) * 1e3
+
+    t_in, t_out, t_both = timed(True, False), timed(False, True), timed(True, True)
+    return {"h2d_gbs": round(h2d_bytes / (t_in * 1e-3) / 1e9, 1),
+            "d2h_gbs": round(d2h_bytes / (t_out * 1e-3) / 1e9, 1),
+            "both_directions_ms": round(t_both, 4)}
+
+
+def run_pair(args):
+    """One fused call and one unfused sequence per step, untimed, for a profiler's launch
+    list: `--warmup` pairs, then `--steps` pairs (1 + 3 launches each)."""
+    import torch
+
+    import quantized_weight_dequantization_gb300 as dq
+
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    cell = gen.CELLS[args.cell]
+    p = cell.problem()
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[cell.out]
+    t = {k: torch.from_numpy(np.ascontiguousarray(getattr(p, k))).to(dev)
+         for k in ("packed", "scale_codes", "nested_absmax", "scale_codebook", "value_codebook")}
+    out = torch.empty(p.n, dtype=tdt, device=dev)
+    scratch = torch.empty(p.nblocks, dtype=torch.float32, device=dev)
+    args_ = (t["packed"], t["scale_codes"], t["nested_absmax"], t["scale_codebook"],
+             t["value_codebook"], float(p.offset), p.n, p.blocksize, p.nested_blocksize, tdt)
+    for _ in range(args.warmup + args.steps):
+        dq.dq4_nested(*args_, out=out)
+        dq.dq4_nested_unfused(*args_, out=out, scale_scratch=scratch)
+    torch.cuda.synchronize(dev)
+    print(json.dumps({"op": "pair", "cell": cell.name, "pairs": args.warmup + args.steps,
+                      "launches_per_pair": {"fused": 1, "unfused": 3},
+                      "scale_scratch_bytes": p.nblocks * 4}), flush=True)
 
 
 # --------------------------------------------------------- CPU baseline
@@ -614,12 +773,9 @@ def run_reference(args):
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": el / K * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "scaling": "weak", "vs_baseline": None, "dtype": cell.out,
         "data": "synthetic (seeded splitmix64 codes, lognormal nested absmax)",
-        "config": {"workload": f"{cell.rows}x{cell.cols} {cell.fmt.upper()}-style nested 4-bit "
-                               f"dequant, blocksize {cell.blocksize}, nested blocksize "
-                               f"{cell.nested_blocksize}, {cell.out.upper()} out ({cell.name})",
-                   "n_values": p.n},
+        "config": cell_config(cell, args.op, world, max(1, args.sets)),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -1125,6 +1281,8 @@ def main():
         run_linear(args)
     elif args.op == "grad_a":
         run_grad_a(args)
+    elif args.op == "pair":
+        run_pair(args)
     else:
         run_ours(args)
 

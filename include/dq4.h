@@ -149,8 +149,8 @@ int dq4_nested_unfused(const uint8_t* packed, const uint8_t* scale_codes,
  * memory is handed out only by its own pool, or an allocator's own hook,
  * which must not re-enter the allocator.  This entry point allocates
  * nothing: the FP32 scale scratch is a fixed array inside the library.
- * The paper (issue #21) has no counterpart of this entry point; it only
- * repackages the unfused sequence above.
+ * No source page has a counterpart of this entry point; it only repackages
+ * the unfused sequence above.
  *
  * Arguments, layout and results are those of dq4_nested_unfused, without
  * `scale_scratch`; the output is bit-identical.
@@ -162,7 +162,10 @@ int dq4_nested_unfused(const uint8_t* packed, const uint8_t* scale_codes,
  *     process exits.
  *   - The first call on each device looks up the array's device address
  *     (once per device, with that device current).  Make that first call
- *     before any stream capture begins.
+ *     before any stream capture begins.  The address is kept until the
+ *     process exits; after cudaDeviceReset the array may be loaded at
+ *     another address, so calls after a reset of the device are not
+ *     supported.
  *   - All calls share the one array, and each call overwrites the part it
  *     uses before reading it (nothing has to start at zero).  Calls that
  *     overlap on the GPU (on different streams, or from different host

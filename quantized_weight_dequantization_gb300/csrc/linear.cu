@@ -488,8 +488,10 @@ __global__ void __launch_bounds__(kLinThreads, 1)
 
   // The setup below touches no global memory (the tensor maps are kernel parameters), so
   // under programmatic dependent launch it overlaps the previous kernel in the stream;
-  // every global read comes after griddepcontrol.wait.  (Two CTAs of this kernel never
-  // share an SM: each takes more than half its shared memory, so the TMEM is free.)
+  // every global read comes after griddepcontrol.wait.  Two CTAs of this kernel never
+  // share an SM (each takes more than half its shared memory), so when the previous
+  // kernel is this one the TMEM is free; after another kernel that holds TMEM on this SM,
+  // the allocation waits until that kernel releases it.
   if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                  :: "r"(smem_u32(&s_tmem)), "r"(kTmemCols));

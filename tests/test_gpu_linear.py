@@ -292,3 +292,77 @@ def test_graph_capture_and_replay(dq):
         torch.cuda.synchronize()
         want = oracle.linear(p, x_bits(X), "bf16", N, K, threads=16)
         assert np.array_equal(Y.double().cpu().numpy(), want), seed
+
+
+# ---- the decoded weight operand itself, bit for bit ("Correctness requirements": the
+# dequantized tensor passes bitwise equality before any GEMM tolerance).  Activation rows
+# that are unit vectors e_k make each entry of Y = X W^T one weight, w[n, k] * 1, plus
+# products with exact zeros: the FP32 accumulator holds w exactly whatever the summation
+# order, so Y^T must equal dq4_nested's output for X's dtype bit for bit.  The one thing a
+# GEMM cannot show is the sign of a zero weight (its +0 and -0 terms may sum to +0), so a
+# zero weight must give a zero of either sign.  Every k is covered at every M below, so
+# every activation-tile width the planner picks decodes the whole weight, on the split
+# path (cached workspace) and on whole tiles (no workspace).
+OPERAND_CASES = [
+    # fmt, absmax sigma, offset, blocksize, nested blocksize, X dtype, N, K, Ms
+    ("nf4", 1.0, 0.0371, 64, 256, "bf16", 11008, 4096, (16, 32, 64, 128, 256, 4096)),
+    ("fp4", 0.5, -0.52, 64, 256, "f16", 11008, 4096, (16, 32, 64, 128, 256, 4096)),
+    ("nf4", 0.5, -0.0371, 32, 256, "f16", 4860, 1216, (16, 64, 1216)),    # per-K-step codes
+    ("fp4", 1.0, 0.52, 4096, 256, "bf16", 4700, 2048, (16, 128, 2048)),  # blocks span rows
+    ("nf4", 0.5, 0.52, 128, 256, "bf16", 2000, 4096, (32, 256)),
+    ("fp4", 0.5, -0.0371, 1024, 1, "f16", 3000, 1024, (16, 64, 1024)),
+    ("nf4", 1.0, -0.52, 256, 64, "bf16", 1111, 2048, (48, 300)),
+]
+
+
+def _f32_bits_of(bits16: np.ndarray, xin: str) -> np.ndarray:
+    """FP32 bit patterns of 16-bit values (both conversions are exact)."""
+    if xin == "bf16":
+        return (bits16.astype(np.uint32) << 16).view(np.int32)
+    return bits16.view(np.float16).astype(np.float32).view(np.int32)
+
+
+def _nonzero_bits(t: torch.Tensor, int_dtype) -> torch.Tensor:
+    """Raw bits with both zeros mapped to +0 (float view t, integer view of the same width)."""
+    return torch.where(t == 0, torch.zeros((), dtype=int_dtype, device=t.device),
+                       t.view(int_dtype))
+
+
+@pytest.mark.parametrize("case", OPERAND_CASES, ids=lambda c: f"{c[0]}-bs{c[3]}-nbs{c[4]}-"
+                         f"{c[5]}-{c[6]}x{c[7]}")
+def test_weight_operand_bits_with_unit_activations(dq, case):
+    fmt, sigma, offset, bs, nbs, xin, N, K, Ms = case
+    p = gen.make_problem(N * K, bs, nbs, fmt, sigma, offset, seed=N + bs + nbs)
+    w16 = oracle.dq4_nested(p, xin, threads=16)
+    want32 = torch.from_numpy(_f32_bits_of(w16, xin).reshape(N, K)).to(DEV).t().contiguous()
+    want16 = torch.from_numpy(w16.view(np.int16).reshape(N, K)).to(DEV).t().contiguous()
+    want32 = torch.where(want32.view(torch.float32) == 0, torch.zeros_like(want32), want32)
+    want16 = _nonzero_bits(want16.view(TDT[xin]), torch.int16)
+    t = {k: torch.from_numpy(np.ascontiguousarray(getattr(p, k))).to(DEV)
+         for k in ("packed", "scale_codes", "nested_absmax", "scale_codebook", "value_codebook")}
+    order = torch.from_numpy(np.argsort(gen.splitmix64(K, 77, K), kind="stable")).to(DEV)
+    none = torch.empty(0, dtype=torch.uint8, device=DEV)
+    split_seen = False
+    for M in Ms:
+        split_seen |= dq.lib.dq4_nested_linear_workspace_bytes(M, N, K) > 0
+        for ws in (None, none):  # cached workspace (split when it pays) / whole tiles
+            bad = torch.zeros(1, dtype=torch.int32, device=DEV)
+            Yt = torch.empty((K, N), dtype=torch.float32, device=DEV)
+            Yt16 = torch.empty((K, N), dtype=TDT[xin], device=DEV)
+            for k0 in range(0, K, M):
+                ks = order[k0:k0 + M]  # M distinct k (the last slice may be shorter)
+                X = torch.zeros((ks.numel(), K), dtype=TDT[xin], device=DEV)
+                X[torch.arange(ks.numel(), device=DEV), ks] = 1
+                args = (X, t["packed"], t["scale_codes"], t["nested_absmax"],
+                        t["scale_codebook"], t["value_codebook"], float(p.offset), N, bs, nbs)
+                Yt[ks] = dq.linear(*args, out_dtype=torch.float32, bad=bad, workspace=ws)
+                Yt16[ks] = dq.linear(*args, out_dtype=TDT[xin], bad=bad, workspace=ws)
+            torch.cuda.synchronize()
+            got32 = _nonzero_bits(Yt, torch.int32)
+            got16 = _nonzero_bits(Yt16, torch.int16)
+            ne = int((got32 != want32).sum().item())
+            assert ne == 0, (M, ws is None, ne)
+            assert torch.equal(got16, want16), (M, ws is None)
+            assert int(bad.item()) == 0
+    if N == 11008:
+        assert split_seen  # the decode sizes take the split path at this shape
