@@ -18,11 +18,14 @@
 // stored at once, and a tile shared by several CTAs is summed from their FP32
 // partials, in K order, by the last of them to finish (no CTA waits for
 // another).
-// Eleven warps:
-//  * warp 9 (lane 0): streams the packed weight rows of each stage's tile with
+// Warps 0..7 dequantize, then 1 or 2 MMA-issuing warps (I, below), then the two TMA
+// warps: 12 warps for narrow tiles (BX <= 64), 11 for wide ones.
+//  * warp 8 + I (lane 0): streams the packed weight rows of each stage's tile with
 //    TMA into a ring of raw stages (four 128-row x 64-value boxes, 4 KB each,
-//    32-byte swizzled), as far ahead as the ring allows;
-//  * warp 10 (lane 0): streams the activation tiles (BX rows x 64 K per K step,
+//    32-byte swizzled), as far ahead as the ring allows, once the dequantizing
+//    warps have issued their first scale-code loads (which would otherwise queue
+//    behind these copies in DRAM);
+//  * warp 9 + I (lane 0): streams the activation tiles (BX rows x 64 K per K step,
 //    128-byte swizzle, rows past M zero-filled) into their own ring, a whole
 //    stage per slot for narrow tiles;
 //  * warps 0..7, two groups of four that take alternate weight stages (so one
@@ -38,10 +41,13 @@
 //    with one tcgen05.st; afterwards
 //    warps 0..7 run the epilogue: tcgen05.ld of each segment's accumulator,
 //    conversion, stores of Y (or of a partial tile, and the shared tiles' sums);
-//  * warp 8: allocates the TMEM; lane 0 issues tcgen05.mma (A = weights from
-//    TMEM, B = activations from shared memory, M = 128, N = BX, K = 16) for
-//    each K step and commits the weight and activation slots back to their
-//    producers.
+//  * warps 8 .. 8 + I - 1: warp 8 allocates the TMEM; lane 0 of each issues
+//    tcgen05.mma (A = weights from TMEM, B = activations from shared memory,
+//    M = 128, N = BX, K = 16) and commits the weight and activation slots back to
+//    their producers.  A tcgen05.mma holds its issuing thread about 120 cycles
+//    whatever N is, so a single issuer would pace narrow tiles; with I = 2, issuer
+//    i takes the stages producer group i decodes, into accumulators of its own,
+//    and the read-out adds the two partial sums in a fixed order.
 // Every W value is computed exactly as dq4_nested does, so the GEMM consumes
 // the same operand bits as "dequantize, then F.linear".  Waits on mbarriers
 // are bounded; a wait that runs out counts into *bad, raises a CTA-wide abort
@@ -70,10 +76,17 @@ static_assert(kGroupWarps == 4 || kGroupWarps == 8 || kGroupWarps == 16, "whole 
 constexpr int kTPR = kGroupWarps / 4;              // producer threads per weight row
 constexpr int kWords = 8 / kTPR;                   // packed 32-bit words per thread and K step
 constexpr int kHalves = kWords >= 8 ? 2 : 1;       // 32-value halves per thread and K step
-constexpr int kMmaWarp = kProducerWarps;           // also allocates TMEM
-constexpr int kRawWarp = kProducerWarps + 1;       // weight TMA
-constexpr int kXWarp = kProducerWarps + 2;         // activation TMA
-constexpr int kLinThreads = 32 * (kProducerWarps + 3);
+constexpr int kMmaWarp = kProducerWarps;           // the first MMA warp; also allocates TMEM
+// MMA-issuing warps.  A tcgen05.mma holds its issuing thread about 120 cycles whatever its N
+// (measured on GB300 for N = 16 .. 128, A from TMEM or shared memory), while two issuing
+// threads in different warps overlap: narrow tiles, whose MMAs carry few FLOPs, issue from
+// two threads, each into accumulators of its own.
+__host__ __device__ constexpr int kIssOf(int bx) { return bx <= 64 ? 2 : 1; }
+__host__ __device__ constexpr int kRawWarpOf(int bx) { return kProducerWarps + kIssOf(bx); }
+__host__ __device__ constexpr int kXWarpOf(int bx) { return kProducerWarps + kIssOf(bx) + 1; }
+__host__ __device__ constexpr int kThreadsOf(int bx) {
+  return 32 * (kProducerWarps + kIssOf(bx) + 2);
+}
 constexpr int kBW = 128;           // weight rows per CTA = MMA M = TMEM lanes
 constexpr int kBK = 64;            // 64 16-bit values = one 128-byte swizzle row
 constexpr int kRawBytes = kBW * kBK / 2;  // one raw stage: 128 rows x 32 packed bytes
@@ -131,6 +144,16 @@ __device__ __forceinline__ bool mbar_try2(uint32_t bar_a, uint32_t par_a, uint32
       : "=r"(done) : "r"(bar_a), "r"(par_a), "r"(bar_b), "r"(par_b), "r"(kSuspendNs)
       : "memory");
   return done != 0;
+}
+
+// Add v to *p and return the old value, with release and acquire semantics at GPU scope:
+// the writes ordered before it are visible to whoever acquires a later value of *p, and
+// the writes released with earlier values are visible after it.
+__device__ __forceinline__ int atomic_add_acq_rel(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;"
+               : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
 }
 
 __device__ __forceinline__ uint64_t global_ns() {
@@ -329,10 +352,11 @@ __host__ __device__ __forceinline__ uint32_t split_begin(uint32_t c, const LinAr
 #endif
 constexpr int kSub = DQ4_LIN_SUB;         // 64-value K steps per weight stage
 constexpr uint32_t kTmemCols = 512;       // the whole TMEM of the SM
-// Accumulator buffers: two for narrow tiles (a segment accumulates while the previous
-// one is read out), one of BX columns otherwise.  They take columns 0 .. kATmem(BX) - 1,
-// the weight ring the rest: kAS(BX) stages.
-__host__ __device__ constexpr int kAccOf(int bx) { return bx <= 64 ? 2 : 1; }
+// Accumulator buffers per MMA issuer: two for the narrowest tiles (a segment accumulates
+// while the previous one is read out), one of BX columns otherwise.  Issuer i's buffer b
+// is columns (i kAcc + b) BX ..; all of them lie in columns 0 .. kATmem(BX) - 1, the weight
+// ring in the rest: kAS(BX) stages.
+__host__ __device__ constexpr int kAccOf(int bx) { return bx <= 32 ? 2 : 1; }
 __host__ __device__ constexpr uint32_t kATmem(int bx) { return bx <= 128 ? 128u : 256u; }
 __host__ __device__ constexpr int kASOf(int bx) {
   return int((kTmemCols - kATmem(bx)) / 32) / kSub;
@@ -340,9 +364,10 @@ __host__ __device__ constexpr int kASOf(int bx) {
 template <int BX>
 struct LinSmem {
   static constexpr int kAS = kASOf(BX);              // weight stages in TMEM
-  static constexpr int kAcc = kAccOf(BX);            // accumulator buffers
+  static constexpr int kAcc = kAccOf(BX);            // accumulator buffers per issuer
+  static constexpr int kIss = kIssOf(BX);            // MMA-issuing threads
   static_assert(kAS >= 2, "double-buffered weight ring");
-  static_assert(kAcc * BX <= int(kATmem(BX)), "accumulators fit before the weight ring");
+  static_assert(kIss * kAcc * BX <= int(kATmem(BX)), "accumulators fit before the weight ring");
   // mbarrier waits test a phase's parity, so a waiter must never be two phases ahead
   // of the barrier.  A group at stage i waits for the MMAs of stage i - kAS and knows,
   // from its previous wait, that those of stage i - kGroups - kAS completed (MMAs
@@ -352,10 +377,12 @@ struct LinSmem {
   static constexpr int kRawSlot = kSub * kRawBytes;
   static constexpr int kB = BX * kBK * 2;           // one K step of activations
   // K steps per activation slot: a whole stage for narrow tiles (one wait and one
-  // release per stage for the MMA thread), one K step for wide ones
-  static constexpr int kXSub = BX <= 32 ? kSub : 1;
+  // release per stage for an MMA thread, and stage l's slot is l % kXS), one K step for
+  // wide ones
+  static constexpr int kXSub = BX <= 64 ? kSub : 1;
+  static_assert(kIss == 1 || kXSub == kSub, "several issuers take whole-stage slots");
   static constexpr int kXSlot = kXSub * kB;
-  static constexpr int kXS = BX <= 32 ? 3 : BX == 64 ? 8 : BX == 128 ? 6 : 4;  // slots
+  static constexpr int kXS = BX <= 64 ? 3 : BX == 128 ? 6 : 4;  // slots
   // The codebook as a byte-indexed pair table: entry b holds (vcb[b >> 4], vcb[b & 15]),
   // the two values of a packed byte, as 8 bytes, replicated 16 times so that lane l reads
   // copy l % 16: each half warp's 8-byte loads then fall in 16 distinct bank pairs
@@ -374,7 +401,8 @@ struct LinSmem {
   static constexpr int kTabOff = kRawOff + kRawS * kRawSlot;
   static constexpr int kBarOff = kTabOff + kTabBytes;
   // full_w, empty_a per weight stage; full_x, empty_x per activation stage;
-  // raw_full, raw_empty per raw stage; acc_full, acc_empty per accumulator; acc_done
+  // raw_full, raw_empty per raw stage; acc_full, acc_empty per accumulator buffer (shared
+  // by the issuers); acc_done
   static constexpr int kBars = 2 * kAS + 2 * kXS + 2 * kRawS + 2 * kAcc + 1;
   static constexpr int kBytes = kBarOff + 8 * kBars + 1024;  // + alignment slack
   // with the kernel's static shared memory (the scale codebook and a few words)
@@ -399,11 +427,12 @@ struct RingPos {
 };
 
 template <int BX, bool kBF16>
-__global__ void __launch_bounds__(kLinThreads, 1)
+__global__ void __launch_bounds__(kThreadsOf(BX), 1)
     dq4_linear_kernel(const __grid_constant__ CUtensorMap tmap_x,
                       const __grid_constant__ CUtensorMap tmap_w, const LinArgs p) {
   using S = LinSmem<BX>;
-  constexpr int kAS = S::kAS, kXS = S::kXS, kRawS = S::kRawS, kAcc = S::kAcc;
+  constexpr int kAS = S::kAS, kXS = S::kXS, kRawS = S::kRawS, kAcc = S::kAcc, kIss = S::kIss;
+  constexpr int kRawWarp = kRawWarpOf(BX), kXWarp = kXWarpOf(BX);
   constexpr uint32_t kATmemCol = kATmem(BX);
   constexpr int kOut = kBF16 ? DQ4_OUT_BF16 : DQ4_OUT_F16;
   constexpr unsigned kFull = 0xFFFFFFFFu;
@@ -411,7 +440,7 @@ __global__ void __launch_bounds__(kLinThreads, 1)
   __shared__ float s_scb[256];
   __shared__ uint32_t s_tmem;          // TMEM base address from tcgen05.alloc
   __shared__ volatile int s_abort;     // set when any wait of the CTA ran out
-  __shared__ int s_last;               // this CTA completes a shared tile
+  __shared__ int s_last[2];            // this CTA completes its first / last shared tile
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(base);
@@ -422,8 +451,8 @@ __global__ void __launch_bounds__(kLinThreads, 1)
   auto empty_x = [&](int s) { return bar0 + 8 * (2 * kAS + kXS + s); };
   auto raw_full = [&](int s) { return bar0 + 8 * (2 * kAS + 2 * kXS + s); };
   auto raw_empty = [&](int s) { return bar0 + 8 * (2 * kAS + 2 * kXS + kRawS + s); };
-  // acc_full(b): the segment in accumulator b is final; acc_empty(b): read out; acc_done:
-  // every MMA done
+  // acc_full(b): the segment in accumulator buffer b is final (one arrival per issuer);
+  // acc_empty(b): read out; acc_done: every MMA done (one arrival per issuer)
   auto acc_full = [&](int b) { return bar0 + 8 * (2 * kAS + 2 * kXS + 2 * kRawS + b); };
   auto acc_empty = [&](int b) { return acc_full(kAcc + b); };
   const uint32_t acc_done = acc_full(2 * kAcc);
@@ -510,10 +539,10 @@ __global__ void __launch_bounds__(kLinThreads, 1)
         mbar_init(raw_empty(s), kGroupWarps);
       }
       for (int g = 0; g < kAcc; ++g) {
-        mbar_init(acc_full(g), 1);
+        mbar_init(acc_full(g), kIss);
         mbar_init(acc_empty(g), 8);  // the 8 epilogue warps
       }
-      mbar_init(acc_done, 1);
+      mbar_init(acc_done, kIss);
       *abort_flag = 0;
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
       asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmap_x)));
@@ -530,6 +559,9 @@ __global__ void __launch_bounds__(kLinThreads, 1)
 #endif
 
   if (warp == kRawWarp) {
+    // the weight copies start once the producers issued their first stages' code loads,
+    // which would otherwise queue behind the copies in DRAM (named barrier 3)
+    asm volatile("bar.sync 3, %0;" :: "n"(kProducerWarps * 32 + 32) : "memory");
     if (lane == 0) {
       // ---- packed weight rows of each local stage's tile: kSub boxes of 128 rows x 32
       // bytes (64 values) per stage, 32-byte swizzled, each in its own 4 KB
@@ -585,108 +617,200 @@ __global__ void __launch_bounds__(kLinThreads, 1)
         for (int j = q - 1; j >= 0 && j >= q - kXS; --j)
           mbar_wait(full_x(j % kXS), (j / kXS) & 1);
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp >= kMmaWarp && warp < kMmaWarp + kIss) {
     if (lane == 0) {
-      // ---- the MMA issue: local stage l reads its weight slot (l % kAS) and its
-      // activation slots (one per stage for narrow tiles, one per K step otherwise),
-      // accumulating into its segment's accumulator (columns buf * BX ..), which the
-      // segment kAcc back must have left; each slot is released when its MMAs complete
-      const uint32_t idesc = instr_desc<BX>(kBF16);
-      RingPos<kAS> apos;
-      RingPos<kXS> xpos;
-      Cursor cs = cursor_at(0);
-      bool stop = false, first = true;  // first: the stage opens its segment
-      int committed = 0;  // segments whose accumulator was committed
-      for (int l = 0; l < nl && !stop; ++l, apos.next(), advance(cs, 1)) {
-        // the weight stage and (with whole-stage activation slots) its activations, polled
-        // together first
-        const bool ready = !*abort_flag &&
-                           (S::kXSub == kSub
-                                ? mbar_try2(full_w(apos.slot), apos.phase, full_x(xpos.slot),
-                                            xpos.phase)
-                                : mbar_try(full_w(apos.slot), apos.phase));
-        if (!ready && (*abort_flag || !mbar_wait(full_w(apos.slot), apos.phase))) {
-          if (!*abort_flag) fail();
-          break;
+      if constexpr (kIss == 1) {
+        // ---- the MMA issue: local stage l reads its weight slot (l % kAS) and its
+        // activation slots (one per stage for narrow tiles, one per K step otherwise),
+        // accumulating into its segment's accumulator (columns buf * BX ..), which the
+        // segment kAcc back must have left; each slot is released when its MMAs complete
+        const uint32_t idesc = instr_desc<BX>(kBF16);
+        RingPos<kAS> apos;
+        RingPos<kXS> xpos;
+        Cursor cs = cursor_at(0);
+        bool stop = false, first = true;  // first: the stage opens its segment
+        int committed = 0;  // segments whose accumulator was committed
+        for (int l = 0; l < nl && !stop; ++l, apos.next(), advance(cs, 1)) {
+          // the weight stage and (with whole-stage activation slots) its activations, polled
+          // together first
+          const bool ready = !*abort_flag &&
+                             (S::kXSub == kSub
+                                  ? mbar_try2(full_w(apos.slot), apos.phase, full_x(xpos.slot),
+                                              xpos.phase)
+                                  : mbar_try(full_w(apos.slot), apos.phase));
+          if (!ready && (*abort_flag || !mbar_wait(full_w(apos.slot), apos.phase))) {
+            if (!*abort_flag) fail();
+            break;
+          }
+          const int buf = kAcc == 1 ? 0 : (cs.seg & 1);
+          if (first && cs.seg >= kAcc &&
+              (*abort_flag ||
+               !mbar_wait(acc_empty(buf), uint32_t(cs.seg / kAcc - 1) & 1u))) {
+            if (!*abort_flag) fail();
+            break;
+          }
+          const int ns = min(kSub, kt_count - cs.stage * kSub);
+          const uint32_t d_tmem = tmem + buf * BX;
+          for (int sub = 0; sub < ns; ++sub) {
+            const int xi = sub % S::kXSub;  // K step within the activation slot
+            if (xi == 0 && !(ready && sub == 0 && S::kXSub == kSub) &&
+                !mbar_wait(full_x(xpos.slot), xpos.phase)) {
+              fail();
+              stop = true;
+              break;
+            }
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            // weights (M side) from TMEM: 8 columns per 16-value K slice
+            const uint32_t a_tmem = tmem + kATmemCol + (apos.slot * kSub + sub) * 32;
+            const uint32_t b_addr = sbase + S::kXOff + xpos.slot * S::kXSlot + xi * S::kB;
+  #pragma unroll
+            for (int ks = 0; ks < kBK / 16; ++ks) {
+              const uint64_t db = smem_desc(b_addr + ks * 32);
+              const uint32_t acc = (first && sub == 0 && ks == 0) ? 0u : 1u;
+              asm volatile(
+                  "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+                  "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}"
+                  :: "r"(d_tmem), "r"(a_tmem + ks * 8), "l"(db), "r"(idesc), "r"(acc));
+            }
+            if (xi == S::kXSub - 1 || sub == ns - 1) {  // the slot's last K step
+              asm volatile(
+                  "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                  :: "r"(empty_x(xpos.slot)) : "memory");
+              xpos.next();
+            }
+          }
+          if (stop) break;
+          asm volatile(
+              "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+              :: "r"(empty_a(apos.slot)) : "memory");
+          first = cs.stage == st_count - 1 || l == nl - 1;  // the segment's last stage
+          if (first) {
+            asm volatile(
+                "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                :: "r"(acc_full(buf)) : "memory");
+            ++committed;
+          }
         }
-        const int buf = kAcc == 1 ? 0 : (cs.seg & 1);
-        if (first && cs.seg >= kAcc &&
-            (*abort_flag ||
-             !mbar_wait(acc_empty(buf), uint32_t(cs.seg / kAcc - 1) & 1u))) {
-          if (!*abort_flag) fail();
-          break;
-        }
-        const int ns = min(kSub, kt_count - cs.stage * kSub);
-        const uint32_t d_tmem = tmem + buf * BX;
-        for (int sub = 0; sub < ns; ++sub) {
-          const int xi = sub % S::kXSub;  // K step within the activation slot
-          if (xi == 0 && !(ready && sub == 0 && S::kXSub == kSub) &&
-              !mbar_wait(full_x(xpos.slot), xpos.phase)) {
-            fail();
+        // after a failure, release the epilogue's next wait on each accumulator
+        for (int k = 0; k < kAcc && committed < nseg; ++k, ++committed)
+          asm volatile(
+              "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+              :: "r"(acc_full(kAcc == 1 ? 0 : (committed & 1))) : "memory");
+        // tracks every MMA issued above: no MMA still writes TMEM when it is freed below
+        asm volatile(
+            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+            :: "r"(acc_done) : "memory");
+        mbar_wait(acc_done, 0);
+      } else {
+        // ---- several issuers: issuer iss issues local stages iss, iss + kIss, .. (the stages
+        // producer group iss decodes) into its own accumulator buffers, columns
+        // (iss kAcc + buf) BX ..; stage l reads weight slot l % kAS and the whole-stage
+        // activation slot l % kXS.  Each issuer arrives once per segment on the segment's
+        // acc_full, having issued its MMAs of that segment (if any); the read-out adds the
+        // issuers' partial sums.  An issuer takes a buffer, and arrives on its acc_full, only
+        // after the read-out of the segment kAcc back (acc_empty), so the phases of a
+        // buffer's barriers never mix segments.
+        const int iss = warp - kMmaWarp;
+        const uint32_t idesc = instr_desc<BX>(kBF16);
+        bool stop = false;
+        int my_seg = 0;     // segments before my_seg have this issuer's acc_full arrival
+        int open_seg = -1;  // the segment this issuer holds a buffer for
+        auto buf_of = [&](int sg) { return kAcc == 1 ? 0 : (sg & 1); };
+        auto acquire = [&](int sg) {  // segment sg's buffer was read out for segment sg - kAcc
+          if (sg < kAcc) return true;
+          if (*abort_flag) return false;
+          if (mbar_wait(acc_empty(buf_of(sg)), uint32_t(sg / kAcc - 1) & 1u)) return true;
+          fail();
+          return false;
+        };
+        auto close = [&](int sg) {  // arrives once this issuer's MMAs so far completed
+          asm volatile(
+              "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+              :: "r"(acc_full(buf_of(sg))) : "memory");
+        };
+        Cursor cs = cursor_at(iss);
+        for (int l = iss; l < nl; l += kIss, advance(cs, kIss)) {
+          for (; my_seg < cs.seg; ++my_seg) {  // segments with no stage of this issuer
+            if (!acquire(my_seg)) {
+              stop = true;
+              break;
+            }
+            close(my_seg);
+          }
+          if (stop) break;
+          const int aslot = l % kAS, xslot = l % kXS;
+          const uint32_t aph = uint32_t(l / kAS) & 1u, xph = uint32_t(l / kXS) & 1u;
+          const bool ready =
+              !*abort_flag && mbar_try2(full_w(aslot), aph, full_x(xslot), xph);
+          if (!ready && (*abort_flag || !mbar_wait(full_w(aslot), aph) ||
+                         !mbar_wait(full_x(xslot), xph))) {
+            if (!*abort_flag) fail();
             stop = true;
             break;
           }
+          const bool first = open_seg != cs.seg;  // this issuer's first stage of the segment
+          if (first) {
+            if (!acquire(cs.seg)) {
+              stop = true;
+              break;
+            }
+            open_seg = cs.seg;
+          }
           asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-          // weights (M side) from TMEM: 8 columns per 16-value K slice
-          const uint32_t a_tmem = tmem + kATmemCol + (apos.slot * kSub + sub) * 32;
-          const uint32_t b_addr = sbase + S::kXOff + xpos.slot * S::kXSlot + xi * S::kB;
+          const int ns = min(kSub, kt_count - cs.stage * kSub);
+          const uint32_t d_tmem = tmem + (iss * kAcc + buf_of(cs.seg)) * BX;
+          for (int sub = 0; sub < ns; ++sub) {
+            const uint32_t a_tmem = tmem + kATmemCol + (aslot * kSub + sub) * 32;
+            const uint32_t b_addr = sbase + S::kXOff + xslot * S::kXSlot + sub * S::kB;
 #pragma unroll
-          for (int ks = 0; ks < kBK / 16; ++ks) {
-            const uint64_t db = smem_desc(b_addr + ks * 32);
-            const uint32_t acc = (first && sub == 0 && ks == 0) ? 0u : 1u;
-            asm volatile(
-                "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-                "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}"
-                :: "r"(d_tmem), "r"(a_tmem + ks * 8), "l"(db), "r"(idesc), "r"(acc));
+            for (int ks = 0; ks < kBK / 16; ++ks) {
+              const uint64_t db = smem_desc(b_addr + ks * 32);
+              const uint32_t acc = (first && sub == 0 && ks == 0) ? 0u : 1u;
+              asm volatile(
+                  "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+                  "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}"
+                  :: "r"(d_tmem), "r"(a_tmem + ks * 8), "l"(db), "r"(idesc), "r"(acc));
+            }
           }
-          if (xi == S::kXSub - 1 || sub == ns - 1) {  // the slot's last K step
-            asm volatile(
-                "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-                :: "r"(empty_x(xpos.slot)) : "memory");
-            xpos.next();
-          }
-        }
-        if (stop) break;
-        asm volatile(
-            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-            :: "r"(empty_a(apos.slot)) : "memory");
-        first = cs.stage == st_count - 1 || l == nl - 1;  // the segment's last stage
-        if (first) {
           asm volatile(
               "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-              :: "r"(acc_full(buf)) : "memory");
-          ++committed;
+              :: "r"(empty_x(xslot)) : "memory");
+          asm volatile(
+              "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+              :: "r"(empty_a(aslot)) : "memory");
+          // this issuer's last stage of the segment: the segment ends before its next stage
+          Cursor cn = cs;
+          advance(cn, kIss);
+          if (l + kIss >= nl || cn.seg != cs.seg) {
+            close(cs.seg);
+            my_seg = cs.seg + 1;
+          }
         }
-      }
-      // after a failure, release the epilogue's next wait on each accumulator
-      for (int k = 0; k < kAcc && committed < nseg; ++k, ++committed)
+        if (!stop) {
+          for (; my_seg < nseg; ++my_seg) {  // trailing segments with no stage of this issuer
+            if (!acquire(my_seg)) {
+              stop = true;
+              break;
+            }
+            close(my_seg);
+          }
+        }
+        // after a failure, release the epilogue's next wait on each buffer
+        for (int k = 0; stop && k < kAcc && my_seg < nseg; ++k, ++my_seg) close(my_seg);
+        // tracks every MMA this issuer issued: no MMA still writes TMEM when it is freed
         asm volatile(
             "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-            :: "r"(acc_full(kAcc == 1 ? 0 : (committed & 1))) : "memory");
-      // tracks every MMA issued above: no MMA still writes TMEM when it is freed below
-      asm volatile(
-          "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-          :: "r"(acc_done) : "memory");
-      mbar_wait(acc_done, 0);
+            :: "r"(acc_done) : "memory");
+        mbar_wait(acc_done, 0);
+      }
     }
   } else {
-    // The pair table, built by the producer warps alone while the TMA warps start their
-    // copies: one codebook load per thread, the entries' values by shuffle (entry b copy
-    // g = word 16 b + g holds vcb[b >> 4], vcb[b & 15]); named barrier 2 over the producer
-    // threads orders it before their first lookup.
-    {
-      static_assert(kProducerWarps * 32 >= 256, "the producers load the scale codebook");
-      if (tid < 256) s_scb[tid] = __ldg(p.w.scb + tid);
-      const float v = __ldg(p.w.vcb + (lane & 15));
-      for (int i = tid; i < 256 * 16; i += kProducerWarps * 32) {
-        const int b = i >> 4;
-        float2 e;
-        e.x = __shfl_sync(kFull, v, b >> 4);
-        e.y = __shfl_sync(kFull, v, b & 15);
-        *reinterpret_cast<float2*>(base + S::kTabOff + 8 * i) = e;
-      }
-      asm volatile("bar.sync 2, %0;" :: "n"(kProducerWarps * 32) : "memory");
-    }
+    // The codebooks, loaded first (their latency overlaps the first stages' code loads
+    // below); the scale codebook goes to shared memory, the value codebook becomes the
+    // pair table after those loads are issued.
+    static_assert(kProducerWarps * 32 >= 256, "the producers load the scale codebook");
+    const float scb_v = tid < 256 ? __ldg(p.w.scb + tid) : 0.f;
+    const float vcb_v = __ldg(p.w.vcb + (lane & 15));
     // ---- dequantize.  Producer group `group` (kGroupWarps warps) takes local stages
     // group, group + kGroups, ...; within it, warp w writes TMEM lanes 32 (w % 4) ..
     // (weight row r = 32 (w % 4) + lane of the stage's tile) and values 8 kWords h ..
@@ -761,7 +885,10 @@ __global__ void __launch_bounds__(kLinThreads, 1)
     // its parts into Y.
     constexpr int kHalf = BX / 2;
     constexpr int kChunk = kHalf < 32 ? kHalf : 32;  // columns per step of the parts' sum
-    constexpr int kLd = kHalf < 32 ? 8 : 32;  // accumulator columns per TMEM read (one wait)
+    constexpr int kBatch = kChunk <= 8 ? 4 : kChunk <= 16 ? 2 : 1;  // parts loaded at once
+    // accumulator columns per TMEM read (one wait); 8 when partial sums of several issuers
+    // are added (two reads live at once)
+    constexpr int kLd = (kHalf < 32 || kIss > 1) ? 8 : 32;
     const int eq = warp & 3, c_begin = ((warp >> 2) & 1) * kHalf;
     auto store_y = [&](int64_t m, int64_t ny, float f) {
       const int64_t o = m * p.N + ny;  // a warp writes 32 consecutive columns of row m
@@ -774,110 +901,169 @@ __global__ void __launch_bounds__(kLinThreads, 1)
       }
     };
     bool failed = false;
-    auto drain = [&](int ds) {
+    // where segment ds sits: its tile, the tile's first activation row for this warp's half
+    // of the columns, this lane's column of Y, and whether the segment is the whole tile
+    struct SegAt {
+      int64_t t, m0, ny;
+      bool whole;
+    };
+    auto seg_at = [&](int ds) {
+      SegAt g;
+      g.t = t0 + ds;
+      const uint32_t tw = uint32_t(g.t) / uint32_t(p.tiles_x);
+      g.m0 = int64_t(uint32_t(g.t) - tw * uint32_t(p.tiles_x)) * BX + c_begin;
+      g.ny = int64_t(tw) * kBW + eq * 32 + lane;
+      g.whole = (ds > 0 || stage0 == 0) && (ds < nseg - 1 || u1 == (g.t + 1) * st_count);
+      return g;
+    };
+    // a shared tile's parts are those of CTAs c_first .. c_last, in K order (found by
+    // stepping from this CTA: a tile has few parts); c_last holds the tile's last part,
+    // which no other shared tile ends in
+    auto parts_of = [&](int64_t t, uint32_t& c_first, uint32_t& c_last) {
+      const uint32_t t_lo = uint32_t(t) * uint32_t(st_count), t_hi = t_lo + st_count;
+      c_first = blockIdx.x;
+      c_last = blockIdx.x;
+      while (split_begin(c_first, p) > t_lo) --c_first;
+      while (split_begin(c_last + 1, p) < t_hi) ++c_last;
+    };
+    // ---- read-out of segments d0 .. d1 - 1 (warps 0..7; named barrier 1 over their 256
+    // threads).  Whole tiles go to Y.  A shared tile goes to this CTA's partial slot (0 for
+    // its first segment, 1 for its last: only those two can be shared), and the CTA
+    // arrives at the counters of all its shared tiles in one round (one barrier, fence and
+    // atomic each); the last of a tile's CTAs to arrive sums its parts into Y.
+    auto drain = [&](int d0, int d1) {
       if (warp >= 8) return;
-      const int buf = kAcc == 1 ? 0 : (ds & 1);
-      const bool mine = !failed && !*abort_flag &&
-                        mbar_wait(acc_full(buf), uint32_t(ds / kAcc) & 1u) && !*abort_flag;
-      if (!bar_and_256(mine)) {  // the same verdict in all 256 threads
-        failed = true;
-        return;
-      }
-      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const int64_t t = t0 + ds;
-      const uint32_t tw = uint32_t(t) / uint32_t(p.tiles_x);
-      const int64_t m0 = int64_t(uint32_t(t) - tw * uint32_t(p.tiles_x)) * BX + c_begin;
-      const int64_t ny = int64_t(tw) * kBW + eq * 32 + lane;  // this lane's column of Y
-      const bool whole =
-          (ds > 0 || stage0 == 0) && (ds < nseg - 1 || u1 == (t + 1) * st_count);
-      const uint32_t t_acc = tmem + (static_cast<uint32_t>(eq * 32) << 16) + buf * BX +
-                             c_begin;
-      // after its TMEM loads of the segment the warp hands the accumulator back
-      auto release = [&]() {
+      int nshared = 0;
+      int shared_seg[2] = {0, 0};
+      for (int ds = d0; ds < d1; ++ds) {
+        const int buf = kAcc == 1 ? 0 : (ds & 1);
+        const bool mine = !failed && !*abort_flag &&
+                          mbar_wait(acc_full(buf), uint32_t(ds / kAcc) & 1u) && !*abort_flag;
+        if (!bar_and_256(mine)) {  // the same verdict in all 256 threads
+          failed = true;
+          return;
+        }
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const SegAt g = seg_at(ds);
+        const uint32_t t_acc = tmem + (static_cast<uint32_t>(eq * 32) << 16) + buf * BX +
+                               c_begin;
+        // kLd accumulator columns from c on: with several issuers, the sum of the partial
+        // sums of those that issued a stage of the segment (local stages sa .. sb - 1), in
+        // issuer order (deterministic)
+        const int sa = seg_start(ds), sb = ds < nseg - 1 ? seg_start(ds + 1) : nl;
+        auto read_acc = [&](int c, uint32_t(&v)[kLd]) {
+          if constexpr (kIss == 1) {
+            tmem_ld(t_acc + c, v);
+          } else {
+            bool any = false;
+#pragma unroll
+            for (int i = 0; i < kIss; ++i) {
+              if (sa + (i - sa % kIss + kIss) % kIss >= sb) continue;  // no stage of issuer i
+              uint32_t w[kLd];
+              tmem_ld(t_acc + i * kAcc * BX + c, w);
+#pragma unroll
+              for (int j = 0; j < kLd; ++j)
+                v[j] = any ? __float_as_uint(
+                                 __fadd_rn(__uint_as_float(v[j]), __uint_as_float(w[j])))
+                           : w[j];
+              any = true;
+            }
+          }
+        };
+        if (g.whole) {
+#pragma unroll 1
+          for (int c = 0; c < kHalf; c += kLd) {
+            if (g.m0 + c >= p.M) break;  // warp-uniform
+            uint32_t v[kLd];
+            read_acc(c, v);
+            if (g.ny >= p.N) continue;
+#pragma unroll
+            for (int j = 0; j < kLd; ++j) {
+              if (g.m0 + c + j >= p.M) break;
+              store_y(g.m0 + c + j, g.ny, __uint_as_float(v[j]));
+            }
+          }
+        } else {
+          float* part = p.ws_part +
+                        ((int64_t(blockIdx.x) * 2 + (ds == 0 ? 0 : 1)) * BX + c_begin) * kBW +
+                        eq * 32 + lane;
+#pragma unroll 1
+          for (int c = 0; c < kHalf; c += kLd) {
+            uint32_t v[kLd];
+            read_acc(c, v);
+#pragma unroll
+            for (int j = 0; j < kLd; ++j) part[(c + j) * kBW] = __uint_as_float(v[j]);
+          }
+          shared_seg[nshared++] = ds;
+        }
+        // after its TMEM loads of the segment the warp hands the accumulator back
         asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
         __syncwarp();
         if (lane == 0) mbar_arrive(acc_empty(buf));
-      };
-      if (whole) {
-#pragma unroll 1
-        for (int c = 0; c < kHalf; c += kLd) {
-          if (m0 + c >= p.M) break;  // warp-uniform
-          uint32_t v[kLd];
-          tmem_ld(t_acc + c, v);
-          if (ny >= p.N) continue;
-#pragma unroll
-          for (int j = 0; j < kLd; ++j) {
-            if (m0 + c + j >= p.M) break;
-            store_y(m0 + c + j, ny, __uint_as_float(v[j]));
-          }
-        }
-        release();
-        return;
       }
-      // a shared tile: this CTA's FP32 partial into its slot (0 for its first segment, 1
-      // for its last), then the last of the tile's CTAs to arrive sums them
-      float* part = p.ws_part +
-                    ((int64_t(blockIdx.x) * 2 + (ds == 0 ? 0 : 1)) * BX + c_begin) * kBW +
-                    eq * 32 + lane;
-#pragma unroll 1
-      for (int c = 0; c < kHalf; c += kLd) {
-        uint32_t v[kLd];
-        tmem_ld(t_acc + c, v);
-#pragma unroll
-        for (int j = 0; j < kLd; ++j) part[(c + j) * kBW] = __uint_as_float(v[j]);
-      }
-      release();
-      // the tile's parts are those of CTAs c_first .. c_last, in K order (found by
-      // stepping from this CTA: a tile has few parts); c_last holds the tile's last part,
-      // which no other shared tile ends in
-      const uint32_t t_lo = uint32_t(t) * uint32_t(st_count), t_hi = t_lo + st_count;
-      uint32_t c_first = blockIdx.x, c_last = blockIdx.x;
-      while (split_begin(c_first, p) > t_lo) --c_first;
-      while (split_begin(c_last + 1, p) < t_hi) ++c_last;
-      // the barrier orders every thread's partial before thread 0's fence (cumulative),
-      // whose release the counter carries; the last arriver's fence acquires the others'
+      if (nshared == 0) return;
+      // the barrier orders every thread's partials before thread 0's release (cumulative),
+      // which the counters carry; the last arriver's acquire takes the others' partials, and
+      // the second barrier hands them to its threads.  Both counters' atomics are in flight
+      // at once.
       asm volatile("bar.sync 1, 256;" ::: "memory");
       if (tid == 0) {
-        __threadfence();
-        s_last = atomicAdd(p.ws_count + c_last, 1) == int(c_last - c_first);
-        __threadfence();
+        uint32_t cf0, cl0, cf1 = 0, cl1 = 0;
+        parts_of(t0 + shared_seg[0], cf0, cl0);
+        if (nshared > 1) parts_of(t0 + shared_seg[1], cf1, cl1);
+        const int o0 = atomic_add_acq_rel(p.ws_count + cl0, 1);
+        const int o1 = nshared > 1 ? atomic_add_acq_rel(p.ws_count + cl1, 1) : 0;
+        s_last[0] = o0 == int(cl0 - cf0);
+        s_last[1] = nshared > 1 && o1 == int(cl1 - cf1);
       }
       asm volatile("bar.sync 1, 256;" ::: "memory");
-      if (!s_last) return;
-      // part q is CTA c_first + q's first segment (slot 0), except that the tile may be
-      // the last segment (slot 1) of CTA c_first, when that CTA began in an earlier tile
-      const int slot0 = split_begin(c_first, p) < t_lo ? 1 : 0;
-      const int nparts = int(c_last - c_first + 1);
-      auto part_of = [&](int q) {
-        return p.ws_part +
-               ((int64_t(c_first + q) * 2 + (q == 0 ? slot0 : 0)) * BX + c_begin) * kBW +
-               eq * 32 + lane;
-      };
+      for (int k = 0; k < nshared; ++k) {
+        if (!s_last[k]) continue;
+        const SegAt g = seg_at(shared_seg[k]);
+        uint32_t c_first, c_last;
+        parts_of(g.t, c_first, c_last);
+        // part q is CTA c_first + q's first segment (slot 0), except that the tile may be
+        // the last segment (slot 1) of CTA c_first, when that CTA began in an earlier tile
+        const int slot0 = split_begin(c_first, p) < uint32_t(g.t) * uint32_t(st_count) ? 1 : 0;
+        const int nparts = int(c_last - c_first + 1);
+        auto part_of = [&](int q) {
+          return p.ws_part +
+                 ((int64_t(c_first + q) * 2 + (q == 0 ? slot0 : 0)) * BX + c_begin) * kBW +
+                 eq * 32 + lane;
+        };
 #pragma unroll 1
-      for (int c = 0; c < kHalf; c += kChunk) {
-        // all loads of a part before its sums (independent loads overlap), parts added in
-        // K order, part 0 first
-        float acc[kChunk];
-        const float* src0 = part_of(0) + c * kBW;
+        for (int c = 0; c < kHalf; c += kChunk) {
+          // the loads of kBatch parts at a time before their sums (independent loads
+          // overlap), parts added in K order, part 0 first
+          float acc[kChunk];
+#pragma unroll 1
+          for (int q0 = 0; q0 < nparts; q0 += kBatch) {
+            float x[kBatch][kChunk];
 #pragma unroll
-        for (int j = 0; j < kChunk; ++j) acc[j] = __ldcg(src0 + j * kBW);
-        for (int q = 1; q < nparts; ++q) {
-          const float* src = part_of(q) + c * kBW;
-          float x[kChunk];
+            for (int qq = 0; qq < kBatch; ++qq) {
+              if (q0 + qq >= nparts) break;
+              const float* src = part_of(q0 + qq) + c * kBW;
 #pragma unroll
-          for (int j = 0; j < kChunk; ++j) x[j] = __ldcg(src + j * kBW);
+              for (int j = 0; j < kChunk; ++j) x[qq][j] = __ldcg(src + j * kBW);
+            }
 #pragma unroll
-          for (int j = 0; j < kChunk; ++j) acc[j] = __fadd_rn(acc[j], x[j]);
-        }
-        if (ny < p.N) {
+            for (int qq = 0; qq < kBatch; ++qq) {
+              if (q0 + qq >= nparts) break;
 #pragma unroll
-          for (int j = 0; j < kChunk; ++j) {
-            if (m0 + c + j >= p.M) break;
-            store_y(m0 + c + j, ny, acc[j]);
+              for (int j = 0; j < kChunk; ++j)
+                acc[j] = q0 + qq == 0 ? x[qq][j] : __fadd_rn(acc[j], x[qq][j]);
+            }
+          }
+          if (g.ny < p.N) {
+#pragma unroll
+            for (int j = 0; j < kChunk; ++j) {
+              if (g.m0 + c + j >= p.M) break;
+              store_y(g.m0 + c + j, g.ny, acc[j]);
+            }
           }
         }
+        if (tid == 0) p.ws_count[c_last] = 0;  // ready for the next call
       }
-      if (tid == 0) p.ws_count[c_last] = 0;  // ready for the next call
     };
 
     // the codes / absmax of this group's next two stages, rotated every stage (no
@@ -891,6 +1077,20 @@ __global__ void __launch_bounds__(kLinThreads, 1)
     fetch(group, cur, cA, aA, wA, mA);
     fetch(group + kGroups, pf, cB, aB, wB, mB);
     advance(pf, kGroups);
+    asm volatile("bar.arrive 3, %0;" :: "n"(kProducerWarps * 32 + 32) : "memory");
+    // The pair table, built by the producer warps alone while the TMA warps start their
+    // copies and the loads above are in flight: the entries' values by shuffle (entry b
+    // copy g = word 16 b + g holds vcb[b >> 4], vcb[b & 15]); named barrier 2 over the
+    // producer threads orders it and the scale codebook before their first lookup.
+    if (tid < 256) s_scb[tid] = scb_v;
+    for (int i = tid; i < 256 * 16; i += kProducerWarps * 32) {
+      const int b = i >> 4;
+      float2 e;
+      e.x = __shfl_sync(kFull, vcb_v, b >> 4);
+      e.y = __shfl_sync(kFull, vcb_v, b & 15);
+      *reinterpret_cast<float2*>(base + S::kTabOff + 8 * i) = e;
+    }
+    asm volatile("bar.sync 2, %0;" :: "n"(kProducerWarps * 32) : "memory");
     RingPos<kAS> apos;
     RingPos<kRawS> rpos;
     for (int g = 0; g < group; ++g) {  // this group's first stage
@@ -902,13 +1102,16 @@ __global__ void __launch_bounds__(kLinThreads, 1)
     // this lane's copy of the pair table: entry b at tab + 128 b
     const uint32_t tab = sbase + S::kTabOff + (lane & 15) * 8;
     const int flip = (r >> 2) & 1;  // the raw boxes' 32-byte swizzle for this row
-    // Segment d is read out before the first stage whose weight slot waits for MMAs that
-    // need its accumulator back (kAS stages into segment d + 1; the MMA then has those
-    // kAS stages queued when it gets the accumulator), the rest after the last stage.
+    // Segment d is read out kAS stages into segment d + 1 (before the first stage whose
+    // weight slot waits for MMAs that may need its accumulator buffer back; the MMAs then
+    // have those kAS stages queued when they get it), the last one after the last stage.
+    // Reading a CTA's first segment out early lets the CTAs that share its tile finish
+    // that tile without it, so each CTA completes at most one tile at its end.
     // The stage loop runs up to the next read-out, so the read-out code stays out of it.
     int l = group;  // this group's next local stage
+    int lim = 0;    // the stages before the next read-out
     for (;;) {
-      const int lim = next_drain < nseg - 1 ? min(nl, seg_start(next_drain + 1) + kAS) : nl;
+      lim = next_drain < nseg - 1 ? min(nl, seg_start(next_drain + 1) + kAS) : nl;
       for (; l < lim; l += kGroups) {  // local stage l
         unpack(wA, mA, cA, aA);  // loaded an iteration ago
         float sc[kSub][kHalves];
@@ -1003,7 +1206,8 @@ __global__ void __launch_bounds__(kLinThreads, 1)
       }
       // every segment is read out, failed or not (each read-out takes all epilogue threads)
       if (next_drain >= nseg) break;
-      drain(next_drain++);
+      drain(next_drain, next_drain + 1);
+      ++next_drain;
       if (failed) l = nl;  // no more stages
     }
   }
@@ -1051,7 +1255,7 @@ int launch_linear(const CUtensorMap& tx, const CUtensorMap& tw, const LinArgs& p
 #if DQ4_PDL
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
-  cfg.blockDim = dim3(kLinThreads);
+  cfg.blockDim = dim3(kThreadsOf(BX));
   cfg.dynamicSmemBytes = S::kBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -1066,7 +1270,7 @@ int launch_linear(const CUtensorMap& tx, const CUtensorMap& tw, const LinArgs& p
   }
   return DQ4_OK;
 #else
-  kernel<<<static_cast<unsigned>(grid), kLinThreads, S::kBytes, stream>>>(tx, tw, p);
+  kernel<<<static_cast<unsigned>(grid), kThreadsOf(BX), S::kBytes, stream>>>(tx, tw, p);
   return check_launch();
 #endif
 }
@@ -1085,9 +1289,11 @@ struct LinPlan {
 // MMAs), a CTA about 2400 more (pipeline fill, drain and read-out), and a split CTA the
 // partial tiles' stores and sums, about 1600 + 15 BX (two FP32 partials of 128 x BX each
 // go out and come back, at the end of the run when every SM does the same), and a
-// read-out per tile boundary it crosses (about 400 with one accumulator, hidden with
-// two).  The widths tried are the powers of two from 16 up to the first one >= M.  With
-// split false only whole-tile plans count.
+// read-out per tile boundary it crosses: hidden with two accumulator buffers per issuer,
+// about 400 with one buffer and one issuer, and 2000 with one buffer for each of two
+// issuers (both wait at the boundary; measured at BX = 64, where whole tiles win).  The
+// widths tried are the powers of two from 16 up to the first one >= M.  With split false
+// only whole-tile plans count.
 LinPlan plan_linear(int64_t M, int64_t N, int64_t K, int sms, bool split) {
   LinPlan best;
   int64_t best_cost = INT64_MAX;
@@ -1111,7 +1317,7 @@ LinPlan plan_linear(int64_t M, int64_t N, int64_t K, int sms, bool split) {
       const int64_t crossings = (per_cta + st_count - 1) / st_count;
       const int64_t split_cost =
           per_cta * stage_cost + 2400 + 1600 + 15 * bx +
-          (kAccOf(bx) == 1 ? 400 * crossings : 0);
+          (kAccOf(bx) == 1 ? (kIssOf(bx) > 1 ? 2000 : 400) * crossings : 0);
       if (split_cost < cost) {
         cost = split_cost;
         pl.ctas = sms;

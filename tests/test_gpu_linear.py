@@ -152,15 +152,17 @@ def test_errors(dq):
 # Tiles that would not fill the SMs in whole rounds: with a workspace one CTA per SM
 # takes an equal share of the (tile, stage) units, a run that may cross tile boundaries;
 # partial FP32 tiles are summed in K order by the last CTA to finish each tile.  On a
-# 152-SM GB300 these take (BX, most tiles one CTA touches): (16, 2), (16, 1), (64, 2),
-# (16, 1) with a partial last stage (K = 1216), (64, 2), (128, 2) ragged, (128, 3)
+# 152-SM GB300 these take (BX, most tiles one CTA touches): (16, 2), (16, 1), (128, 2),
+# (16, 1) with a partial last stage (K = 1216), (32, 2), (128, 2) ragged, (128, 3)
 # ragged, (256, 2) ragged, (256, 3) with a partial last stage, (256, 4) ragged with
-# one-stage tiles of one K step, (256, 5) one-stage, (16, 3), (256, 5).
-# BX <= 64 alternates two accumulators, wider tiles reuse one.
+# one-stage tiles of one K step, (256, 5) one-stage, (16, 3), (256, 5), and (64, 2)
+# twice (M = 64 and a ragged M = 40).  BX <= 64 issues its MMAs from two threads, each
+# into its own accumulators (two buffers each up to BX = 32, one at BX = 64); wider tiles
+# issue from one thread into one buffer.
 SPLIT_SHAPES = [(16, 11008, 4096), (3, 2000, 4096), (128, 1024, 8192), (16, 4860, 1216),
                 (128, 2000, 2048), (384, 1000, 4096), (300, 9856, 2048), (300, 4096, 4096),
                 (1024, 9856, 1216), (1500, 9856, 64), (2048, 9856, 256), (16, 49152, 512),
-                (2048, 9856, 512)]
+                (2048, 9856, 512), (64, 2000, 16384), (40, 2000, 16384)]
 
 
 @pytest.mark.parametrize("M,N,K", SPLIT_SHAPES)
