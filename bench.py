@@ -970,11 +970,14 @@ def run_int8prep(args):
 
 
 def run_outprod(args):
-    """Time dq4_nested_out_prod (row blocks, bounded transient) against the whole-copy path."""
+    """Time dq4_nested_out_prod (W decoded in row blocks inside a tcgen05 GEMM with FP32
+    accuracy) against the page's unfused sequence (row blocks dequantized into a bounded FP32
+    transient, each accumulated by a cuBLAS FP32 GEMM) and against dequantizing all of W."""
     import torch
 
     import quantized_weight_dequantization_gb300 as dq
 
+    torch.backends.cuda.matmul.allow_tf32 = False  # the comparison GEMMs in true FP32
     dev = torch.device("cuda:0")
     rows, cols, ncols = args.rows, args.cols, args.ncols
     p = gen.make_problem(rows * cols, 64, 256, "nf4", 0.5, 0.0371, seed=7)
@@ -982,21 +985,36 @@ def run_outprod(args):
          for k in ("packed", "scale_codes", "nested_absmax", "scale_codebook", "value_codebook")}
     G = torch.from_numpy(gen.make_normal_g(rows, ncols, seed=8)).to(dev)
     dst = torch.empty((cols, ncols), dtype=torch.float32, device=dev)
-    budget = args.transient_mib << 20
-    transient = torch.empty(max(1, min(rows, budget // (4 * cols))) * cols, dtype=torch.float32,
-                            device=dev)
+    args_w = (t["packed"], t["scale_codes"], t["nested_absmax"], t["scale_codebook"],
+              t["value_codebook"], float(p.offset))
 
-    def blocked():
-        dq.out_prod(t["packed"], t["scale_codes"], t["nested_absmax"], t["scale_codebook"],
-                    t["value_codebook"], float(p.offset), rows, cols, G, dst=dst,
-                    transient=transient, transient_bytes=budget)
+    def fused():
+        dq.out_prod(*args_w, rows, cols, G, dst=dst)
+
+    # the page's sequence: row blocks of at most --transient-mib MiB of FP32, each block
+    # starting on a nested-group boundary (16384 values), beta 0 for the first GEMM, 1 after
+    unit = 64 * 256
+    rb = max(1, min(rows, (args.transient_mib << 20) // (4 * cols)))
+    align = unit // int(np.gcd(cols, unit))
+    if rb >= align:
+        rb -= rb % align
+    transient = torch.empty(rb * cols, dtype=torch.float32, device=dev)
+
+    def blocked_unfused():
+        for r0 in range(0, rows, rb):
+            nr = min(rb, rows - r0)
+            first = r0 * cols
+            w = dq.dq4_nested(t["packed"][first // 2:], t["scale_codes"][first // 64:],
+                              t["nested_absmax"][first // unit:], t["scale_codebook"],
+                              t["value_codebook"], float(p.offset), nr * cols, 64, 256,
+                              torch.float32, out=transient[:nr * cols])
+            torch.addmm(dst, w.view(nr, cols).t(), G[r0:r0 + nr], beta=0.0 if r0 == 0 else 1.0,
+                        out=dst)
 
     full = torch.empty((rows, cols), dtype=torch.float32, device=dev)
 
     def whole():  # dequantize all of W to FP32, then one GEMM
-        dq.dq4_nested(t["packed"], t["scale_codes"], t["nested_absmax"], t["scale_codebook"],
-                      t["value_codebook"], float(p.offset), rows * cols, 64, 256, torch.float32,
-                      out=full.view(-1))
+        dq.dq4_nested(*args_w, rows * cols, 64, 256, torch.float32, out=full.view(-1))
         torch.mm(full.t(), G, out=dst)
 
     def timeit(fn, k):
@@ -1012,20 +1030,54 @@ def run_outprod(args):
         return e0.elapsed_time(e1) / k
 
     k = max(1, args.steps)
-    ms_blocked = timeit(blocked, k)
+    fused()
+    torch.cuda.synchronize(dev)
+    ref = dst.clone()
+    blocked_unfused()
+    torch.cuda.synchronize(dev)
+    rel = float((ref - dst).abs().max() / dst.abs().max())
+    if not rel < 1e-4:
+        raise SystemExit(f"fused and unfused out_prod differ (max relative {rel}); refusing to time")
+    ms_fused = timeit(fused, k)
+    ms_blocked = timeit(blocked_unfused, k)
     ms_whole = timeit(whole, k)
     flops = 2.0 * rows * cols * ncols
-    nblocks = -(-rows // max(1, transient.numel() // cols))
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except (OSError, ValueError):
+        pass
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    bf16 = float(peaks.get("bf16_tflops", 1900.0))
+    # the two bounds of one call: its algorithmic bytes (packed W, codes, absmax, G read once,
+    # dst written once) at the copy bandwidth, and its tensor work (six BF16 products per
+    # FP32 multiply-add) at the BF16 peak
+    alg_bytes = rows * cols // 2 + rows * cols // 64 + 4 * (rows * cols // unit) + \
+        4 * rows * ncols + 4 * cols * ncols
+    hbm_ms = alg_bytes / (hbm * 1e9) * 1e3
+    tensor_ms = 6 * flops / (bf16 * 1e12) * 1e3
+    bound = "tensor" if tensor_ms >= hbm_ms else "hbm"
+    nws = int(dq.lib.dq4_nested_out_prod_workspace_bytes(rows, cols, ncols))
     print(json.dumps({
         "metric": "row-blocked dequant + GEMM (dst = W^T G) time",
-        "value": ms_blocked, "unit": "ms", "higher_is_better": False, "n_gpus": 1,
-        "steps": k, "warmup": args.warmup, "ms_per_step": ms_blocked,
-        "config": {"workload": f"out_prod rows={rows} cols={cols} ncols={ncols}, transient "
-                               f"<= {args.transient_mib} MiB ({nblocks} blocks)"},
-        "gemm_tflops": flops / (ms_blocked / 1e3) / 1e12,
-        "whole_copy_ms": ms_whole,
-        "transient_bytes": transient.numel() * 4, "whole_copy_bytes": rows * cols * 4,
-        "gpu_launches_per_step": 2 * nblocks,
+        "value": ms_fused, "unit": "ms", "higher_is_better": False, "n_gpus": 1,
+        "steps": k, "warmup": args.warmup, "ms_per_step": ms_fused, "dtype": "f32",
+        "config": {"workload": f"out_prod rows={rows} cols={cols} ncols={ncols}, NF4-style "
+                               f"nested (bs 64, nested 256), FP32 G and dst",
+                   "l2": f"G alone is {4 * rows * ncols / 1e6:.0f} MB per call"},
+        "fp32_equivalent_tflops": flops / (ms_fused / 1e3) / 1e12,
+        "roofline": {"bound": bound, "hbm_ms": hbm_ms, "tensor_ms_6_bf16_products": tensor_ms,
+                     "frac": max(hbm_ms, tensor_ms) / ms_fused, "peaks": "measured"
+                     if peaks else "fallback"},
+        "unfused_blocked_ms": ms_blocked,
+        "unfused_blocked_transient_bytes": rb * cols * 4,
+        "unfused_blocks": -(-rows // rb),
+        "whole_copy_ms": ms_whole, "whole_copy_bytes": rows * cols * 4,
+        "speedup_vs_unfused_blocked": ms_blocked / ms_fused,
+        "workspace_bytes": nws,
+        "fused_vs_unfused_max_rel_diff": rel,
+        "gpu_launches_per_step": 2 if nws > 0 else 1,
     }), flush=True)
 
 

@@ -68,8 +68,8 @@ extern "C" {
 #define DQ4_ERR_DEVICE 7           /* no current CUDA device could be queried */
 #define DQ4_ERR_ARCH 8             /* current device is not compute capability 10.3 */
 #define DQ4_ERR_LAUNCH 9           /* the CUDA runtime reported an error at launch */
-#define DQ4_ERR_TOO_LARGE 10       /* more scratch needed than given (static array, transient) */
-#define DQ4_ERR_CUBLAS 11          /* cuBLAS could not be loaded or reported an error */
+#define DQ4_ERR_TOO_LARGE 10       /* more scratch needed than given (the static array) */
+#define DQ4_ERR_CUBLAS 11          /* reserved: no entry point calls cuBLAS any more */
 
 /* Version of this interface (incremented on any change of a signature). */
 int dq4_abi_version(void);
@@ -204,31 +204,50 @@ int dq4_int8_correction_prep(const uint16_t* A, const int8_t* CB, const float* S
                              uint16_t* subA, uint16_t* subB, int* bad_cols, void* stream);
 
 /*
- * Row-blocked dequantization feeding a GEMM, with a bounded transient:
+ * Row-blocked dequantization fused into a GEMM:
  *   dst = W^T * G       W = the FP32 dequantization of the rows x cols weight
  * (dq4_nested's values read row-major), G a rows x ncols FP32 matrix, dst a
- * cols x ncols FP32 matrix, all row-major.  The sum runs over W's rows, in
- * blocks of as many rows as `transient` holds (at least one row): each block
- * is dequantized to FP32 into `transient` and a cuBLAS GEMM accumulates it
- * into dst with beta = 0 for the first block and 1 after.  Source: "cuda:
- * out_prod dequantizes a 2D weight in row blocks" (llama.cpp pull request
- * #4), sections "What" and the approving review (the blocked sum, beta 0 then
- * 1, the transient bound of at most 256 MiB).
- *   transient        device float buffer of transient_bytes (>= 4 * cols)
- *   cublas_handle    a cublasHandle_t of the cuBLAS already loaded in the
- *                    process (e.g. the framework's); its stream is set to
- *                    `stream`; GEMMs run with FP32 compute
- * The dequantized blocks are bit-identical to dq4_nested's FP32 output; the
- * GEMM follows cuBLAS's FP32 accumulation.  rows == 0 zero-fills dst.
- * DQ4_ERR_TOO_LARGE if transient_bytes < 4 * cols; DQ4_ERR_CUBLAS if cuBLAS
- * cannot be loaded or fails; cols, ncols must fit in int32.
+ * cols x ncols FP32 matrix, all row-major.  The sum runs over W's rows in
+ * blocks of 64 rows, each dequantized inside the GEMM kernel (the whole
+ * dequantized weight never exists, nor does any dequantized block in device
+ * memory).  Source: "cuda: out_prod dequantizes a 2D weight in row blocks"
+ * (llama.cpp pull request #4), section "What" (the weight's row blocks
+ * dequantized through the F32 converter and accumulated into dst block
+ * after block, with a bounded transient).
+ *
+ * Accuracy: each FP32 operand is split exactly into three BF16 terms and the
+ * tensor cores accumulate in FP32 the six products whose terms total at most
+ * 2 (the three dropped ones are below 2^-24 of each product), so dst carries
+ * FP32 accuracy.  A G with a single 1 per column returns W's values exactly.
+ *   workspace        optional device float buffer of workspace_bytes: the
+ *                    rows are cut into row ranges that run on separate SMs
+ *                    (as many as fill the GPU and whose cols x ncols FP32
+ *                    partial tiles fit the buffer); a second kernel then
+ *                    adds the partial tiles in range order, so the result is
+ *                    deterministic.  NULL or too small: one row range,
+ *                    written straight to dst.
+ *                    dq4_nested_out_prod_workspace_bytes gives the size that
+ *                    fills the current device.
+ *   bad              optional device int: incremented when a wait inside the
+ *                    kernel timed out (the result is then invalid)
+ * rows == 0 zero-fills dst; cols == 0 or ncols == 0 is a no-op.
+ * Requires a CC 10.3 device; every pointer 4-byte aligned (packed and
+ * scale_codes included: they are staged in 4-byte words), else
+ * DQ4_ERR_ALIGN.
  */
 int dq4_nested_out_prod(const uint8_t* packed, const uint8_t* scale_codes,
                         const float* nested_absmax, const float* scale_codebook,
                         const float* value_codebook, float offset, int64_t rows, int64_t cols,
                         int32_t blocksize, int32_t nested_blocksize, const float* G,
-                        int64_t ncols, float* dst, float* transient, int64_t transient_bytes,
-                        void* cublas_handle, void* stream);
+                        int64_t ncols, float* dst, float* workspace, int64_t workspace_bytes,
+                        int* bad, void* stream);
+
+/*
+ * The workspace bytes dq4_nested_out_prod uses to spread an (rows, cols,
+ * ncols) problem over the current device's SMs (0 when one row range fills
+ * them; negative DQ4_ERR_DEVICE if there is no usable device).
+ */
+int64_t dq4_nested_out_prod_workspace_bytes(int64_t rows, int64_t cols, int64_t ncols);
 
 /*
  * Nested 4-bit dequantization fused into a tensor-core GEMM (one launch):

@@ -70,6 +70,8 @@ def _load() -> ctypes.CDLL:
     L.dq4_nested_linear.restype = ctypes.c_int
     L.dq4_nested_linear_workspace_bytes.argtypes = [i64, i64, i64]
     L.dq4_nested_linear_workspace_bytes.restype = ctypes.c_int64
+    L.dq4_nested_out_prod_workspace_bytes.argtypes = [i64, i64, i64]
+    L.dq4_nested_out_prod_workspace_bytes.restype = ctypes.c_int64
     L.dq4_nested_host.argtypes = [p, p, p, p, p, f32, i64, i32, i32, i32, p, p, i64, p]
     L.dq4_nested_host.restype = ctypes.c_int
     L.dq4_nested_host_scratch_bytes.argtypes = [i64, i32, i32, i32]
@@ -412,21 +414,41 @@ def int8_correction_prep(A: torch.Tensor, CB: torch.Tensor, SCB: torch.Tensor,
     return subA, subB
 
 
-TRANSIENT_BYTES_DEFAULT = 256 << 20
+# The largest workspace out_prod takes by default: the bound on the transient of "cuda:
+# out_prod dequantizes a 2D weight in row blocks" (at most 256 MiB).
+OUT_PROD_WORKSPACE_MAX = 256 << 20
+_OUT_PROD_WORKSPACES = {}
+
+
+def _out_prod_workspace(rows: int, cols: int, ncols: int, device, handle) -> torch.Tensor:
+    """The cached partial-tile workspace of (device, stream), grown to this problem's size
+    (capped at OUT_PROD_WORKSPACE_MAX; the library takes fewer row ranges when it is)."""
+    need = min(int(get_lib().dq4_nested_out_prod_workspace_bytes(rows, cols, ncols)),
+               OUT_PROD_WORKSPACE_MAX)
+    key = (device.index, handle)
+    ws = _OUT_PROD_WORKSPACES.get(key)
+    if need <= 0:
+        return ws if ws is not None else torch.empty(0, dtype=torch.float32, device=device)
+    if ws is None or ws.numel() * 4 < need:
+        ws = torch.empty((need + 3) // 4, dtype=torch.float32, device=device)
+        _OUT_PROD_WORKSPACES[key] = ws
+    return ws
 
 
 def out_prod(packed: torch.Tensor, scale_codes: torch.Tensor, nested_absmax: torch.Tensor,
              scale_codebook: torch.Tensor, value_codebook: torch.Tensor, offset: float,
              rows: int, cols: int, G: torch.Tensor, blocksize: int = 64,
              nested_blocksize: int = 256, dst: Optional[torch.Tensor] = None,
-             transient: Optional[torch.Tensor] = None,
-             transient_bytes: int = TRANSIENT_BYTES_DEFAULT, stream=None) -> torch.Tensor:
-    """dst = W^T G with W the rows x cols dequantized weight, in bounded row blocks.
+             workspace: Optional[torch.Tensor] = None, bad: Optional[torch.Tensor] = None,
+             stream=None) -> torch.Tensor:
+    """dst = W^T G with W the rows x cols dequantized weight (FP32), decoded in row blocks
+    inside a tcgen05 GEMM with FP32 accuracy.
 
     "cuda: out_prod dequantizes a 2D weight in row blocks" (llama.cpp pull
-    request #4): each block of rows is dequantized to FP32 into ``transient``
-    (at most ``transient_bytes``) and accumulated into dst by a cuBLAS GEMM,
-    beta 0 for the first block and 1 after.  Returns dst (cols x ncols, FP32).
+    request #4), section "What".  ``workspace`` (float32) holds the partial tiles
+    of the row ranges the SMs share; by default a cached buffer per (device,
+    stream) of at most 256 MiB is used, and an empty tensor runs one range
+    straight into dst.  Returns dst (cols x ncols, FP32).
     """
     device = packed.device
     n = rows * cols
@@ -443,17 +465,18 @@ def out_prod(packed: torch.Tensor, scale_codes: torch.Tensor, nested_absmax: tor
     if dst is None:
         dst = torch.empty((cols, ncols), dtype=torch.float32, device=device)
     _check(dst, "dst", torch.float32, cols * ncols, device)
-    if transient is None:
-        rb = max(1, min(rows, transient_bytes // max(1, 4 * cols)))
-        transient = torch.empty(max(1, rb * cols), dtype=torch.float32, device=device)
-    _check(transient, "transient", torch.float32, 1, device)
-    transient_bytes = min(transient_bytes, transient.numel() * 4)
-    handle = torch.cuda.current_blas_handle()
+    if bad is not None:
+        _check(bad, "bad", torch.int32, 1, device)
+    handle = _stream_handle(stream, device)
+    if workspace is None:
+        workspace = _out_prod_workspace(rows, cols, ncols, device, handle)
+    elif workspace.numel() > 0:
+        _check(workspace, "workspace", torch.float32, 1, device)
     st = get_lib().dq4_nested_out_prod(
         _ptr(packed), _ptr(scale_codes), _ptr(nested_absmax), _ptr(scale_codebook),
         _ptr(value_codebook), float(offset), rows, cols, blocksize, nested_blocksize, _ptr(G),
-        ncols, _ptr(dst), _ptr(transient), transient_bytes, handle,
-        _stream_handle(stream, device))
+        ncols, _ptr(dst), _ptr(workspace) if workspace.numel() > 0 else None,
+        workspace.numel() * 4, _ptr(bad), handle)
     if st:
         raise Dq4Error(st, "dq4_nested_out_prod")
     return dst

@@ -14,7 +14,8 @@ CSRC = os.path.join(PKG, "csrc")
 SOURCES = [os.path.join(CSRC, f) for f in
            ("flat.cu", "transposed.cu", "int8_prep.cu", "out_prod.cu", "linear.cu",
             "host_pipeline.cu", "host.cu")]
-HEADERS = [os.path.join(ROOT, "include", "dq4.h"), os.path.join(CSRC, "common.cuh")]
+HEADERS = [os.path.join(ROOT, "include", "dq4.h"), os.path.join(CSRC, "common.cuh"),
+           os.path.join(CSRC, "tcgen05.cuh")]
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libdq4.so")
 

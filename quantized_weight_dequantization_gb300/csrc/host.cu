@@ -103,7 +103,7 @@ using namespace dq4d;
 extern "C" {
 
 // incremented on any change of a signature in dq4.h (2: dq4_nested_linear's workspace)
-constexpr int kAbiVersion = 2;
+constexpr int kAbiVersion = 3;
 int dq4_abi_version(void) { return kAbiVersion; }
 
 const char* dq4_status_string(int status) {
@@ -121,7 +121,7 @@ const char* dq4_status_string(int status) {
     case DQ4_ERR_TOO_LARGE:
       return "the problem needs more scratch than given (DQ4_STATIC_SCRATCH_BLOCKS for the "
              "static array; one row of W for a transient buffer)";
-    case DQ4_ERR_CUBLAS: return "cuBLAS could not be loaded or reported an error";
+    case DQ4_ERR_CUBLAS: return "reserved (no entry point calls cuBLAS)";
     default: return "unknown status";
   }
 }

@@ -39,6 +39,7 @@ def test_header_declares_the_boundary():
                             "dq4_nested_unfused_static", "dq4_status_string",
                             "dq4_int8_correction_prep", "dq4_nested_out_prod",
                             "dq4_nested_linear", "dq4_nested_linear_workspace_bytes",
+                            "dq4_nested_out_prod_workspace_bytes",
                             "dq4_nested_host", "dq4_nested_host_scratch_bytes",
                             "dq4_last_cuda_error"]), names
 
@@ -70,7 +71,7 @@ def test_status_strings(dq):
         s = dq.lib.dq4_status_string(code)
         assert s and s != b"unknown status", code
     assert dq.lib.dq4_status_string(1234) == b"unknown status"
-    assert dq.lib.dq4_abi_version() == 2
+    assert dq.lib.dq4_abi_version() == 3
 
 
 def test_host_validation_before_any_cuda_call(dq):
@@ -121,13 +122,21 @@ def test_host_validation_before_any_cuda_call(dq):
     assert P(None, nz, nz, nz, 4, 4, 4, 2, nz, nz, None, None) == 1
     assert P(nz, nz, nz, nz + 4, 4, 4, 4, 2, nz, nz, None, None) == 6
     assert P(nz, nz, nz + 2, nz, 4, 4, 4, 2, nz, nz, None, None) == 6
-    # row-blocked dequant + GEMM: shape, budget and pointers on the host
+    # row-blocked dequant fused into a GEMM: shape, workspace and pointers on the host
     O = L.dq4_nested_out_prod
-    assert O(nz, nz, nz, nz, nz, 0.0, -1, 8, 64, 256, nz, 4, nz, nz, 1 << 20, nz, None) == 2
-    assert O(nz, nz, nz, nz, nz, 0.0, 8, 8, 64, 256, nz, 0, nz, nz, 1 << 20, nz, None) == 0
-    assert O(nz, nz, nz, nz, nz, 0.0, 8, 256, 64, 256, nz, 4, nz, nz, 1000, nz, None) == 10
-    assert O(nz, nz, nz, nz, nz, 0.0, 8, 8, 64, 256, nz, 4, nz, nz, 1 << 20, None, None) == 1
-    assert O(nz, nz, nz, nz, nz, 0.0, 8, 8, 48, 256, nz, 4, nz, nz, 1 << 20, nz, None) == 3
+    assert O(nz, nz, nz, nz, nz, 0.0, -1, 8, 64, 256, nz, 4, nz, nz, 1 << 20, None, None) == 2
+    assert O(nz, nz, nz, nz, nz, 0.0, 8, 8, 64, 256, nz, 0, nz, nz, 1 << 20, None, None) == 0
+    assert O(nz, nz, nz, nz, nz, 0.0, 8, 256, 64, 256, nz, 4, nz, nz, -1, None, None) == 2
+    assert O(nz, nz, nz, nz, nz, 0.0, 8, 8, 64, 256, None, 4, nz, nz, 1 << 20, None, None) == 1
+    assert O(nz, nz, nz, nz, nz, 0.0, 8, 8, 64, 256, nz, 4, None, nz, 1 << 20, None, None) == 1
+    assert O(nz, nz, nz, nz, nz, 0.0, 8, 8, 48, 256, nz, 4, nz, nz, 1 << 20, None, None) == 3
+    assert O(nz, nz, nz, nz, nz, 0.0, 8, 8, 64, 256, nz, 4, nz, nz + 2, 1 << 20, None,
+             None) == 6  # a workspace that is not 4-byte aligned
+    assert O(nz, nz, nz, nz, nz, 0.0, 8, 8, 64, 256, nz, 4, nz, nz, 1 << 20, nz + 2,
+             None) == 6  # the failure counter likewise
+    assert O(nz + 1, nz, nz, nz, nz, 0.0, 8, 8, 64, 256, nz, 4, nz, nz, 1 << 20, None,
+             None) == 6  # packed is staged in 4-byte words
+    assert L.dq4_nested_out_prod_workspace_bytes(0, 8, 8) == 0
     # fused dequant + GEMM: shapes, dtypes and alignment on the host
     Lr = L.dq4_nested_linear
     assert Lr(nz, 1, nz, nz, nz, nz, nz, 0.0, 4, 8, 100, 64, 256, 1, nz, None, 0, None, None) == 2

@@ -1,16 +1,18 @@
-"""Row-blocked dequantization feeding cuBLAS GEMMs (dst = W^T G), on the GPU.
+"""Row-blocked dequantization fused into a tcgen05 GEMM (dst = W^T G), on the GPU.
 
 "cuda: out_prod dequantizes a 2D weight in row blocks" (llama.cpp pull
-request #4): each row block is dequantized to FP32 into a bounded transient
-and accumulated into dst by a GEMM with beta 0 for the first block and 1
-after; its three new cases run k = 600000 rows at m = 256 (three blocks).
-Checks: (1) integer-valued problems, where every FP32 partial sum is an exact
-integer below 2^24, so dst must equal the float64 oracle exactly whatever
-the GEMM's summation order; (2) the dequantized transient itself is
-bit-identical to the oracle ("Fuse nested scale reconstruction into SM103
-4-bit dequantization", section "Correctness requirements": the dequantized
-tensor passes bitwise equality before any GEMM tolerance); (3) realistic
-NF4 data with an FP32 accumulation tolerance.
+request #4): the weight's row blocks are dequantized to FP32 and a GEMM
+accumulates them into dst, so the whole dequantized weight never exists; its
+three new cases run k = 600000 rows at m = 256.  Here the row blocks are
+decoded inside the GEMM kernel and the FP32 products come from three BF16
+terms per operand.  Checks: (1) the decoded weight bit for bit: a G with one
+1 per column makes each column of dst one row of W, exactly ("Fuse nested
+scale reconstruction into SM103 4-bit dequantization", section "Correctness
+requirements": the dequantized tensor passes bitwise equality before any GEMM
+tolerance); (2) integer-valued problems, where every partial sum is an exact
+integer below 2^24, so dst must equal the float64 oracle exactly whatever the
+summation order; (3) realistic NF4 data within an FP32 accumulation bound;
+(4) determinism, the single-range and split paths, ragged tiles, errors.
 """
 
 import numpy as np
@@ -40,47 +42,72 @@ def to_dev(p):
 
 def run(dq, p, rows, cols, G, **kw):
     t = to_dev(p)
-    Gd = torch.from_numpy(G).to(DEV)
+    Gd = G if isinstance(G, torch.Tensor) else torch.from_numpy(G).to(DEV)
     return dq.out_prod(t["packed"], t["scale_codes"], t["nested_absmax"], t["scale_codebook"],
                        t["value_codebook"], float(p.offset), rows, cols, Gd, p.blocksize,
                        p.nested_blocksize, **kw)
 
 
-@pytest.mark.parametrize("rows,cols,ncols,budget", [
-    (600000, 256, 64, 256 << 20),   # three blocks: 262144 + 262144 + 75712 rows
-    (600000, 256, 64, 1 << 20),     # 1024-row blocks (586 of them)
-    (5000, 100, 7, 100 * 4 * 37),   # 37-row blocks, not group-aligned: per-value path
-    (4097, 4095, 3, 4095 * 4 * 1000),
-    (1, 64, 1, 1 << 20),
+NONE = torch.empty(0, dtype=torch.float32, device=DEV) if torch.cuda.is_available() else None
+
+
+# (rows, cols, ncols, workspace): "auto" = the cached workspace (row ranges over the SMs),
+# "none" = one range straight into dst, an int = a workspace of that many bytes
+@pytest.mark.parametrize("rows,cols,ncols,ws", [
+    (600000, 256, 64, "auto"),    # the page's row count: 76 ranges of 124 stages
+    (600000, 256, 64, "none"),    # one range per CTA: 9375 stages each
+    (5000, 100, 7, "auto"),       # a partial W-column tile, a 16-wide G tile, 4-byte G rows
+    (4097, 4095, 3, "auto"),      # odd columns: 32 W-column tiles, rows not byte-aligned
+    (1, 64, 1, "auto"),           # one row: a partial stage
+    (3000, 512, 300, "auto"),     # three G tiles of 128, the last ragged
+    (70000, 128, 256, 2 * 128 * 256 * 4),  # two G tiles, a workspace for two ranges only
 ])
-def test_integer_exact(dq, rows, cols, ncols, budget):
+def test_integer_exact(dq, rows, cols, ncols, ws):
     p = gen.make_integer_problem(rows, cols, seed=rows % 97)
     G = gen.make_ternary_g(rows, ncols, seed=cols)
-    got = run(dq, p, rows, cols, G, transient_bytes=budget).cpu().numpy()
+    kw = {}
+    if ws == "none":
+        kw["workspace"] = NONE
+    elif isinstance(ws, int):
+        kw["workspace"] = torch.empty(ws // 4, dtype=torch.float32, device=DEV)
+    bad = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got = run(dq, p, rows, cols, G, bad=bad, **kw).cpu().numpy()
     want = oracle.out_prod(p, rows, cols, G, threads=16)
     assert np.array_equal(got.astype(np.float64), want), np.abs(got - want).max()
+    assert int(bad.item()) == 0
 
 
-def test_transient_holds_the_last_block_bit_exact(dq):
-    rows, cols, ncols = 3000, 512, 4
-    p = gen.make_problem(rows * cols, 64, 256, "nf4", 0.5, 0.0371, seed=11)
-    G = gen.make_normal_g(rows, ncols, seed=12)
-    rb = 700  # a 700-row budget, aligned down to a multiple of 16384 / gcd(512, 16384) = 32
-    transient = torch.empty(rb * cols, dtype=torch.float32, device=DEV)
-    run(dq, p, rows, cols, G, transient=transient, transient_bytes=rb * cols * 4)
-    torch.cuda.synchronize()
-    blk = 672
-    last0 = ((rows - 1) // blk) * blk
-    w = oracle.dq4_nested(p, "f32").reshape(rows, cols)
-    got = transient[:(rows - last0) * cols].cpu().numpy().reshape(rows - last0, cols)
-    assert np.array_equal(got.view(np.uint32), w[last0:].view(np.uint32))
+@pytest.mark.parametrize("fmt,bs,nbs,offset,rows,cols", [
+    ("nf4", 64, 256, 0.0371, 2048, 384),
+    ("fp4", 32, 256, -0.52, 1536, 256),
+    ("nf4", 4096, 256, 0.52, 1024, 1000),   # blocks span rows; a ragged W-column tile
+    ("fp4", 128, 1, -0.0371, 777, 130),     # nested blocksize 1, odd rows, ragged tiles
+])
+def test_decoded_rows_bit_exact(dq, fmt, bs, nbs, offset, rows, cols):
+    """G with one 1 per column: column j of dst is row r_j of W, bit for bit (both zeros
+    compare equal: a GEMM adds +0 and -0 terms); every row of W is visited."""
+    p = gen.make_problem(rows * cols, bs, nbs, fmt, 0.5, offset, seed=rows + bs)
+    w = oracle.dq4_nested(p, "f32", threads=16).reshape(rows, cols)
+    t = to_dev(p)
+    ncols = 256
+    order = np.argsort(gen.splitmix64(rows, 91, rows), kind="stable")
+    for j0 in range(0, rows, ncols):
+        sel = order[j0:j0 + ncols]
+        G = torch.zeros((rows, ncols), dtype=torch.float32, device=DEV)
+        G[torch.from_numpy(sel).to(DEV), torch.arange(sel.size, device=DEV)] = 1.0
+        got = dq.out_prod(t["packed"], t["scale_codes"], t["nested_absmax"], t["scale_codebook"],
+                          t["value_codebook"], float(p.offset), rows, cols, G, bs,
+                          nbs).cpu().numpy()[:, :sel.size]
+        want = w[sel].T
+        same = (got.view(np.uint32) == want.view(np.uint32)) | ((got == 0) & (want == 0))
+        assert same.all(), (j0, int((~same).sum()))
 
 
 def test_realistic_weights_within_fp32_accumulation_tolerance(dq):
     rows, cols, ncols = 200000, 256, 32
     p = gen.make_problem(rows * cols, 64, 256, "nf4", 1.0, -0.1, seed=13)
     G = gen.make_normal_g(rows, ncols, seed=14)
-    got = run(dq, p, rows, cols, G, transient_bytes=32 << 20).cpu().numpy().astype(np.float64)
+    got = run(dq, p, rows, cols, G).cpu().numpy().astype(np.float64)
     want = oracle.out_prod(p, rows, cols, G, threads=16)
     w = oracle.dq4_nested(p, "f32", threads=16).reshape(rows, cols).astype(np.float64)
     # FP32 accumulation: |err| <= 4 u K^(3/2) rms(w g) per entry (u = 2^-24), far below a
@@ -90,6 +117,28 @@ def test_realistic_weights_within_fp32_accumulation_tolerance(dq):
     err = np.abs(got - want)
     assert np.all(err <= tol), float((err / tol).max())
     assert float((err / tol).max()) < 0.5
+    # the three-term products: every entry within 8 u K rms(w g) (measured: 2.7).  The tensor
+    # pipe's FP32 accumulation loses up to about an ulp of the accumulator per MMA, six MMAs
+    # per K step here, so the error grows with the accumulation length like u K, not u
+    # sqrt(K); a single BF16 term per operand would be off by ~2^-8 sqrt(K) rms, about 280
+    # u K rms at K = 200000
+    assert float((err / (2.0 ** -24 * rows * rms)).max()) < 8.0
+
+
+def test_split_and_single_range_agree_and_repeat(dq):
+    rows, cols, ncols = 50000, 256, 128
+    p = gen.make_problem(rows * cols, 64, 256, "nf4", 0.5, 0.0371, seed=15)
+    G = torch.from_numpy(gen.make_normal_g(rows, ncols, seed=16)).to(DEV)
+    split = [run(dq, p, rows, cols, G) for _ in range(3)]
+    one = run(dq, p, rows, cols, G, workspace=NONE)
+    torch.cuda.synchronize()
+    assert torch.equal(split[0], split[1]) and torch.equal(split[0], split[2])
+    want = oracle.out_prod(p, rows, cols, G.cpu().numpy(), threads=16)
+    scale = np.abs(want).max()
+    # both within 2e-5 of the largest entry: the kernel adds its accumulator into the output
+    # in FP32 every 512 rows, so one range over all 50000 rows is as accurate as many
+    for got in (split[0], one):
+        assert np.abs(got.cpu().numpy() - want).max() <= 2e-5 * scale
 
 
 def test_zero_rows_and_errors(dq):
@@ -101,7 +150,12 @@ def test_zero_rows_and_errors(dq):
                 t["value_codebook"], 0.0, 0, 64, G, dst=dst)
     assert torch.count_nonzero(dst).item() == 0
     G2 = torch.zeros((64, 3), dtype=torch.float32, device=DEV)
-    with pytest.raises(dq.Dq4Error, match="TOO_LARGE"):
+    buf = torch.zeros(16, dtype=torch.float32, device=DEV)
+    st = dq.lib.dq4_nested_out_prod(
+        t["packed"].data_ptr(), t["scale_codes"].data_ptr(), t["nested_absmax"].data_ptr(),
+        t["scale_codebook"].data_ptr(), t["value_codebook"].data_ptr(), 0.0, 64, 64, 64, 256,
+        G2.data_ptr(), 3, dst.data_ptr(), buf.data_ptr() + 2, 32, None, None)
+    assert st == 6  # DQ4_ERR_ALIGN: a workspace that is not 4-byte aligned
+    with pytest.raises(ValueError, match="rows x ncols"):
         dq.out_prod(t["packed"], t["scale_codes"], t["nested_absmax"], t["scale_codebook"],
-                    t["value_codebook"], 0.0, 64, 64, G2,
-                    transient=torch.empty(16, device=DEV), transient_bytes=64)
+                    t["value_codebook"], 0.0, 64, 64, G2[:10])
