@@ -15,7 +15,7 @@ SOURCES = [os.path.join(CSRC, f) for f in
            ("flat.cu", "transposed.cu", "int8_prep.cu", "out_prod.cu", "linear.cu",
             "host_pipeline.cu", "host.cu")]
 HEADERS = [os.path.join(ROOT, "include", "dq4.h"), os.path.join(CSRC, "common.cuh"),
-           os.path.join(CSRC, "tcgen05.cuh")]
+           os.path.join(CSRC, "tcgen05.cuh"), os.path.join(CSRC, "tmap.cuh")]
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libdq4.so")
 

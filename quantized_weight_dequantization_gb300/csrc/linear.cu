@@ -54,8 +54,7 @@
 // flag, and the CTA drains its copies and MMAs, frees its TMEM and returns.
 #include "common.cuh"
 #include "tcgen05.cuh"
-
-#include <cuda.h>  // CUtensorMap and its enums (the encoder is reached through the runtime)
+#include "tmap.cuh"
 
 #include <mutex>
 
@@ -1027,25 +1026,6 @@ __global__ void __launch_bounds__(kThreadsOf(BX), 1)
 }
 
 // ------------------------------------------------------------- host side
-using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                 const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiled tensor_map_encoder() {
-  static std::once_flag once;
-  static EncodeTiled fn = nullptr;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                         cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiled>(ptr);
-  });
-  return fn;
-}
-
 template <int BX, bool kBF16>
 int launch_linear(const CUtensorMap& tx, const CUtensorMap& tw, const LinArgs& p, int64_t grid,
                   cudaStream_t stream, int dev) {

@@ -66,6 +66,11 @@ SHAPES = [
     # rows % 4 == 0 and cols % 32 == 0 with partial row tiles: 16-bit outputs take the
     # 8-byte (four-row) stores there
     (100, 96), (260, 320), (4, 32), (132, 4096),
+    # the staged kernel (cols % 32 == 0): partial 128-row and 256-column CTA tiles, a last
+    # warp tile of 32 columns, one warp tile, rows % 8 == 0 (16-bit four-row stores) and
+    # rows % 4 == 0
+    (8, 32), (64, 32), (72, 96), (136, 352), (1000, 160), (520, 4064), (16, 8192),
+    (12, 64),
 ]
 
 
@@ -116,6 +121,27 @@ def test_unaligned_output_and_canaries(dq):
                                                              == 0x5A), kind
         assert np.array_equal(bits(view), want_bits(oracle.dq4_nested_transposed(p, rows, cols,
                                                                                   kind)))
+
+
+def test_staged_path_stays_inside_out(dq):
+    """Ragged shapes on the staged kernel (rows and cols not multiples of its tiles, out
+    16-byte aligned inside a guarded buffer): W^T is written exactly and nothing around
+    it."""
+    for rows, cols in ((200, 160), (72, 96), (8, 32)):
+        p = gen.make_problem(rows * cols, 32, 256, "nf4", 0.5, -0.0371, seed=rows + cols)
+        t = to_dev(p)
+        for kind in DT:
+            isz = torch.empty(0, dtype=DT[kind]).element_size()
+            guard = 4096
+            buf = torch.full((rows * cols * isz + 2 * guard,), 0x5A, dtype=torch.uint8,
+                             device=DEV)
+            view = buf[guard:guard + rows * cols * isz].view(DT[kind])
+            run(dq, p, t, rows, cols, kind, out=view)
+            host = buf.cpu().numpy()
+            assert np.all(host[:guard] == 0x5A) and np.all(host[guard + rows * cols * isz:]
+                                                           == 0x5A), (rows, cols, kind)
+            assert np.array_equal(bits(view), want_bits(
+                oracle.dq4_nested_transposed(p, rows, cols, kind))), (rows, cols, kind)
 
 
 def test_zero_and_errors(dq):
