@@ -551,15 +551,18 @@ def run_ours(args):
 
 
 def time_cells(names, dev, stream, transposed: bool, peak: float, batches: int = 7):
-    """Each named cell timed like the main step: back-to-back launches on `stream` over
-    rotating buffer sets (together more than twice the L2, so no launch finds its inputs
-    there), >= 20 warm-up launches, then `batches` batches of >= 2 ms each; per call the
-    median, p10 and p90 over the batches, the effective GB/s and its fraction of `peak`."""
+    """Each named cell timed as back-to-back launches on `stream` over rotating buffer sets
+    (together more than twice the L2, so no launch finds its inputs there): >= 20 warm-up
+    launches, then one batch of >= 2 ms of launches captured in a CUDA graph and replayed
+    `batches` times, so that the record is the device's time per call and not the gaps
+    between Python launches (which exceed the kernel at the 42 MB cells); per call the
+    median, p10 and p90 over the replays, the effective GB/s and its fraction of `peak`."""
     import torch
 
     import quantized_weight_dequantization_gb300 as dq
 
     L = dq.lib
+    stream = torch.cuda.Stream(dev)  # graphs are captured on a stream of their own
     sh = stream.cuda_stream
     l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 << 20))
     codes = {"f16": dq.OUT_F16, "bf16": dq.OUT_BF16, "f32": dq.OUT_F32}
@@ -596,15 +599,20 @@ def time_cells(names, dev, stream, transposed: bool, peak: float, batches: int =
             if call(i):
                 raise SystemExit(f"{name}: launch failed")
         torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for j in range(iters):
+                if call(j):
+                    raise SystemExit(f"{name}: launch failed during capture")
+        graph.replay()  # one untimed replay
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(batches + 1)]
-        j = 0
-        for b in range(batches):
-            ev[b].record(stream)
-            for _ in range(iters):
-                call(j)
-                j += 1
-        ev[batches].record(stream)
+        with torch.cuda.stream(stream):
+            for b in range(batches):
+                ev[b].record(stream)
+                graph.replay()
+            ev[batches].record(stream)
         torch.cuda.synchronize(dev)
+        del graph
         us = [ev[b].elapsed_time(ev[b + 1]) / iters * 1e3 for b in range(batches)]
         med = pct(us, 50)
         gbs = alg / (med * 1e-6) / 1e9
@@ -617,8 +625,9 @@ def time_cells(names, dev, stream, transposed: bool, peak: float, batches: int =
     bar = [v["frac"] for v in rec.values() if v["in_bar"]]
     return {"cells": rec, "bar_min_frac": min(bar) if bar else None,
             "protocol": f"per cell: rotating buffer sets (> 2x L2 in all), >= 20 warm-up "
-                        f"launches, {batches} batches of >= 2 ms of back-to-back launches, "
-                        f"median / p10 / p90 per call over the batches"}
+                        f"launches, >= 2 ms of back-to-back launches captured in one CUDA "
+                        f"graph and replayed {batches} times, median / p10 / p90 per call "
+                        f"over the replays"}
 
 
 def link_bound(h2d_bytes: int, d2h_bytes: int, dev, reps: int = 5):

@@ -26,7 +26,11 @@
 //    hint: every byte is touched once.
 //  * Launched with programmatic dependent launch: CTAs of a launch may be
 //    scheduled while the previous kernel in the stream finishes, and wait
-//    for its completion (griddepcontrol.wait) before touching memory.
+//    for its completion (griddepcontrol.wait) before reading or writing
+//    memory.  In grids of up to 8 waves each warp first asks L2 for its first
+//    tile's lines (prefetch.global.L2, which returns nothing and so changes no
+//    value read after the wait), so its DRAM reads start during the previous
+//    kernel's tail and the codebook staging.
 //  * Values after the last whole word (fewer than one word, including an
 //    odd padding nibble) are written one by one by CTA 0.  Unaligned
 //    `packed` / `out` pointers take a per-value kernel with the same math.
@@ -128,18 +132,41 @@ __global__ void __launch_bounds__(kThreads) dq4_vec_kernel(const Args a) {
   constexpr int64_t kTile = 32 * Tile<OUT>::U;
   __shared__ float s_vcb[16];
   __shared__ float s_scb[NESTED ? 256 : 1];
-#if DQ4_PDL
-  // No global memory is touched before the previous grid in the stream has
-  // completed; dependents may be scheduled once every CTA here has started.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;");
-#endif
-
   const int64_t n_words = a.n >> T::kLog2Vals;
   const int wshift = a.log2_bs - T::kLog2Vals;  // log2(words per outer block)
   const int lane = threadIdx.x & 31;
   const int64_t warp = (int64_t(blockIdx.x) * kThreads + threadIdx.x) >> 5;
   const int64_t stride = ((int64_t(gridDim.x) * kThreads) >> 5) * kTile;
+#if DQ4_PDL
+#if DQ4_L2_PREFETCH
+  // A prefetch returns nothing to the thread and L2 is the point of coherence, so asking
+  // for these lines before the previous grid completes changes no value this kernel
+  // reads; it only starts their DRAM reads early.  One lane per 128-byte line of the
+  // tile's packed words, one for its first scale codes and one for its first absmax.
+  // (The host sets prefetch_ctas to the grid for small grids and to 0 for large ones.)
+  if (blockIdx.x < a.prefetch_ctas) {
+    using Word = typename T::Word;
+    constexpr int kLines = int(kTile * sizeof(Word) / 128);
+    const int64_t base0 = warp * kTile;
+    if (base0 < n_words) {
+      const char* pk = reinterpret_cast<const char*>(a.packed) + base0 * int64_t(sizeof(Word));
+      const int64_t bytes = (n_words - base0) * int64_t(sizeof(Word));
+      const int64_t b0 = base0 >> wshift;
+      if (lane < kLines && int64_t(lane) * 128 < bytes) {
+        asm volatile("prefetch.global.L2 [%0];" :: "l"(pk + lane * 128));
+      } else if (NESTED && lane == kLines) {
+        asm volatile("prefetch.global.L2 [%0];" :: "l"(a.codes + b0));
+      } else if (lane == kLines + 1) {
+        asm volatile("prefetch.global.L2 [%0];" :: "l"(a.absmax + (NESTED ? b0 >> a.log2_nbs : b0)));
+      }
+    }
+  }
+#endif
+  // No global memory is read or written before the previous grid in the stream has
+  // completed; dependents may be scheduled once every CTA here has started.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+#endif
 
   int64_t base = warp * kTile;
   const bool active = base < n_words;  // warp-uniform
@@ -219,7 +246,11 @@ int launch_dq4(const Args& a, cudaStream_t stream) {
     const int64_t cap = DQ4_CTAS_PER_SM > 0 ? int64_t(sms) * DQ4_CTAS_PER_SM : kMaxGrid;
     if (grid > cap) grid = cap;
     if (grid < 1) grid = 1;
-    return launch_kernel(dq4_vec_kernel<OUT, NESTED>, grid, stream, a);
+    static std::atomic<int> vec_occ[kMaxDevices];
+    Args b = a;
+    const int64_t wave = int64_t(sms) * ctas_per_sm(dq4_vec_kernel<OUT, NESTED>, dev, vec_occ);
+    b.prefetch_ctas = grid <= int64_t(DQ4_PREFETCH_WAVES) * wave ? grid : 0;
+    return launch_kernel(dq4_vec_kernel<OUT, NESTED>, grid, stream, b);
   } else {
     static std::atomic<int> occ_cache[kMaxDevices];
     auto kernel = dq4_scalar_kernel<OUT, NESTED>;

@@ -93,6 +93,7 @@ Args make_args(const uint8_t* packed, const uint8_t* codes, const float* absmax,
   a.offset = offset;
   a.log2_bs = log2_exact(blocksize);
   a.log2_nbs = log2_exact(nested_blocksize);
+  a.prefetch_ctas = 0;
   return a;
 }
 
