@@ -38,6 +38,7 @@
 // and the CTA leaves its loops, waits for its MMAs and frees its TMEM.
 #include "common.cuh"
 #include "tcgen05.cuh"
+#include "tmap.cuh"
 
 #include <atomic>
 
@@ -67,17 +68,18 @@ static_assert(kOpATmem + kOpGroups * kOpASlotCols <= kOpTmemCols, "A slots fit T
 __device__ constexpr int kOpPassW[6] = {2, 1, 0, 1, 0, 0};
 __device__ constexpr int kOpPassG[6] = {0, 1, 2, 0, 1, 0};
 
-template <int NB>
+template <int NB, bool kTma>
 struct OpSmem {
   static_assert(NB == 16 || NB == 32 || NB == 64 || NB == 128, "N tile");
   static constexpr int kPlane = NB * 128;  // one B plane: NB rows (G columns) x 64 BF16
   static constexpr int kSlot = kOpPlanes * kPlane;
-  // A group's staging of one stage's inputs (cp.async): the G rows (kOpK x NB FP32), and per
-  // row of W's tile its packed bytes (17 aligned words: 128 nibbles from any start), scale
-  // codes (2 aligned words: at most 5 blocks of >= 32 values) and absmax (8 aligned floats:
-  // at most 5 groups)
+  // A group's staging of one stage's inputs: the G rows (kOpK x NB FP32), and per row of W's
+  // tile its packed bytes (17 aligned words by cp.async: 128 nibbles from any start; with
+  // kTma one 64-byte TMA box row, the rows starting on 32-value boundaries), scale codes
+  // (2 aligned words: at most 5 blocks of >= 32 values) and absmax (8 aligned floats: at
+  // most 5 groups)
   static constexpr int kGRowBytes = NB * 4;
-  static constexpr int kWRowBytes = 68, kCRowBytes = 8, kARowBytes = 32;
+  static constexpr int kWRowBytes = kTma ? 64 : 68, kCRowBytes = 8, kARowBytes = 32;
   static constexpr int kGOff = 0;
   static constexpr int kWOff = kGOff + kOpK * kGRowBytes;
   static constexpr int kCOff = kWOff + kOpK * kWRowBytes;
@@ -86,15 +88,17 @@ struct OpSmem {
   // (first block) on
   static constexpr int kSOff = kAOff + kOpK * kARowBytes;
   static constexpr int kSRowBytes = 32;
-  static constexpr int kStage = kSOff + kOpK * kSRowBytes;
+  // (1024-byte aligned: TMA boxes land at its start)
+  static constexpr int kStage = (kSOff + kOpK * kSRowBytes + 1023) / 1024 * 1024;
   static constexpr int kStageOff = kOpGroups * kSlot;
   static constexpr int kBarOff = kStageOff + kOpGroups * kStage;
   // accumulator buffers in TMEM (columns b NB ..): two when they fit beside the A slots, so
   // a chain is added into the output while the next one accumulates
   static constexpr int kAccBufs = 2;
   static_assert(kAccBufs * NB <= int(kOpATmem), "accumulators fit before the A slots");
-  // full and empty per slot; acc_full and acc_empty per accumulator buffer; acc_done
-  static constexpr int kBars = 2 * kOpGroups + 2 * kAccBufs + 1;
+  // full and empty per slot; acc_full and acc_empty per accumulator buffer; acc_done; the
+  // TMA staging's completion per group
+  static constexpr int kBars = 2 * kOpGroups + 2 * kAccBufs + 1 + kOpGroups;
   static constexpr int kUsed = kBarOff + 8 * kBars + 1024;  // + alignment slack
   // more than half an SM's shared memory: one CTA per SM, so the 512-column TMEM
   // allocation never waits for another CTA
@@ -110,6 +114,9 @@ struct OpArgs {
   int64_t rows_per_range;  // a multiple of kOpK
   int tiles_c;            // W-column tiles (blockIdx.x = tile_j * tiles_c + tile_c)
   int g_vec4;             // G's rows start 16-byte aligned (ncols % 4 == 0, G aligned)
+  // every row of W starts on an 8-value word and meets the scale blocks at the same column
+  // offsets (cols % 8 == 0, and cols % blocksize == 0 or blocksize % cols == 0)
+  int rows_alike;
   int* bad;               // optional device counter of timed-out waits
 };
 
@@ -169,9 +176,11 @@ __device__ __forceinline__ void split3(float x, uint32_t& t0, uint32_t& t1, uint
   t2 = __float_as_uint(__fsub_rn(r, __uint_as_float(t1)));  // exact, at most 8 bits
 }
 
-template <int NB>
-__global__ void __launch_bounds__(kOpThreads, 1) dq4_outprod_kernel(const OpArgs p) {
-  using S = OpSmem<NB>;
+template <int NB, bool kTma>
+__global__ void __launch_bounds__(kOpThreads, 1)
+    dq4_outprod_kernel(const __grid_constant__ CUtensorMap tm_g,
+                       const __grid_constant__ CUtensorMap tm_w, const OpArgs p) {
+  using S = OpSmem<NB, kTma>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ float s_scb[256];
   __shared__ float s_vcb[16];
@@ -188,6 +197,8 @@ __global__ void __launch_bounds__(kOpThreads, 1) dq4_outprod_kernel(const OpArgs
   auto acc_full = [&](int b) { return bar0 + 8 * (2 * kOpGroups + b); };
   auto acc_empty = [&](int b) { return bar0 + 8 * (2 * kOpGroups + kAccBufs + b); };
   const uint32_t acc_done = bar0 + 8 * (2 * kOpGroups + 2 * kAccBufs);
+  // staged(g): the TMA boxes of group g's current stage landed (kTma)
+  auto staged = [&](int g) { return bar0 + 8 * (2 * kOpGroups + 2 * kAccBufs + 1 + g); };
   volatile int* abort_flag = &s_abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   auto fail = [&]() {
@@ -215,8 +226,13 @@ __global__ void __launch_bounds__(kOpThreads, 1) dq4_outprod_kernel(const OpArgs
         mbar_init(acc_empty(b), kOpMmaWarp);  // every producer warp
       }
       mbar_init(acc_done, 1);
+      for (int g = 0; g < kOpGroups; ++g) mbar_init(staged(g), 1);
       *abort_flag = 0;
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+      if (kTma) {
+        asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tm_g)));
+        asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tm_w)));
+      }
     }
   } else if (tid < 256) {
     static_assert(kOpMmaWarp * 32 >= 256, "the producers load the scale codebook");
@@ -337,10 +353,23 @@ __global__ void __launch_bounds__(kOpThreads, 1) dq4_outprod_kernel(const OpArgs
     const int64_t npk = (p.w.n + 1) / 2, nblk = (p.w.n + (int64_t(1) << p.w.log2_bs) - 1) >>
                                                p.w.log2_bs;
     const int64_t ngrp = (nblk + (int64_t(1) << p.w.log2_nbs) - 1) >> p.w.log2_nbs;
+    bool tma_pending = false;  // (thread tg 0) a stage's boxes are in flight, not yet waited for
+    int tma_l = 0;             // (thread tg 0) the local stage they belong to
     auto stage_in = [&](int64_t r0) {
       // G rows r0 .. r0 + 63, columns j0 .. j0 + NB - 1 (rows and columns past the ends are
-      // left alone: the split reads zeros for them)
-      if (p.g_vec4) {
+      // left alone, or with kTma zero-filled past the matrix: a whole stage of rows reads
+      // them only into dst columns that are never stored, a partial one selects zeros); with
+      // kTma also W's packed rows, one box each, completing on staged(group)
+      if constexpr (kTma) {
+        if (tg == 0) {
+          mbar_expect(staged(group), kOpK * S::kGRowBytes + kOpK * S::kWRowBytes);
+          tma_load_2d(stg + S::kGOff, reinterpret_cast<uint64_t>(&tm_g), int(j0), int(r0),
+                      staged(group));
+          tma_load_2d(stg + S::kWOff, reinterpret_cast<uint64_t>(&tm_w), int(c0 / 2), int(r0),
+                      staged(group));
+          tma_pending = true;
+        }
+      } else if (p.g_vec4) {
         for (int q = tg; q < kOpK * NB / 4; q += kOpGroupThreads) {
           const int rr = q / (NB / 4), jq = q - rr * (NB / 4);
           const int64_t r = r0 + rr, j = j0 + 4 * jq;
@@ -365,7 +394,18 @@ __global__ void __launch_bounds__(kOpThreads, 1) dq4_outprod_kernel(const OpArgs
           const int64_t i0 = r * p.cols + c0;  // the tile row's first value
           const int64_t b0 = i0 >> p.w.log2_bs;
           const uint32_t wrow = stg + S::kWOff + rr * S::kWRowBytes;
-          if (part < 3) {
+          if (kTma) {  // the codes and two halves of the absmax words, one part each
+            const int64_t a0 = (b0 >> p.w.log2_nbs) & ~int64_t(3);
+            if (part == 0) {
+              for (int k = 0; k < 2; ++k)
+                stage_word(stg + S::kCOff + rr * S::kCRowBytes + 4 * k, p.w.codes,
+                           (b0 >> 2) + k, nblk);
+            } else if (part < 3) {
+              for (int k = 4 * (part - 1); k < 4 * part; ++k)
+                if (a0 + k < ngrp)
+                  cp_async4(stg + S::kAOff + rr * S::kARowBytes + 4 * k, p.w.absmax + a0 + k);
+            }
+          } else if (part < 3) {
             for (int k = part * 6; k < (part < 2 ? part * 6 + 6 : 17); ++k)
               stage_word(wrow + 4 * k, p.w.packed, (i0 >> 3) + k, npk);
           } else {
@@ -386,6 +426,7 @@ __global__ void __launch_bounds__(kOpThreads, 1) dq4_outprod_kernel(const OpArgs
       const int64_t r0 = r_begin + int64_t(l) * kOpK;
       group_bar();  // every thread of the group is done with the previous stage's staging
       stage_in(r0);
+      if (kTma) tma_l = l;
       // the chains before that of stage l - 2 (whose slot this stage reuses): added out one
       // chain after they completed, so the MMAs, which need a buffer back kAccBufs chains
       // later, find it free (the MMAs of those chains were issued: their stages are decoded)
@@ -403,6 +444,16 @@ __global__ void __launch_bounds__(kOpThreads, 1) dq4_outprod_kernel(const OpArgs
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       }
       cp_async_wait_all();
+      if constexpr (kTma) {  // the stage's boxes landed (every thread acquires them)
+        const bool got =
+            __all_sync(0xFFFFFFFFu, mbar_wait(staged(group), uint32_t(l >> 1) & 1u));
+        if (tg == 0 && got) tma_pending = false;
+        if (!got) {
+          if (lane == 0 && !*abort_flag) fail();
+          ok = false;
+          break;
+        }
+      }
       group_bar();  // every thread's copies landed
       // each row's nested scales (separately rounded FP32 multiply and add), for the blocks
       // b0 + k it touches: 64 rows x 5 blocks over the group's threads
@@ -426,29 +477,54 @@ __global__ void __launch_bounds__(kOpThreads, 1) dq4_outprod_kernel(const OpArgs
       // plane) at a time:
       // with m8 = the row's first value's offset in its aligned 8-value word and mb = its
       // offset in its block, value c0 + t sits in byte (m8 + t) / 2 of the staged words and
-      // in block (mb + t) >> log2 blocksize of the row's scales
+      // in block (mb + t) >> log2 blocksize of the row's scales.  The staged bytes and scales
+      // are read with plain loads (no shared-memory store comes between them and the
+      // barrier above), so the compiler may issue a batch's loads together.
+      const uint8_t* st_p = base + (stg - sbase);
+      const int rows_left = r_end - r0 < kOpK ? int(r_end - r0) : kOpK;
+      const uint32_t i0s = uint32_t(r0 * p.cols + c0);  // low bits suffice
+      const uint32_t cols32 = uint32_t(p.cols), bs_mask = (1u << p.w.log2_bs) - 1u;
+      // A whole stage of alike rows: value t of every row sits at byte t / 2 of its staged
+      // word run (c0 and the rows start on 8-value words) and in the same slot of its scales,
+      // so the row loop needs no per-row index arithmetic.  Columns past cols then decode
+      // staged bytes of no meaning, into TMEM lanes whose sums are never stored.
+      const bool fast = p.rows_alike && rows_left == kOpK;  // uniform across the group
+      const uint8_t* w_t = st_p + S::kWOff + (t >> 1);
+      const uint32_t nib_shift = (t & 1) ? 0u : 4u;
+      const float* s_t = reinterpret_cast<const float*>(st_p + S::kSOff) +
+                         (p.cols % (int64_t(1) << p.w.log2_bs) == 0
+                              ? (((uint32_t(c0) & bs_mask) + uint32_t(t)) >> p.w.log2_bs)
+                              : 0u);
 #pragma unroll 1
       for (int h = 2 * hf; h < 2 * hf + 2; ++h) {
+        float v[16];
+        if (fast) {
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            const int rr = h * 16 + q;
+            const uint32_t nib = (uint32_t(w_t[rr * S::kWRowBytes]) >> nib_shift) & 0xFu;
+            v[q] = __fmul_rn(s_vcb[nib], s_t[rr * (S::kSRowBytes / 4)]);
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            const int rr = h * 16 + q;
+            const uint32_t i0lo = i0s + uint32_t(rr) * cols32;
+            const uint32_t m8 = (i0lo & 7u) + uint32_t(t);
+            const uint32_t mb = (i0lo & bs_mask) + uint32_t(t);
+            const uint32_t byte = st_p[S::kWOff + rr * S::kWRowBytes + (m8 >> 1)];
+            const uint32_t nib = (m8 & 1u) ? (byte & 0xFu) : (byte >> 4);
+            const float sc = *reinterpret_cast<const float*>(
+                st_p + S::kSOff + rr * S::kSRowBytes + 4 * (mb >> p.w.log2_bs));
+            v[q] = (c_ok && rr < rows_left) ? __fmul_rn(s_vcb[nib], sc) : 0.f;
+          }
+        }
         uint32_t t0[8], t1[8], t2[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           uint32_t e0[2], e1[2], e2[2];
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int rr = h * 16 + 2 * k + e;
-            float v = 0.f;
-            if (c_ok && r0 + rr < r_end) {
-              const uint32_t i0lo = uint32_t((r0 + rr) * p.cols + c0);  // low bits suffice
-              const uint32_t m8 = (i0lo & 7u) + uint32_t(t);
-              const uint32_t mb = (i0lo & ((1u << p.w.log2_bs) - 1u)) + uint32_t(t);
-              const uint32_t byte = ld_shared_u8(stg + S::kWOff + rr * S::kWRowBytes + (m8 >> 1));
-              const uint32_t nib = (m8 & 1u) ? (byte & 0xFu) : (byte >> 4);
-              const float sc = ld_shared_f32(stg + S::kSOff + rr * S::kSRowBytes +
-                                             4 * (mb >> p.w.log2_bs));
-              v = __fmul_rn(s_vcb[nib], sc);
-            }
-            split3(v, e0[e], e1[e], e2[e]);
-          }
+          for (int e = 0; e < 2; ++e) split3(v[2 * k + e], e0[e], e1[e], e2[e]);
           t0[k] = hi_pair(e0[0], e0[1]);
           t1[k] = hi_pair(e1[0], e1[1]);
           t2[k] = hi_pair(e2[0], e2[1]);
@@ -457,41 +533,55 @@ __global__ void __launch_bounds__(kOpThreads, 1) dq4_outprod_kernel(const OpArgs
         tmem_st<8>(t_lane + 1 * kOpAPlaneCols + h * 8, t1);
         tmem_st<8>(t_lane + 2 * kOpAPlaneCols + h * 8, t2);
       }
-      // G column j0 + jl over half the stage's rows (thread tg: column tg % 128, rows of
-      // chunks 4 (tg / 128) ..), split and transposed: plane row jl = the G column, 64 BF16 of
-      // K = 128 bytes, 16-byte chunk w stored at w ^ (jl & 7) within the 1024-byte group of
-      // 8 rows
-      if ((tg & 127) < NB) {
-        const int jl = tg & 127, gh = tg >> 7;
-        const bool j_ok = j0 + jl < p.ncols;
-        const uint32_t row = b_slot + (jl >> 3) * 1024 + (jl & 7) * 128;
-#pragma unroll 2
-        for (int w = 4 * gh; w < 4 * gh + 4; ++w) {  // 8 rows of K per 16-byte chunk
-          uint32_t q0[4], q1[4], q2[4];
+      // G column j0 + jl over kGChunks of the stage's 8 chunks of 8 rows (thread tg: column
+      // tg % NB, chunks kGChunks (tg / NB) ..; every thread of the group takes a share when
+      // NB >= 32), split and transposed: plane row jl = the G column, 64 BF16 of K = 128
+      // bytes, 16-byte chunk w stored at w ^ (jl & 7) within the 1024-byte group of 8 rows.
+      // A chunk's 8 values are loaded before its plane stores.
+      {
+        constexpr int kTpc = kOpGroupThreads / NB < 8 ? kOpGroupThreads / NB : 8;
+        constexpr int kGChunks = 8 / kTpc;
+        if (tg < NB * kTpc) {
+          const int jl = tg % NB, w0 = (tg / NB) * kGChunks;
+          const bool j_ok = j0 + jl < p.ncols;
+          const uint32_t row = b_slot + (jl >> 3) * 1024 + (jl & 7) * 128;
+          const float* gp = reinterpret_cast<const float*>(st_p + S::kGOff) + jl;
+          constexpr int kBatch = kGChunks < 2 ? kGChunks : 2;  // chunks loaded together
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            uint32_t e0[2], e1[2], e2[2];
+          for (int wb = 0; wb < kGChunks; wb += kBatch) {
+          float g[8 * kBatch];
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int rr = w * 8 + 2 * k + e;
-              const float g = (j_ok && r0 + rr < r_end)
-                                  ? ld_shared_f32(stg + S::kGOff + rr * S::kGRowBytes + 4 * jl)
-                                  : 0.f;
-              split3(g, e0[e], e1[e], e2[e]);
-            }
-            q0[k] = hi_pair(e0[0], e0[1]);
-            q1[k] = hi_pair(e1[0], e1[1]);
-            q2[k] = hi_pair(e2[0], e2[1]);
+          for (int q = 0; q < 8 * kBatch; ++q) {
+            const int rr = 8 * (w0 + wb) + q;
+            const float x = gp[rr * (S::kGRowBytes / 4)];
+            // (a whole stage keeps columns past ncols as staged: they feed only dst
+            // columns that are never stored)
+            g[q] = (rows_left == kOpK || (j_ok && rr < rows_left)) ? x : 0.f;
           }
-          const uint32_t off = row + ((w ^ (jl & 7)) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                       :: "r"(off), "r"(q0[0]), "r"(q0[1]), "r"(q0[2]), "r"(q0[3]) : "memory");
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                       :: "r"(off + S::kPlane), "r"(q1[0]), "r"(q1[1]), "r"(q1[2]), "r"(q1[3])
-                       : "memory");
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                       :: "r"(off + 2 * S::kPlane), "r"(q2[0]), "r"(q2[1]), "r"(q2[2]),
-                          "r"(q2[3]) : "memory");
+#pragma unroll
+          for (int wq = 0; wq < kBatch; ++wq) {
+            const int w = w0 + wb + wq;
+            uint32_t q0[4], q1[4], q2[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              uint32_t e0[2], e1[2], e2[2];
+#pragma unroll
+              for (int e = 0; e < 2; ++e) split3(g[8 * wq + 2 * k + e], e0[e], e1[e], e2[e]);
+              q0[k] = hi_pair(e0[0], e0[1]);
+              q1[k] = hi_pair(e1[0], e1[1]);
+              q2[k] = hi_pair(e2[0], e2[1]);
+            }
+            const uint32_t off = row + ((w ^ (jl & 7)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                         :: "r"(off), "r"(q0[0]), "r"(q0[1]), "r"(q0[2]), "r"(q0[3]) : "memory");
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                         :: "r"(off + S::kPlane), "r"(q1[0]), "r"(q1[1]), "r"(q1[2]), "r"(q1[3])
+                         : "memory");
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                         :: "r"(off + 2 * S::kPlane), "r"(q2[0]), "r"(q2[1]), "r"(q2[2]),
+                            "r"(q2[3]) : "memory");
+          }
+          }
         }
       }
       // the B planes (generic writes) visible to the MMAs (async proxy), the A planes'
@@ -502,6 +592,8 @@ __global__ void __launch_bounds__(kOpThreads, 1) dq4_outprod_kernel(const OpArgs
       __syncwarp();
       if (lane == 0) mbar_arrive(full(group));
     }
+    // boxes still in flight after a failed wait land before the CTA leaves
+    if (kTma && tma_pending) mbar_wait(staged(group), uint32_t(tma_l >> 1) & 1u);
     // the remaining chains, the last one after the last stage; then the sums out
     for (; ok && flushed < nchains; ++flushed) ok = flush(flushed);
     if (ok && reads && c_ok) {
@@ -531,18 +623,50 @@ __global__ void outprod_reduce_kernel(const float* __restrict__ part, int ranges
   }
 }
 
-template <int NB>
-int launch_outprod(const OpArgs& a, int tiles, int ranges, cudaStream_t st, int dev) {
-  using S = OpSmem<NB>;
+template <int NB, bool kTma>
+int launch_outprod(const CUtensorMap& tm_g, const CUtensorMap& tm_w, const OpArgs& a, int tiles,
+                   int ranges, cudaStream_t st, int dev) {
+  using S = OpSmem<NB, kTma>;
   static std::atomic<int> configured[kMaxDevices];
   if (dev >= 0 && dev < kMaxDevices && !configured[dev].load()) {
     const cudaError_t e = cudaFuncSetAttribute(
-        dq4_outprod_kernel<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kBytes);
+        dq4_outprod_kernel<NB, kTma>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kBytes);
     if (e != cudaSuccess) return fail_cuda(DQ4_ERR_LAUNCH, e);
     configured[dev].store(1);
   }
-  dq4_outprod_kernel<NB><<<dim3(unsigned(tiles), unsigned(ranges)), kOpThreads, S::kBytes, st>>>(a);
+  dq4_outprod_kernel<NB, kTma>
+      <<<dim3(unsigned(tiles), unsigned(ranges)), kOpThreads, S::kBytes, st>>>(tm_g, tm_w, a);
   return check_launch();
+}
+
+// The tensor maps of the TMA staging: G as rows x ncols FP32 (NB x 64 boxes) and the packed
+// weight as rows x cols / 2 bytes (64 x 64 boxes: 128 values of 64 rows), both unswizzled
+// and zero-filled past the matrix.  False when the shape or the pointers do not allow them
+// (then the kernel stages by cp.async).
+bool outprod_tensor_maps(const uint8_t* packed, const float* G, int64_t rows, int64_t cols,
+                         int64_t ncols, int nb, bool rows_alike, CUtensorMap* tm_g,
+                         CUtensorMap* tm_w) {
+  if (!rows_alike || cols % 32 != 0 || ncols % 4 != 0 || misaligned(G, 16) ||
+      misaligned(packed, 16) || rows >= (int64_t(1) << 31) || ncols >= (int64_t(1) << 31) ||
+      cols >= (int64_t(1) << 32))
+    return false;
+  EncodeTiled encode = tensor_map_encoder();
+  if (!encode) return false;
+  const cuuint32_t estride[2] = {1, 1};
+  const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(ncols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(ncols) * 4};
+  const cuuint32_t gbox[2] = {static_cast<cuuint32_t>(nb), static_cast<cuuint32_t>(kOpK)};
+  if (encode(tm_g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(G), gdim, gstride, gbox,
+             estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  const cuuint64_t wdim[2] = {static_cast<cuuint64_t>(cols / 2), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t wstride[1] = {static_cast<cuuint64_t>(cols / 2)};
+  const cuuint32_t wbox[2] = {static_cast<cuuint32_t>(kOpM / 2), static_cast<cuuint32_t>(kOpK)};
+  return encode(tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(packed), wdim,
+                wstride, wbox, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
 }
 
 // How a problem runs: the G-column tile width, the tiles, and the row ranges.
@@ -623,13 +747,24 @@ int dq4_nested_out_prod(const uint8_t* packed, const uint8_t* scale_codes,
   a.rows_per_range = pl.rows_per_range;
   a.tiles_c = int(pl.tiles_c);
   a.g_vec4 = (ncols % 4 == 0 && !misaligned(G, 16)) ? 1 : 0;
+  a.rows_alike = (cols % 8 == 0 && (cols % blocksize == 0 || blocksize % cols == 0)) ? 1 : 0;
   a.bad = bad;
+  CUtensorMap tm_g, tm_w;
+  std::memset(&tm_g, 0, sizeof tm_g);
+  std::memset(&tm_w, 0, sizeof tm_w);
+  const bool tma =
+      outprod_tensor_maps(packed, G, rows, cols, ncols, pl.nb, a.rows_alike != 0, &tm_g, &tm_w);
+  const int T = int(pl.tiles), R = int(pl.ranges);
   int status;
-  switch (pl.nb) {
-    case 16: status = launch_outprod<16>(a, int(pl.tiles), int(pl.ranges), st, dev); break;
-    case 32: status = launch_outprod<32>(a, int(pl.tiles), int(pl.ranges), st, dev); break;
-    case 64: status = launch_outprod<64>(a, int(pl.tiles), int(pl.ranges), st, dev); break;
-    default: status = launch_outprod<128>(a, int(pl.tiles), int(pl.ranges), st, dev); break;
+  switch (pl.nb * 2 + (tma ? 1 : 0)) {
+    case 32: status = launch_outprod<16, false>(tm_g, tm_w, a, T, R, st, dev); break;
+    case 33: status = launch_outprod<16, true>(tm_g, tm_w, a, T, R, st, dev); break;
+    case 64: status = launch_outprod<32, false>(tm_g, tm_w, a, T, R, st, dev); break;
+    case 65: status = launch_outprod<32, true>(tm_g, tm_w, a, T, R, st, dev); break;
+    case 128: status = launch_outprod<64, false>(tm_g, tm_w, a, T, R, st, dev); break;
+    case 129: status = launch_outprod<64, true>(tm_g, tm_w, a, T, R, st, dev); break;
+    case 256: status = launch_outprod<128, false>(tm_g, tm_w, a, T, R, st, dev); break;
+    default: status = launch_outprod<128, true>(tm_g, tm_w, a, T, R, st, dev); break;
   }
   if (status || pl.ranges == 1) return status;
   const int64_t count = cols * ncols;
