@@ -141,6 +141,24 @@ def test_split_and_single_range_agree_and_repeat(dq):
         assert np.abs(got.cpu().numpy() - want).max() <= 2e-5 * scale
 
 
+@pytest.mark.parametrize("rows,cols,ncols", [(20000, 256, 64), (3000, 512, 300), (777, 384, 16)])
+def test_tma_and_copy_staging_agree(dq, rows, cols, ncols):
+    """The same problem through the TMA staging (G 16-byte aligned) and the cp.async staging
+    (G one float off 16 bytes): the decode and the MMA order are the same, so dst agrees bit
+    for bit, and both are exact on integer-valued data."""
+    p = gen.make_integer_problem(rows, cols, seed=rows % 89)
+    G = torch.from_numpy(gen.make_ternary_g(rows, ncols, seed=cols)).to(DEV)
+    buf = torch.empty(rows * ncols + 4, dtype=torch.float32, device=DEV)
+    G1 = buf[1:1 + rows * ncols].view(rows, ncols)  # 4 bytes past a 16-byte boundary
+    G1.copy_(G)
+    assert G.data_ptr() % 16 == 0 and G1.data_ptr() % 16 == 4
+    a = run(dq, p, rows, cols, G).cpu()
+    b = run(dq, p, rows, cols, G1).cpu()
+    assert torch.equal(a, b)
+    want = oracle.out_prod(p, rows, cols, G.cpu().numpy(), threads=16)
+    assert np.array_equal(a.numpy().astype(np.float64), want)
+
+
 def test_zero_rows_and_errors(dq):
     p = gen.make_integer_problem(64, 64, seed=1)
     t = to_dev(p)
