@@ -50,7 +50,7 @@ DEFAULT_CELL = "C4a"
 # Every cell of the >= 80 % bar (the >= 4096x11008 weights: C3, C4, and C5 at each block size,
 # whose four offsets change arithmetic, not traffic, so each block size is timed at one of
 # them) and the smaller C1 / C2 cells, timed one by one for the `cells` record.
-DEFAULT_CELLS = (["C1", "C2a", "C2b", "C3a", "C3b", "C3c", "C3d", "C4b", "C4c", "C4d"]
+DEFAULT_CELLS = (["C1", "C2a", "C2b", "C3a", "C3b", "C3c", "C3d", "C4a", "C4b", "C4c", "C4d"]
                  + [f"C5-bs{bs}-off{off:+g}" for bs, off in
                     zip((32, 64, 128, 256, 512, 1024, 2048, 4096),
                         (-1.0, -1e-3, 1e-3, 1.0, -1.0, -1e-3, 1e-3, 1.0))])
