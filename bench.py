@@ -640,10 +640,11 @@ def time_cells(names, dev, stream, transposed: bool, peak: float, batches: int =
                         f"over the replays"}
 
 
-def link_bound(h2d_bytes: int, d2h_bytes: int, dev, reps: int = 5):
+def link_bound(h2d_bytes: int, d2h_bytes: int, dev, reps: int = 7):
     """The host link alone for one e2e step's byte counts: one pinned H2D and one pinned
     D2H cudaMemcpyAsync timed apart (GB/s) and at once on two streams (ms, the e2e step's
-    floor: its pipeline overlaps the two directions)."""
+    floor: its pipeline overlaps the two directions).  Each is the fastest of `reps`
+    repetitions after one untimed: a floor, which a slowed repetition must not raise."""
     import torch
 
     hin = torch.empty(h2d_bytes, dtype=torch.uint8).pin_memory()
@@ -665,7 +666,7 @@ def link_bound(h2d_bytes: int, d2h_bytes: int, dev, reps: int = 5):
                     hout.copy_(dout, non_blocking=True)
             torch.cuda.synchronize(dev)
             ts.append(time.perf_counter() - t0)
-        return statistics.median(ts[1:]) * 1e3
+        return min(ts[1:]) * 1e3
 
     t_in, t_out, t_both = timed(True, False), timed(False, True), timed(True, True)
     return {"h2d_gbs": round(h2d_bytes / (t_in * 1e-3) / 1e9, 1),
