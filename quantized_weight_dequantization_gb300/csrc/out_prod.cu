@@ -350,6 +350,15 @@ __global__ void __launch_bounds__(kOpThreads, 1)
     auto group_bar = [&]() {
       asm volatile("bar.sync %0, %1;" :: "r"(1 + group), "n"(kOpGroupThreads) : "memory");
     };
+    // the same barrier, returning whether any of the group's threads passed `mine` true
+    auto group_bar_any = [&](bool mine) -> bool {
+      uint32_t any;
+      asm volatile(
+          "{\n.reg .pred p, q;\nsetp.ne.u32 q, %1, 0;\n"
+          "bar.red.or.pred p, %2, %3, q;\nselp.u32 %0, 1, 0, p;\n}"
+          : "=r"(any) : "r"(mine ? 1u : 0u), "r"(1 + group), "n"(kOpGroupThreads) : "memory");
+      return any != 0;
+    };
     const int64_t npk = (p.w.n + 1) / 2, nblk = (p.w.n + (int64_t(1) << p.w.log2_bs) - 1) >>
                                                p.w.log2_bs;
     const int64_t ngrp = (nblk + (int64_t(1) << p.w.log2_nbs) - 1) >> p.w.log2_nbs;
@@ -430,31 +439,31 @@ __global__ void __launch_bounds__(kOpThreads, 1)
       // the chains before that of stage l - 2 (whose slot this stage reuses): added out one
       // chain after they completed, so the MMAs, which need a buffer back kAccBufs chains
       // later, find it free (the MMAs of those chains were issued: their stages are decoded)
+      bool wok = true;  // this warp's waits of this stage (warp-uniform)
       for (const int need = (l >= kOpGroups ? (l - kOpGroups) / kOpChain : 0) - 1;
-           ok && flushed <= need; ++flushed)
-        ok = flush(flushed);
-      if (!ok) break;
-      if (l >= kOpGroups) {  // the MMAs of this slot's previous stage completed
-        ok = !*abort_flag && mbar_wait(empty(group), uint32_t((l >> 1) - 1) & 1u);
-        if (!__all_sync(0xFFFFFFFFu, ok)) {
-          if (lane == 0 && !*abort_flag) fail();
-          ok = false;
-          break;
-        }
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+           wok && flushed <= need; ++flushed)
+        wok = flush(flushed);
+      if (wok && l >= kOpGroups) {  // the MMAs of this slot's previous stage completed
+        wok = __all_sync(0xFFFFFFFFu,
+                         !*abort_flag && mbar_wait(empty(group), uint32_t((l >> 1) - 1) & 1u));
+        if (wok)
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        else if (lane == 0 && !*abort_flag)
+          fail();
       }
       cp_async_wait_all();
-      if constexpr (kTma) {  // the stage's boxes landed (every thread acquires them)
-        const bool got =
-            __all_sync(0xFFFFFFFFu, mbar_wait(staged(group), uint32_t(l >> 1) & 1u));
-        if (tg == 0 && got) tma_pending = false;
-        if (!got) {
-          if (lane == 0 && !*abort_flag) fail();
-          ok = false;
-          break;
-        }
+      if (kTma && wok) {  // the stage's boxes landed (every thread acquires them)
+        wok = __all_sync(0xFFFFFFFFu, mbar_wait(staged(group), uint32_t(l >> 1) & 1u));
+        if (tg == 0 && wok) tma_pending = false;
+        if (!wok && lane == 0 && !*abort_flag) fail();
       }
-      group_bar();  // every thread's copies landed
+      // every thread's copies landed: the group's barrier, which also ORs the warps' failed
+      // waits, so the group's warps leave their loop together (a warp that left alone would
+      // leave the others waiting at the next group barrier)
+      if (group_bar_any(!wok)) {
+        ok = false;
+        break;
+      }
       // each row's nested scales (separately rounded FP32 multiply and add), for the blocks
       // b0 + k it touches: 64 rows x 5 blocks over the group's threads
       for (int q = tg; q < kOpK * 5; q += kOpGroupThreads) {
