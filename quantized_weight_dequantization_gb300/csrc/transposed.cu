@@ -74,11 +74,13 @@ __device__ __forceinline__ void store_pair(void* out, int64_t o, float v0, float
 }
 
 // Staged form (cols % 32 == 0, `packed` 16-byte aligned).  A CTA owns 128 rows
-// x 256 columns of W: its packed bytes (128 B per row, whole cache lines) and
-// the scales of its 32-value row segments are first loaded cooperatively and
-// coalesced into shared memory; then each warp decodes one 64 x 64 warp tile
-// from shared memory and stores it as above.  CTAs are walked in column-major
-// order.
+// x 256 columns of W: the scale codes and absmax of its 32-value row segments
+// are loaded into registers first, then its packed bytes (128 B per row, whole
+// cache lines) cooperatively and coalesced into shared memory, so both round
+// trips overlap; after one barrier the threads turn their codes into the
+// segments' scales in shared memory, and after another each warp decodes one
+// 64 x 64 warp tile from shared memory and stores it as above.  CTAs are walked
+// in column-major order.
 constexpr int kSR = 128;                 // CTA tile rows
 constexpr int kSC = 256;                 // CTA tile columns (128 packed bytes per row)
 constexpr int kSRowBytes = kSC / 2;      // smem row: 8 chunks of 16 B, XOR-swizzled
@@ -134,6 +136,23 @@ __global__ void __launch_bounds__(kThreads, DQ4_T_MIN_CTAS)
   const int64_t r0 = int64_t(blockIdx.x % tiles_r) * kSR;  // column-major CTA order
   const int64_t c0 = int64_t(blockIdx.x / tiles_r) * kSC;
 
+  // the scale inputs of the 32-value segments first, so their loads overlap the packed rows'
+  constexpr int kScPer = kSR * kSSeg / kThreads;
+  uint32_t sc_code[kScPer];
+  float sc_am[kScPer];
+#pragma unroll
+  for (int k = 0; k < kScPer; ++k) {
+    const int id = threadIdx.x + kThreads * k;
+    const int rr = id / kSSeg, q = id % kSSeg;
+    const int64_t r = r0 + rr, c = c0 + 32 * q;
+    sc_code[k] = 0;
+    sc_am[k] = 0.f;
+    if (r < rows && c < cols) {
+      const int64_t b = (r * cols + c) >> a.log2_bs;
+      sc_code[k] = __ldg(a.codes + b);
+      sc_am[k] = __ldg(a.absmax + (b >> a.log2_nbs));
+    }
+  }
   // packed rows: 8 x 16 B per row; a warp reads 4 whole rows per instruction
 #pragma unroll
   for (int k = 0; k < kSR * 8 / kThreads; ++k) {
@@ -148,12 +167,11 @@ __global__ void __launch_bounds__(kThreads, DQ4_T_MIN_CTAS)
   __syncthreads();  // codebooks staged
   // scales of the 32-value segments (bs >= 32 and cols % 32 == 0: one block each)
 #pragma unroll
-  for (int k = 0; k < kSR * kSSeg / kThreads; ++k) {
+  for (int k = 0; k < kScPer; ++k) {
     const int id = threadIdx.x + kThreads * k;
     const int rr = id / kSSeg, q = id % kSSeg;  // a warp: 4 rows x 8 segments (codes coalesced)
-    const int64_t r = r0 + rr, c = c0 + 32 * q;
-    s_sc[q][rr] = (r < rows && c < cols) ? nested_scale(a, s_scb, (r * cols + c) >> a.log2_bs)
-                                         : 0.f;
+    // (segments past the edges get a scale of no meaning: their values are never stored)
+    s_sc[q][rr] = __fadd_rn(__fmul_rn(s_scb[sc_code[k]], sc_am[k]), a.offset);
   }
   __syncthreads();
 
