@@ -15,12 +15,11 @@ namespace dq4d {
 // contiguous per warp store instruction, with no shared-memory staging.
 // Tiles are walked in column-major order (consecutive warps go down a
 // column band), so consecutive warps extend the same output rows.
-// kLoadVec: cols % 32 == 0 and `packed` 16-byte aligned (every row segment
-// is two aligned 16-byte loads); otherwise values are read one by one.
-// kStoreVec: rows is even and `out` is aligned to two elements (pair
-// stores); otherwise elements are stored one by one.
-constexpr int kTR = 64;  // warp-tile rows of W
-constexpr int kTC = 64;  // warp-tile columns of W
+// That is the staged form below (cols % 32 == 0 and `packed` 16-byte aligned,
+// every row segment two aligned 16-byte chunks); kStoreVec: rows is even and
+// `out` is aligned to two elements (pair stores), otherwise elements are
+// stored one by one.  Other shapes take the odd-shape staged form further
+// down.
 
 template <int OUT>
 __device__ __forceinline__ uint32_t out_bits(float v) {
@@ -239,45 +238,156 @@ __global__ void __launch_bounds__(kThreads, DQ4_T_MIN_CTAS)
   }
 }
 
-// Per-value form for other shapes: a warp owns 64 rows x 64 columns, lane p
-// the rows r0 + 2p and r0 + 2p + 1, read value by value.
-template <int OUT, bool kStoreVec>
+// Staged form for any other shape (cols % 32 != 0 or `packed` not 16-byte aligned): the
+// same 128 x 256 CTA tile and 64 x 64 warp tiles as the staged form.  A row of the tile
+// starts at any nibble and may cross several scale blocks, so the CTA stages, per row, the
+// packed bytes that hold its (at most 256) values, and the scales of the (at most 9) blocks
+// they touch; a lane then decodes rows 2p and 2p + 1 of its warp tile column by column from
+// shared memory, finding each value's byte, nibble and scale from the row's first value
+// index.  Warp w stages rows 16 w .. 16 w + 15: with `packed` 4-byte aligned, the 34
+// aligned words that hold a row's bytes (129 bytes cover 256 nibbles from an odd start,
+// plus up to 3 bytes before them), every load of its rows in flight together; otherwise
+// byte by byte.  Here lane p decodes rows p and p + 32 of its warp tile (not 2p, 2p + 1):
+// with staged rows 35 words apart its 32 lanes read 32 banks, and each store instruction
+// writes 32 consecutive elements of W^T (element stores: rows and columns of any parity).
+constexpr int kOddRowWords = 34;
+constexpr int kOddRowStride = 4 * 35;  // bytes between staged rows (35 words: odd)
+constexpr int kOddSeg = kSC / 32 + 1;  // blocks of >= 32 values a 256-value row run touches
+
+template <int OUT>
 __global__ void __launch_bounds__(kThreads)
-    dq4_transposed_any_kernel(const Args a, int64_t rows, int64_t cols, uint32_t tiles_r,
-                              uint32_t n_tiles) {
+    dq4_transposed_any_kernel(const Args a, int64_t rows, int64_t cols, uint32_t tiles_r) {
   __shared__ float s_vcb[16];
   __shared__ float s_scb[256];
+  __shared__ __align__(16) uint8_t s_pk[kSR][kOddRowStride];
+  __shared__ float s_sc[kSR][kOddSeg];
 #if DQ4_PDL
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
 #endif
-  stage_codebooks<true>(a, s_vcb, s_scb);
-  const uint32_t t = blockIdx.x * uint32_t(kWarpsPerCta) + (threadIdx.x >> 5);
-  if (t >= n_tiles) return;
-  const int lane = threadIdx.x & 31;
-  const int64_t r0 = int64_t(t % tiles_r) * kTR;  // column-major tile order
-  const int64_t c0 = int64_t(t / tiles_r) * kTC;
-  const int64_t ra = r0 + 2 * lane;
-  const bool has0 = ra < rows, has1 = ra + 1 < rows;
-  if (!has0) return;
-  const int ncol = int(cols - c0 < kTC ? cols - c0 : kTC);
-  // each row's scale is rebuilt only when the row crosses into a new block
-  const int64_t i0 = ra * cols + c0, i1 = i0 + cols;
-  int64_t b0 = -1, b1 = -1;
-  float sc0 = 0.f, sc1 = 0.f;
-  int64_t o = c0 * rows + ra;
-  for (int cc = 0; cc < ncol; ++cc) {
-    const int64_t ia = i0 + cc, ib = i1 + cc;
-    if ((ia >> a.log2_bs) != b0) { b0 = ia >> a.log2_bs; sc0 = nested_scale(a, s_scb, b0); }
-    const uint32_t ba = a.packed[ia >> 1];
-    const float v0 = __fmul_rn(s_vcb[(ia & 1) ? (ba & 0xFu) : (ba >> 4)], sc0);
-    float v1 = 0.f;
-    if (has1) {
-      if ((ib >> a.log2_bs) != b1) { b1 = ib >> a.log2_bs; sc1 = nested_scale(a, s_scb, b1); }
-      const uint32_t bb = a.packed[ib >> 1];
-      v1 = __fmul_rn(s_vcb[(ib & 1) ? (bb & 0xFu) : (bb >> 4)], sc1);
+  if (threadIdx.x < 16) s_vcb[threadIdx.x] = __ldg(a.vcb + threadIdx.x);
+  for (int k = threadIdx.x; k < 256; k += kThreads) s_scb[k] = __ldg(a.scb + k);
+  const int64_t r0 = int64_t(blockIdx.x % tiles_r) * kSR;  // column-major CTA order
+  const int64_t c0 = int64_t(blockIdx.x / tiles_r) * kSC;
+  const int nv = int(cols - c0 < kSC ? cols - c0 : kSC);  // values of a row in the tile
+  const int64_t n_bytes = (a.n + 1) >> 1;
+  // the scale codes and absmax of the blocks each row touches, into registers first
+  constexpr int kScPer = (kSR * kOddSeg + kThreads - 1) / kThreads;
+  uint32_t sc_code[kScPer];
+  float sc_am[kScPer];
+#pragma unroll
+  for (int k = 0; k < kScPer; ++k) {
+    const int id = threadIdx.x + kThreads * k;
+    const int rr = id / kOddSeg, q = id - rr * kOddSeg;
+    const int64_t r = r0 + rr;
+    sc_code[k] = 0;
+    sc_am[k] = 0.f;
+    if (rr < kSR && r < rows) {
+      const int64_t i0 = r * cols + c0;
+      const int64_t b = (i0 >> a.log2_bs) + q;
+      if (b <= (i0 + nv - 1) >> a.log2_bs) {
+        sc_code[k] = __ldg(a.codes + b);
+        sc_am[k] = __ldg(a.absmax + (b >> a.log2_nbs));
+      }
     }
-    store_pair<OUT, kStoreVec>(a.out, o, v0, v1, has0, has1);
+  }
+  // the packed bytes of each row's values: staged byte k of row rr is byte
+  // ((i0 >> 1) & ~3) + k of the array (word aligned; byte (i0 >> 1) + k with byte loads)
+  {
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int kRowsPerWarp = kSR / kWarpsPerCta;
+    const bool words = (reinterpret_cast<uintptr_t>(a.packed) & 3) == 0;  // CTA-uniform
+    if (words) {
+      const uint32_t* pw = reinterpret_cast<const uint32_t*>(a.packed);
+      const int64_t full_words = n_bytes >> 2;  // words wholly inside the array
+#pragma unroll 4
+      for (int q = 0; q < kRowsPerWarp; ++q) {
+        const int rr = w * kRowsPerWarp + q;
+        const int64_t r = r0 + rr;
+        const int64_t w0 = r < rows ? ((r * cols + c0) >> 1) >> 2 : 0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int j = lane + 32 * h;
+          if (j >= kOddRowWords) break;
+          const int64_t wi = w0 + j;
+          uint32_t v = 0;
+          if (r < rows) {
+            if (wi < full_words) {
+              v = __ldcs(pw + wi);
+            } else {  // the array's last, partial word
+              for (int e = 0; e < 4 && 4 * wi + e < n_bytes; ++e)
+                v |= uint32_t(a.packed[4 * wi + e]) << (8 * e);
+            }
+          }
+          reinterpret_cast<uint32_t*>(s_pk[rr])[j] = v;
+        }
+      }
+    } else {
+#pragma unroll 2
+      for (int q = 0; q < kRowsPerWarp; ++q) {
+        const int rr = w * kRowsPerWarp + q;
+        const int64_t r = r0 + rr;
+        const int64_t b0 = r < rows ? (r * cols + c0) >> 1 : 0;
+        constexpr int kBytes = 4 * kOddRowWords;
+        uint8_t v[(kBytes + 31) / 32];
+#pragma unroll
+        for (int h = 0; h < (kBytes + 31) / 32; ++h) {
+          const int k = lane + 32 * h;
+          v[h] = (k < kBytes && r < rows && b0 + k < n_bytes) ? __ldcs(a.packed + b0 + k)
+                                                             : uint8_t(0);
+        }
+#pragma unroll
+        for (int h = 0; h < (kBytes + 31) / 32; ++h) {
+          const int k = lane + 32 * h;
+          if (k < kBytes) s_pk[rr][k] = v[h];
+        }
+      }
+    }
+  }
+  __syncthreads();  // codebooks staged
+#pragma unroll
+  for (int k = 0; k < kScPer; ++k) {
+    const int id = threadIdx.x + kThreads * k;
+    const int rr = id / kOddSeg, q = id - rr * kOddSeg;
+    // (blocks past a row's values get a scale of no meaning: no value reads it)
+    if (rr < kSR) s_sc[rr][q] = __fadd_rn(__fmul_rn(s_scb[sc_code[k]], sc_am[k]), a.offset);
+  }
+  __syncthreads();
+
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wr = 64 * (w >> 2);  // warp tile: rows wr .. +64, columns wc .. +64 of the CTA tile
+  const int wc = 64 * (w & 3);
+  const int la = wr + lane, lb = la + 32;  // this lane's rows of the CTA tile
+  const int64_t ra = r0 + la, rb = r0 + lb;
+  const bool has0 = ra < rows, has1 = rb < rows;
+  if (!has0) return;
+  const int ncol = nv - wc < 64 ? nv - wc : 64;
+  if (ncol <= 0) return;
+  // per row: the nibble position of column 0 in the staged row (twice the row's first
+  // byte's offset in its staged run, plus the first value's parity) and the first value's
+  // offset in its block; column c of the tile is then byte (n + c) >> 1, nibble (n + c) & 1,
+  // block ((m + c) >> log2 bs) of the row's staged bytes and scales
+  const bool words = (reinterpret_cast<uintptr_t>(a.packed) & 3) == 0;
+  const uint32_t bs_mask = (1u << a.log2_bs) - 1u, pmask = words ? 7u : 1u;
+  const int64_t i0a = ra * cols + c0, i0b = rb * cols + c0;
+  const uint32_t pa = uint32_t(i0a) & pmask, pb = uint32_t(i0b) & pmask;
+  const uint32_t ma = uint32_t(i0a) & bs_mask, mb = uint32_t(i0b) & bs_mask;
+  const uint8_t* pka = s_pk[la];
+  const uint8_t* pkb = s_pk[lb];
+  const float* sca = s_sc[la];
+  const float* scb = s_sc[lb];
+  int64_t o = (c0 + wc) * rows + ra;  // W^T index of (ra, column); advances by rows
+  for (int cc = 0; cc < ncol; ++cc) {
+    const uint32_t c = uint32_t(wc + cc);
+    const uint32_t na = pa + c, nb = pb + c;
+    const uint32_t ba = pka[na >> 1];
+    store_one<OUT>(a.out, o, __fmul_rn(s_vcb[(na & 1u) ? (ba & 0xFu) : (ba >> 4)],
+                                       sca[(ma + c) >> a.log2_bs]));
+    if (has1) {
+      const uint32_t bb = pkb[nb >> 1];
+      store_one<OUT>(a.out, o + 32, __fmul_rn(s_vcb[(nb & 1u) ? (bb & 0xFu) : (bb >> 4)],
+                                              scb[(mb + c) >> a.log2_bs]));
+    }
     o += rows;
   }
 }
@@ -310,13 +420,11 @@ int launch_transposed(const Args& a, int64_t rows, int64_t cols, cudaStream_t st
     if (sv) return launch_kernel(dq4_transposed_kernel<OUT, true>, grid, stream, b, rows, cols, tr);
     return launch_kernel(dq4_transposed_kernel<OUT, false>, grid, stream, b, rows, cols, tr);
   }
-  const int64_t tiles_r = (rows + kTR - 1) / kTR;
-  const int64_t n_tiles = tiles_r * ((cols + kTC - 1) / kTC);
-  if (n_tiles > int64_t(UINT32_MAX) - kWarpsPerCta) return DQ4_ERR_N;  // 32-bit tile ids
-  const int64_t grid = (n_tiles + kWarpsPerCta - 1) / kWarpsPerCta;
-  const uint32_t tr = uint32_t(tiles_r), nt = uint32_t(n_tiles);
-  if (sv) return launch_kernel(dq4_transposed_any_kernel<OUT, true>, grid, stream, a, rows, cols, tr, nt);
-  return launch_kernel(dq4_transposed_any_kernel<OUT, false>, grid, stream, a, rows, cols, tr, nt);
+  const int64_t tiles_r = (rows + kSR - 1) / kSR;
+  const int64_t grid = tiles_r * ((cols + kSC - 1) / kSC);  // one CTA per 128 x 256 tile
+  if (grid > int64_t(UINT32_MAX)) return DQ4_ERR_N;        // 32-bit tile ids
+  return launch_kernel(dq4_transposed_any_kernel<OUT>, grid, stream, a, rows, cols,
+                       uint32_t(tiles_r));
 }
 
 }  // namespace dq4d
