@@ -141,7 +141,8 @@ def test_split_and_single_range_agree_and_repeat(dq):
         assert np.abs(got.cpu().numpy() - want).max() <= 2e-5 * scale
 
 
-@pytest.mark.parametrize("rows,cols,ncols", [(20000, 256, 64), (3000, 512, 300), (777, 384, 16)])
+@pytest.mark.parametrize("rows,cols,ncols", [(20000, 256, 64), (3000, 512, 300), (777, 384, 16),
+                                             (10, 256, 8), (63, 512, 100)])
 def test_tma_and_copy_staging_agree(dq, rows, cols, ncols):
     """The same problem through the TMA staging (G 16-byte aligned) and the cp.async staging
     (G one float off 16 bytes): the decode and the MMA order are the same, so dst agrees bit
