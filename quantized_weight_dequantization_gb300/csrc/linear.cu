@@ -1128,7 +1128,11 @@ struct LinPlan {
 // costs 640 + BX (dequantization with the shared-memory reads it contends for, and the
 // MMAs), a CTA about 2400 more (pipeline fill, drain and read-out), and a split CTA the
 // partial tiles' stores and sums, about 1600 + 15 BX (two FP32 partials of 128 x BX each
-// go out and come back, at the end of the run when every SM does the same), and a
+// go out and come back, at the end of the run when every SM does the same) plus, for
+// BX >= 128, 12 BX per CTA beyond two sharing a tile (its last arriver sums that many
+// partials of 64 KB or more: with 4 to 17 sharers such splits lost to whole tiles at
+// N = K = 4096, M = 128 .. 512 and at N <= 1024, and with 2 they won by 12 to 25 % at
+// N = 9856; narrower tiles' partials are small, and their splits kept winning), and a
 // read-out per tile boundary it crosses: hidden with two accumulator buffers per issuer,
 // about 400 with one buffer and one issuer, and 2000 with one buffer for each of two
 // issuers (both wait at the boundary; measured at BX = 64, where whole tiles win).  The
@@ -1155,8 +1159,11 @@ LinPlan plan_linear(int64_t M, int64_t N, int64_t K, int sms, bool split) {
     if (split && units >= sms && units <= int64_t(UINT32_MAX) && sms < 65536) {
       const int64_t per_cta = (units + sms - 1) / sms;
       const int64_t crossings = (per_cta + st_count - 1) / st_count;
+      // CTAs sharing a tile, whose 128 x BX FP32 partials its last arriver sums
+      const int64_t parts = (st_count + per_cta - 1) / per_cta + 1;
       const int64_t split_cost =
           per_cta * stage_cost + 2400 + 1600 + 15 * bx +
+          (bx >= 128 && parts > 2 ? 12 * bx * (parts - 2) : 0) +
           (kAccOf(bx) == 1 ? (kIssOf(bx) > 1 ? 2000 : 400) * crossings : 0);
       if (split_cost < cost) {
         cost = split_cost;

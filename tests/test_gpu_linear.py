@@ -159,8 +159,8 @@ def test_errors(dq):
 # twice (M = 64 and a ragged M = 40).  BX <= 64 issues its MMAs from two threads, each
 # into its own accumulators (two buffers each up to BX = 32, one at BX = 64); wider tiles
 # issue from one thread into one buffer.
-SPLIT_SHAPES = [(16, 11008, 4096), (3, 2000, 4096), (128, 1024, 8192), (16, 4860, 1216),
-                (128, 2000, 2048), (384, 1000, 4096), (300, 9856, 2048), (300, 4096, 4096),
+SPLIT_SHAPES = [(16, 11008, 4096), (3, 2000, 4096), (640, 1024, 8192), (16, 4860, 1216),
+                (128, 2000, 2048), (200, 3000, 8192), (300, 9856, 2048), (300, 9856, 4096),
                 (1024, 9856, 1216), (1500, 9856, 64), (2048, 9856, 256), (16, 49152, 512),
                 (2048, 9856, 512), (64, 2000, 16384), (40, 2000, 16384)]
 
