@@ -13,8 +13,8 @@ plan": warm-ups, >= 7 timed batches, every batch sample with median / p10 /
 p90, unfused sequence timed interleaved as the comparison):
   * W untimed warm-up steps, then exactly K steps between barrier +
     synchronize on both sides; the time is the max over ranks.
-  * every step uses the next of 3 rotating buffer sets (1.77 GB in all, each
-    larger than L2), so no step finds the previous step's lines in L2.
+  * every step uses the next of 4 rotating buffer sets (2.36 GB in all, each
+    larger than L2), so no step finds the previous steps' lines in L2.
   * nvidia-smi samples SM clocks and throttle reasons during the timed region.
 
 Other legs: `e2e` (the same metric with host buffers: one dq4_nested_host call
@@ -55,7 +55,7 @@ DEFAULT_CELLS = (["C1", "C2a", "C2b", "C3a", "C3b", "C3c", "C3d", "C4a", "C4b", 
                     zip((32, 64, 128, 256, 512, 1024, 2048, 4096),
                         (-1.0, -1e-3, 1e-3, 1.0, -1.0, -1e-3, 1e-3, 1.0))])
 BAR_CELL_PREFIXES = ("C3", "C4", "C5")
-N_SETS = 3
+N_SETS = 4  # rotating buffer sets of the timed region (each larger than L2)
 E2E_WINDOWS = 5  # the e2e steps are timed in this many windows (median window reported)
 HOLD_CYCLES = 2_000_000  # the pre-region spin: ~1 ms at the 2.07 GHz SM clock
 FALLBACK_HBM_GBS = 6800.0
@@ -573,7 +573,7 @@ def run_ours(args):
 
 
 def time_cells(names, dev, stream, transposed: bool, peak: float, batches: int = 7):
-    """Each named cell timed as back-to-back launches on `stream` over rotating buffer sets
+    """Each named cell timed as back-to-back launches on `stream` over >= 4 rotating buffer sets
     (together more than twice the L2, so no launch finds its inputs there): >= 20 warm-up
     launches, then one batch of >= 2 ms of launches captured in a CUDA graph and replayed
     `batches` times, so that the record is the device's time per call and not the gaps
@@ -594,7 +594,7 @@ def time_cells(names, dev, stream, transposed: bool, peak: float, batches: int =
         cell = gen.CELLS[name]
         p = cell.problem()
         alg = cell.algorithmic_bytes()
-        n_sets = max(3, -(-2 * l2 // alg) + 1)
+        n_sets = max(4, -(-2 * l2 // alg) + 1)
         first = {k: torch.from_numpy(np.ascontiguousarray(getattr(p, k))).to(dev)
                  for k in ("packed", "scale_codes", "nested_absmax")}
         scb = torch.from_numpy(p.scale_codebook).to(dev)
@@ -646,7 +646,7 @@ def time_cells(names, dev, stream, transposed: bool, peak: float, batches: int =
         del sets, first
     bar = [v["frac"] for v in rec.values() if v["in_bar"]]
     return {"cells": rec, "bar_min_frac": min(bar) if bar else None,
-            "protocol": f"per cell: rotating buffer sets (> 2x L2 in all), >= 20 warm-up "
+            "protocol": f"per cell: >= 4 rotating buffer sets (> 2x L2 in all), >= 20 warm-up "
                         f"launches, >= 2 ms of back-to-back launches captured in one CUDA "
                         f"graph and replayed {batches} times, median / p10 / p90 per call "
                         f"over the replays"}
