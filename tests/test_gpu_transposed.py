@@ -97,6 +97,35 @@ def test_large_weight(dq, name):
     check(dq, cell.problem(), cell.rows, cell.cols, cell.out)
 
 
+@pytest.mark.parametrize("rows,cols", [(65540, 32800), (65537, 32771)])
+def test_beyond_2_pow_31_values(dq, rows, cols):
+    """rows x cols > 2^31 values (64-bit value and output indices), on the staged kernel
+    (cols % 32 == 0; partial last row and column tiles) and on the odd-shape one (odd n):
+    whole rows of W, read back from W^T, against the oracle on windows of whole nested
+    groups: the first rows, the rows across flat index 2^31, and the last rows."""
+    n = rows * cols
+    assert n > (1 << 31)
+    p = gen.make_problem(n, 64, 256, "nf4", 0.5, 0.0371, seed=rows + cols)
+    t = to_dev(p)
+    out = run(dq, p, t, rows, cols, "f16")
+    torch.cuda.synchronize()
+    wt = out.view(cols, rows)
+    unit = 64 * 256
+    r_mid = (1 << 31) // cols
+    for r0 in (0, r_mid - 1, rows - 3):
+        r1 = min(rows, r0 + 3)
+        lo = (r0 * cols) // unit * unit
+        hi = min(n, -(-(r1 * cols) // unit) * unit)
+        sub = gen.Problem(p.packed[lo // 2:(hi + 1) // 2], p.scale_codes[lo // 64:-(-hi // 64)],
+                          p.nested_absmax[lo // unit:-(-hi // unit)], p.scale_codebook,
+                          p.value_codebook, p.offset, hi - lo, 64, 256)
+        want = oracle.dq4_nested(sub, "f16")[r0 * cols - lo:r1 * cols - lo]
+        got = wt[:, r0:r1].t().contiguous()
+        assert np.array_equal(bits(got), want_bits(want)), (rows, cols, r0)
+    del out, wt, t
+    torch.cuda.empty_cache()
+
+
 def test_every_code_transposed(dq):
     p = gen.enumeration_problem(0.52, blocksize=32, groups=4)
     rows, cols = 256, p.n // 256
