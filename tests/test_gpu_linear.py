@@ -368,3 +368,46 @@ def test_weight_operand_bits_with_unit_activations(dq, case):
             assert int(bad.item()) == 0
     if N == 11008:
         assert split_seen  # the decode sizes take the split path at this shape
+
+
+def test_weight_operand_bits_beyond_2_pow_31_values(dq):
+    """N x K > 2^31 weight values (64-bit weight indices; a partial last row tile): 16 unit
+    activation rows pick 16 columns k of W (the first, the last and 14 others), and those
+    columns of every row in three windows (the first rows, the rows across flat index 2^31,
+    the last rows) must equal dq4_nested's bits for X's dtype, on the split path (cached
+    workspace) and on whole tiles (no workspace).  Zeros compare as zeros of either sign."""
+    N, K, bs, nbs, xin = 65600, 32768, 64, 256, "bf16"
+    assert N * K > (1 << 31)
+    p = gen.make_problem(N * K, bs, nbs, "nf4", 1.0, 0.0371, seed=N + K)
+    t = {k: torch.from_numpy(np.ascontiguousarray(getattr(p, k))).to(DEV)
+         for k in ("packed", "scale_codes", "nested_absmax", "scale_codebook", "value_codebook")}
+    perm = np.argsort(gen.splitmix64(K, 91, K), kind="stable")
+    ks = [0, K - 1] + [int(k) for k in perm if k not in (0, K - 1)][:14]
+    X = torch.zeros((len(ks), K), dtype=TDT[xin], device=DEV)
+    X[torch.arange(len(ks), device=DEV), torch.tensor(ks, device=DEV)] = 1
+    none = torch.empty(0, dtype=torch.uint8, device=DEV)
+    args = (X, t["packed"], t["scale_codes"], t["nested_absmax"], t["scale_codebook"],
+            t["value_codebook"], float(p.offset), N, bs, nbs)
+    unit = bs * nbs
+    mid = (1 << 31) // K  # the first row at flat index >= 2^31
+    windows = [(0, 256), (mid - 64, mid + 32), (N - 96, N)]
+    for ws in (None, none):
+        bad = torch.zeros(1, dtype=torch.int32, device=DEV)
+        Y = dq.linear(*args, out_dtype=torch.float32, bad=bad, workspace=ws)
+        torch.cuda.synchronize()
+        assert int(bad.item()) == 0
+        for n0, n1 in windows:
+            lo, hi = n0 * K, n1 * K  # K is a multiple of bs * nbs: whole nested groups
+            assert lo % unit == 0 and hi % unit == 0
+            sub = gen.Problem(p.packed[lo // 2:hi // 2], p.scale_codes[lo // bs:hi // bs],
+                              p.nested_absmax[lo // unit:hi // unit], p.scale_codebook,
+                              p.value_codebook, p.offset, hi - lo, bs, nbs)
+            w16 = oracle.dq4_nested(sub, xin, threads=16).reshape(n1 - n0, K)[:, ks]
+            want = torch.from_numpy(np.ascontiguousarray(_f32_bits_of(w16, xin).T)).to(DEV)
+            want = torch.where(want.view(torch.float32) == 0, torch.zeros_like(want), want)
+            got = _nonzero_bits(Y[:, n0:n1].contiguous(), torch.int32)
+            ne = int((got != want).sum().item())
+            assert ne == 0, (ws is None, n0, ne)
+        del Y
+    del t
+    torch.cuda.empty_cache()
