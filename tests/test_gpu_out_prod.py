@@ -103,6 +103,39 @@ def test_decoded_rows_bit_exact(dq, fmt, bs, nbs, offset, rows, cols):
         assert same.all(), (j0, int((~same).sum()))
 
 
+def test_decoded_rows_bit_exact_beyond_2_pow_31_values(dq):
+    """rows x cols > 2^31 weight values (64-bit value indices): G picks 16 rows of W (the
+    first, the last, the two at flat index 2^31 and 12 others), and each column of dst must
+    be its row of W bit for bit, against the oracle on windows of whole nested groups."""
+    rows, cols, bs, nbs = (1 << 23) + 64, 256, 64, 256
+    n = rows * cols
+    assert n > (1 << 31)
+    p = gen.make_problem(n, bs, nbs, "nf4", 0.5, 0.0371, seed=rows % 1009)
+    t = to_dev(p)
+    mid = (1 << 31) // cols  # the first row at flat index >= 2^31
+    perm = np.argsort(gen.splitmix64(rows, 93, rows), kind="stable")
+    picks = [0, rows - 1, mid - 1, mid]
+    sel = np.array(picks + [int(r) for r in perm if int(r) not in picks][:12], dtype=np.int64)
+    ncols = sel.size
+    G = torch.zeros((rows, ncols), dtype=torch.float32, device=DEV)
+    G[torch.from_numpy(sel).to(DEV), torch.arange(ncols, device=DEV)] = 1.0
+    got = dq.out_prod(t["packed"], t["scale_codes"], t["nested_absmax"], t["scale_codebook"],
+                      t["value_codebook"], float(p.offset), rows, cols, G, bs, nbs).cpu().numpy()
+    unit = bs * nbs
+    for j, r in enumerate(sel):
+        lo = (int(r) * cols) // unit * unit
+        hi = min(n, lo + unit)
+        sub = gen.Problem(p.packed[lo // 2:hi // 2], p.scale_codes[lo // bs:-(-hi // bs)],
+                          p.nested_absmax[lo // unit:-(-hi // unit)], p.scale_codebook,
+                          p.value_codebook, p.offset, hi - lo, bs, nbs)
+        want = oracle.dq4_nested(sub, "f32")[int(r) * cols - lo:(int(r) + 1) * cols - lo]
+        col = np.ascontiguousarray(got[:, j])
+        same = (col.view(np.uint32) == want.view(np.uint32)) | ((col == 0) & (want == 0))
+        assert same.all(), (int(r), int((~same).sum()))
+    del t, G
+    torch.cuda.empty_cache()
+
+
 def test_realistic_weights_within_fp32_accumulation_tolerance(dq):
     rows, cols, ncols = 200000, 256, 32
     p = gen.make_problem(rows * cols, 64, 256, "nf4", 1.0, -0.1, seed=13)
