@@ -90,16 +90,21 @@ constexpr int kSSeg = kSC / 32;          // 32-value scale segments per row
 // chunk positions, i.e. all 32 banks.
 __device__ __forceinline__ int swz(int rr, int ch) { return ch ^ ((rr >> 1) & 7); }
 
-// minimum resident CTAs per SM the staged transposed kernel is compiled for
-#ifndef DQ4_T_MIN_CTAS
-#define DQ4_T_MIN_CTAS 8
-#endif
+// Resident CTAs per SM the staged transposed kernel is compiled for: 8 (32 registers a
+// thread, the full 64 warps) by default.  The four-row form is also built for 6 (40
+// registers): a grid of more than one but at most 1.5 waves of 8 CTAs per SM runs as 1.3 to
+// 2 waves of 6 instead of a full wave and a thin second one, which measured faster there
+// (GB300, FP16/BF16, 4096 x 11008 and 11008 x 4096: 21.5 -> 20.7 us; 4096 x 12288: 23.9 ->
+// 22.4 us; at exactly one wave, at 1.74 waves and from 2.5 waves on, and for grids under
+// one wave, 8 per SM was as fast or faster).
+constexpr int kTMinCtas = 8;
+constexpr int kTMinCtasWide = 6;
 
 // kQuad (16-bit output, rows % 4 == 0, out 8-byte aligned): lanes 2q and 2q + 1 hold rows
 // 4q .. 4q + 3 of the tile between them; per two columns they swap one packed pair, so each
 // writes 8 bytes (4 rows) of one column: half the store instructions of pair stores.
-template <int OUT, bool kStoreVec, bool kQuad = false>
-__global__ void __launch_bounds__(kThreads, DQ4_T_MIN_CTAS)
+template <int OUT, bool kStoreVec, bool kQuad = false, int kMinCtas = kTMinCtas>
+__global__ void __launch_bounds__(kThreads, kMinCtas)
     dq4_transposed_kernel(const Args a, int64_t rows, int64_t cols, uint32_t tiles_r) {
   __shared__ float s_vcb[16];
   __shared__ float s_scb[256];
@@ -410,11 +415,18 @@ int launch_transposed(const Args& a, int64_t rows, int64_t cols, cudaStream_t st
     // and the prefetch measured slower (8192 x 8192: 49.3 -> 51.6 us; FP16 28672 x 8192:
     // 100.2 -> 97.0 us, 4096 x 4096: 10.7 -> 9.5 us)
     static std::atomic<int> occ_cache[kMaxDevices];
+    static std::atomic<int> occ_cache_wide[kMaxDevices];
     Args b = a;
     const int64_t wave =
         int64_t(sms) * ctas_per_sm(dq4_transposed_kernel<OUT, true, true>, dev, occ_cache);
     b.prefetch_ctas =
         OUT != DQ4_OUT_F32 && grid <= int64_t(DQ4_PREFETCH_WAVES) * wave ? grid : 0;
+    if (quad && grid > wave && 2 * grid <= 3 * wave) {  // (1, 1.5] waves of 8 CTAs per SM
+      constexpr auto kWide = dq4_transposed_kernel<OUT, true, true, kTMinCtasWide>;
+      const int64_t wave6 = int64_t(sms) * ctas_per_sm(kWide, dev, occ_cache_wide);
+      b.prefetch_ctas = grid <= int64_t(DQ4_PREFETCH_WAVES) * wave6 ? grid : 0;
+      return launch_kernel(kWide, grid, stream, b, rows, cols, tr);
+    }
     if (quad)
       return launch_kernel(dq4_transposed_kernel<OUT, true, true>, grid, stream, b, rows, cols, tr);
     if (sv) return launch_kernel(dq4_transposed_kernel<OUT, true>, grid, stream, b, rows, cols, tr);

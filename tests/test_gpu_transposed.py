@@ -91,6 +91,20 @@ def test_cells(dq, name, rows, cols):
     check(dq, cell.problem(), rows, cols, cell.out)
 
 
+@pytest.mark.parametrize("kind", ["bf16", "f16"])
+def test_grid_of_one_to_one_and_a_half_waves(dq, kind):
+    """A grid of more than one and at most 1.5 waves of 8 CTAs per SM (the four-row kernel
+    then runs its 6-CTA-per-SM build), with a partial last row tile and column tile."""
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    rows = 4100  # 33 row tiles, the last of 4 rows
+    ct = -(-int(8 * sms * 1.06) // 33)
+    cols = 256 * ct - 96  # ct column tiles, the last of 160 columns
+    tiles = 33 * ct
+    assert 8 * sms < tiles and 2 * tiles <= 3 * 8 * sms
+    p = gen.make_problem(rows * cols, 64, 256, "nf4", 1.0, 0.1, seed=cols + len(kind))
+    check(dq, p, rows, cols, kind)
+
+
 @pytest.mark.parametrize("name", ["C4a", "C4d"])
 def test_large_weight(dq, name):
     cell = gen.CELLS[name]
