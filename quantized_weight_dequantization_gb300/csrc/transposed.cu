@@ -255,6 +255,16 @@ __global__ void __launch_bounds__(kThreads, kMinCtas)
 // byte by byte.  Here lane p decodes rows p and p + 32 of its warp tile (not 2p, 2p + 1):
 // with staged rows 35 words apart its 32 lanes read 32 banks, and each store instruction
 // writes 32 consecutive elements of W^T (element stores: rows and columns of any parity).
+// Values n .. n + 7 of a staged row (n counted in value order from the row's first staged
+// byte), one per nibble, value n + k at bits 4k: the two words holding them, each byte's two
+// nibbles swapped (the high nibble is the even value), shifted down to value n.
+__device__ __forceinline__ uint32_t nibbles8(const uint32_t* w, uint32_t n) {
+  const uint32_t i = n >> 3;
+  uint64_t v = (uint64_t(w[i + 1]) << 32) | w[i];
+  v = ((v >> 4) & 0x0F0F0F0F0F0F0F0Full) | ((v << 4) & 0xF0F0F0F0F0F0F0F0ull);
+  return uint32_t(v >> (4 * (n & 7u)));
+}
+
 constexpr int kOddRowWords = 34;
 constexpr int kOddRowStride = 4 * 35;  // bytes between staged rows (35 words: odd)
 constexpr int kOddSeg = kSC / 32 + 1;  // blocks of >= 32 values a 256-value row run touches
@@ -368,32 +378,45 @@ __global__ void __launch_bounds__(kThreads)
   if (!has0) return;
   const int ncol = nv - wc < 64 ? nv - wc : 64;
   if (ncol <= 0) return;
-  // per row: the nibble position of column 0 in the staged row (twice the row's first
-  // byte's offset in its staged run, plus the first value's parity) and the first value's
-  // offset in its block; column c of the tile is then byte (n + c) >> 1, nibble (n + c) & 1,
-  // block ((m + c) >> log2 bs) of the row's staged bytes and scales
+  // per row: the nibble position of column 0 in the staged row (value order from the staged
+  // run's first byte: 8 x that word's index plus the first value's place in it) and the first
+  // value's offset in its block; column c of the tile is then nibble n + c of the staged row
+  // and block ((m + c) >> log2 bs) of the row's staged scales
   const bool words = (reinterpret_cast<uintptr_t>(a.packed) & 3) == 0;
   const uint32_t bs_mask = (1u << a.log2_bs) - 1u, pmask = words ? 7u : 1u;
   const int64_t i0a = ra * cols + c0, i0b = rb * cols + c0;
   const uint32_t pa = uint32_t(i0a) & pmask, pb = uint32_t(i0b) & pmask;
   const uint32_t ma = uint32_t(i0a) & bs_mask, mb = uint32_t(i0b) & bs_mask;
-  const uint8_t* pka = s_pk[la];
-  const uint8_t* pkb = s_pk[lb];
+  const uint32_t* wa = reinterpret_cast<const uint32_t*>(s_pk[la]);
+  const uint32_t* wb = reinterpret_cast<const uint32_t*>(s_pk[lb]);
   const float* sca = s_sc[la];
   const float* scb = s_sc[lb];
   int64_t o = (c0 + wc) * rows + ra;  // W^T index of (ra, column); advances by rows
-  for (int cc = 0; cc < ncol; ++cc) {
+  // eight columns at a time: their nibbles from two staged words, and the scales of the (at
+  // most two: blocks hold >= 32 values) blocks they fall in
+#pragma unroll 1
+  for (int cc = 0; cc < ncol; cc += 8) {
     const uint32_t c = uint32_t(wc + cc);
-    const uint32_t na = pa + c, nb = pb + c;
-    const uint32_t ba = pka[na >> 1];
-    store_one<OUT>(a.out, o, __fmul_rn(s_vcb[(na & 1u) ? (ba & 0xFu) : (ba >> 4)],
-                                       sca[(ma + c) >> a.log2_bs]));
-    if (has1) {
-      const uint32_t bb = pkb[nb >> 1];
-      store_one<OUT>(a.out, o + 32, __fmul_rn(s_vcb[(nb & 1u) ? (bb & 0xFu) : (bb >> 4)],
-                                              scb[(mb + c) >> a.log2_bs]));
+    const uint32_t xa = nibbles8(wa, pa + c), xb = nibbles8(wb, pb + c);
+    const uint32_t qa = (ma + c) >> a.log2_bs, qb = (mb + c) >> a.log2_bs;
+    // columns left in the block of column c (>= 1); the next block's index is clamped to
+    // the staged ones (a row's 256 values touch at most kOddSeg blocks)
+    const uint32_t ta = (bs_mask + 1u) - ((ma + c) & bs_mask);
+    const uint32_t tb = (bs_mask + 1u) - ((mb + c) & bs_mask);
+    const float sa0 = sca[qa], sa1 = sca[min(qa + 1u, uint32_t(kOddSeg - 1))];
+    const float sb0 = scb[qb], sb1 = scb[min(qb + 1u, uint32_t(kOddSeg - 1))];
+    const int kn = ncol - cc < 8 ? ncol - cc : 8;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (k < kn) {
+        store_one<OUT>(a.out, o, __fmul_rn(s_vcb[(xa >> (4 * k)) & 0xFu],
+                                           uint32_t(k) < ta ? sa0 : sa1));
+        if (has1)
+          store_one<OUT>(a.out, o + 32, __fmul_rn(s_vcb[(xb >> (4 * k)) & 0xFu],
+                                                  uint32_t(k) < tb ? sb0 : sb1));
+      }
+      o += rows;
     }
-    o += rows;
   }
 }
 

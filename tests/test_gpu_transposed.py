@@ -166,6 +166,29 @@ def test_unaligned_output_and_canaries(dq):
                                                                                   kind)))
 
 
+@pytest.mark.parametrize("shift", [1, 2, 4, 8])
+def test_packed_off_sixteen_byte_boundaries(dq, shift):
+    """`packed` 1, 2, 4 or 8 bytes past a 16-byte boundary: the odd-shape kernel takes every
+    shape then (cols % 32 == 0 too), staging whole words when `packed` is 4-byte aligned and
+    single bytes otherwise; W^T stays bit-exact."""
+    for rows, cols in ((200, 160), (333, 777), (130, 96), (64, 4101)):
+        p = gen.make_problem(rows * cols, 64, 256, "nf4", 0.5, 0.0371, seed=rows + cols + shift)
+        t = to_dev(p)
+        buf = torch.zeros(t["packed"].numel() + 16, dtype=torch.uint8, device=DEV)
+        base = (16 - buf.data_ptr() % 16) % 16
+        view = buf[base + shift:base + shift + t["packed"].numel()]
+        view.copy_(t["packed"])
+        assert view.data_ptr() % 16 == shift
+        t2 = dict(t, packed=view)
+        for kind in DT:
+            got = dq.dq4_nested_transposed(t2["packed"], t2["scale_codes"], t2["nested_absmax"],
+                                           t2["scale_codebook"], t2["value_codebook"],
+                                           float(p.offset), rows, cols, p.blocksize,
+                                           p.nested_blocksize, DT[kind])
+            want = oracle.dq4_nested_transposed(p, rows, cols, kind, threads=1)
+            assert np.array_equal(bits(got), want_bits(want)), (rows, cols, kind, shift)
+
+
 def test_staged_path_stays_inside_out(dq):
     """Ragged shapes on the staged kernel (rows and cols not multiples of its tiles, out
     16-byte aligned inside a guarded buffer): W^T is written exactly and nothing around
