@@ -243,18 +243,6 @@ __global__ void __launch_bounds__(kThreads, kMinCtas)
   }
 }
 
-// Staged form for any other shape (cols % 32 != 0 or `packed` not 16-byte aligned): the
-// same 128 x 256 CTA tile and 64 x 64 warp tiles as the staged form.  A row of the tile
-// starts at any nibble and may cross several scale blocks, so the CTA stages, per row, the
-// packed bytes that hold its (at most 256) values, and the scales of the (at most 9) blocks
-// they touch; a lane then decodes rows 2p and 2p + 1 of its warp tile column by column from
-// shared memory, finding each value's byte, nibble and scale from the row's first value
-// index.  Warp w stages rows 16 w .. 16 w + 15: with `packed` 4-byte aligned, the 34
-// aligned words that hold a row's bytes (129 bytes cover 256 nibbles from an odd start,
-// plus up to 3 bytes before them), every load of its rows in flight together; otherwise
-// byte by byte.  Here lane p decodes rows p and p + 32 of its warp tile (not 2p, 2p + 1):
-// with staged rows 35 words apart its 32 lanes read 32 banks, and each store instruction
-// writes 32 consecutive elements of W^T (element stores: rows and columns of any parity).
 // Values n .. n + 7 of a staged row (n counted in value order from the row's first staged
 // byte), one per nibble, value n + k at bits 4k: the two words holding them, each byte's two
 // nibbles swapped (the high nibble is the even value), shifted down to value n.
@@ -265,6 +253,18 @@ __device__ __forceinline__ uint32_t nibbles8(const uint32_t* w, uint32_t n) {
   return uint32_t(v >> (4 * (n & 7u)));
 }
 
+// Staged form for any other shape (cols % 32 != 0 or `packed` not 16-byte aligned): the
+// same 128 x 256 CTA tile and 64 x 64 warp tiles as the staged form.  A row of the tile
+// starts at any nibble and may cross several scale blocks, so the CTA stages, per row, the
+// packed bytes that hold its (at most 256) values, and the scales of the (at most 9) blocks
+// they touch.  Warp w stages rows 16 w .. 16 w + 15: with `packed` 4-byte aligned, the 34
+// aligned words that hold a row's bytes (129 bytes cover 256 nibbles from an odd start,
+// plus up to 3 bytes before them), every load of its rows in flight together; otherwise
+// byte by byte.  Lane p then decodes rows p and p + 32 of its warp tile (not 2p, 2p + 1),
+// eight columns at a time: their nibbles from two staged words (nibbles8) and the scales of
+// the at most two blocks they fall in.  With staged rows 35 words apart its 32 lanes read 32
+// banks, and each store instruction writes 32 consecutive elements of W^T (element stores:
+// rows and columns of any parity).
 constexpr int kOddRowWords = 34;
 constexpr int kOddRowStride = 4 * 35;  // bytes between staged rows (35 words: odd)
 constexpr int kOddSeg = kSC / 32 + 1;  // blocks of >= 32 values a 256-value row run touches
