@@ -104,9 +104,11 @@ int dq4_nested(const uint8_t* packed, const uint8_t* scale_codes, const float* n
  * dq4_nested; rows and cols must be >= 0 and rows * cols must fit in
  * int64 (DQ4_ERR_N otherwise).  Source: issue #21, section "Correctness
  * requirements", which lists the op's transposed-output behaviour among
- * the cases that must stay bitwise identical.  Fastest when cols % 8 == 0
- * and rows * element size % 16 == 0 (other shapes take per-element loads or
- * stores inside the same kernel).
+ * the cases that must stay bitwise identical.  Fastest when cols % 32 == 0
+ * and `packed` is 16-byte aligned, and, for 16-bit output, rows % 4 == 0
+ * with `out` 8-byte aligned (8-byte stores of four rows); any other shape
+ * or alignment takes a second kernel, with the same results, that stages
+ * each row's bytes from any nibble and stores element by element.
  */
 int dq4_nested_transposed(const uint8_t* packed, const uint8_t* scale_codes,
                           const float* nested_absmax, const float* scale_codebook,
