@@ -255,8 +255,9 @@ int64_t dq4_nested_out_prod_workspace_bytes(int64_t rows, int64_t cols, int64_t 
  * Nested 4-bit dequantization fused into a tensor-core GEMM (one launch):
  *   Y = X * W^T       X: M x K (BF16 or FP16, in_dtype), W: the N x K weight
  * whose n = N * K values (row-major) are given as nested 4-bit codes exactly
- * as for dq4_nested; W is decoded tile by tile into shared memory (the same
- * operand bits dq4_nested writes for in_dtype) and never materialised.  Y is
+ * as for dq4_nested; W is decoded stage by stage into tensor memory, where
+ * the MMAs read it as their A operand (the same operand bits dq4_nested
+ * writes for in_dtype), and never materialised in device memory.  Y is
  * M x N row-major in out_dtype; the accumulation is FP32 (tcgen05, sm_103a).
  * Source: "Fuse nested scale reconstruction into SM103 4-bit dequantization"
  * (bitsandbytes issue #21), sections "Problem" and "B300 evidence plan" (the
