@@ -55,6 +55,9 @@ DEFAULT_CELLS = (["C1", "C2a", "C2b", "C3a", "C3b", "C3c", "C3d", "C4a", "C4b", 
                     zip((32, 64, 128, 256, 512, 1024, 2048, 4096),
                         (-1.0, -1e-3, 1e-3, 1.0, -1.0, -1e-3, 1e-3, 1.0))])
 BAR_CELL_PREFIXES = ("C3", "C4", "C5")
+# cells also timed through dq4_nested_transposed (W^T out) in the default run, so the
+# transposed path's record comes from the same run as the headline
+DEFAULT_T_CELLS = ["C1", "C3a", "C3c", "C4a", "C4b", "C5-bs64-off-0.001"]
 N_SETS = 4  # rotating buffer sets of the timed region (each larger than L2)
 E2E_WINDOWS = 5  # the e2e steps are timed in this many windows (median window reported)
 HOLD_CYCLES = 2_000_000  # the pre-region spin: ~1 ms at the 2.07 GHz SM clock
@@ -102,6 +105,9 @@ def parse_args():
                     help="launches timed one by one (own event pair) after the timed region")
     ap.add_argument("--cells", default=",".join(DEFAULT_CELLS),
                     help="cells timed one by one into the `cells` record (empty: none)")
+    ap.add_argument("--t-cells", default=",".join(DEFAULT_T_CELLS),
+                    help="cells timed through the transposed entry point into the "
+                         "`transposed_cells` record (--op nested only; empty: none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-compare", action="store_true")
@@ -503,6 +509,8 @@ def run_ours(args):
     link = link_bound(h2d, d2h, dev) if e2e_ms is not None else None
     names = [c for c in args.cells.split(",") if c]
     cells_rec = time_cells(names, dev, stream, transposed, peak) if names else None
+    t_names = [c for c in args.t_cells.split(",") if c] if not transposed else []
+    t_cells_rec = time_cells(t_names, dev, stream, True, peak) if t_names else None
     ms_per_step = elapsed_ms / K
     value = whole_job_rate(world, K * n, elapsed_ms)
     achieved_gbs = alg_bytes / (avg_launch_ms / 1e3) / 1e9
@@ -558,6 +566,7 @@ def run_ours(args):
             "link_gbs": link, "link_bound_ms": link["both_directions_ms"],
             "frac": link["both_directions_ms"] / (e2e_ms / E)},
         "cells": cells_rec,
+        "transposed_cells": t_cells_rec,
         "gpu_launches": K,
         "timed_region_start": (f"launch queue filled behind a {hold_cycles}-cycle spin kernel "
                                f"(untimed)" if hold_cycles else "idle device"),
